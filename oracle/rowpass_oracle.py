@@ -1,0 +1,334 @@
+"""fp64 CPU oracle for the GRPO / entropy / selective-log-softmax row pass.
+
+TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously correct
+definition of what the CUDA library computes.  Only the test suite, the smoke
+check in ``__graft_entry__.smoke`` and the ``cpu_baseline`` / reference leg of
+``bench.py`` may import it.  The product path (the C-ABI library and its Python
+binding) never calls it, and it shares no code with that path: no kernels, no
+helpers, no constants, no pre- or post-processing.
+
+Sources (the three web pages the method is described on):
+
+* [Liger-bwd]  "LinkedIn Liger-Kernel GRPO Loss Backward optimisation: 50%
+  faster by removing needless work" (write-up of Liger-Kernel PR #1550).
+  Sections used: "Code analysis" (the ``_grpo_loss_bwd_kernel`` and
+  ``_grpo_loss_bwd_kernel_seq`` diffs), "Why it's good", "Review feedback
+  analysis".
+* [Liger-TRL]  "Liger GRPO meets TRL".  Sections used: "2. The core principle
+  that sets GRPO apart from PPO" (group-relative, verifiable rewards),
+  "4. The chunked loss that computes gradients during the forward".
+* [axolotl]    "Axolotl: entropy and selective log-softmax with Triton kernels"
+  (write-up of axolotl PR #3510).  Sections used: "1. benchmarks/bench_entropy.py"
+  (the original eager entropy definition), "2. benchmarks/bench_selective_logsoftmax.py".
+
+Notation (one row r = one token (b, l) of a [B, L, V] logits tensor):
+
+* x_j     raw logit, j in [0, V); decoded exactly from bf16 or fp32 bits
+* T       sampling temperature; z_j = x_j / T
+* lse     log sum_j exp(z_j)
+* p_j     exp(z_j - lse)
+* idx     the sampled token of the row; logp = z_idx - lse
+* H       entropy  -sum_j p_j log p_j  =  sum_j p_j (lse - z_j)
+
+Parity status per function: every public function below is pinned by
+``tests/test_oracle_pins.py`` against brute force (mpmath / long double),
+closed forms, an independent library (scipy), finite differences or an
+invariant.  None is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "decode_logits",
+    "round_to_bf16_bits",
+    "round_to_fp32",
+    "bf16_bits_to_fp64",
+    "log_softmax_rows",
+    "selective_log_softmax",
+    "entropy_from_logits",
+    "grpo_token_terms",
+    "grpo_dlogp",
+    "softmax_gather_grad",
+    "grpo_loss_fwd",
+    "grpo_loss_bwd",
+    "selective_log_softmax_bwd",
+    "per_row",
+]
+
+
+# ---------------------------------------------------------------------------
+# exact conversions
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_fp64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly.
+
+    A bf16 value is the upper half of an IEEE binary32 pattern, so shifting the
+    16 bits into the top of a 32-bit word and reading it as float32 gives the
+    value exactly; float32 -> float64 is exact as well.
+    """
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def decode_logits(raw, dtype: str) -> np.ndarray:
+    """Raw logits as stored ('bf16': uint16 bit patterns, 'fp32': float32) -> float64."""
+    if dtype == "bf16":
+        return bf16_bits_to_fp64(raw)
+    if dtype == "fp32":
+        return np.asarray(raw, dtype=np.float32).astype(np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+_BF16_MANT_BITS = 7          # stored mantissa bits of bf16
+_BF16_MIN_EXP = -126         # exponent of the smallest normal bf16 (same as binary32)
+
+
+def round_to_bf16_bits(v) -> np.ndarray:
+    """Round float64 values to bf16 with round-to-nearest-even, DIRECTLY.
+
+    Rounding through float32 first would round twice; this routine instead
+    scales |v| so that one unit of the bf16 grid at |v| becomes 1.0, rounds to
+    the nearest integer with ties to even (``np.rint``), and scales back.  All
+    scalings are by powers of two and therefore exact.  The grid spacing is
+    2**(e - 7) for a normal value in [2**e, 2**(e+1)) and 2**-133 in the
+    subnormal range.  Results beyond the largest finite bf16 become +-inf, NaN
+    becomes the canonical quiet NaN 0x7FC0 (sign kept), and the sign of zero is
+    kept.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        a = np.abs(v)
+        _, e = np.frexp(a)                      # a = f * 2**e with f in [0.5, 1)
+        # exponent of one grid unit at a: (e - 1) - 7, floored at the subnormal unit
+        unit_exp = np.maximum(e - 1 - _BF16_MANT_BITS, _BF16_MIN_EXP - _BF16_MANT_BITS)
+        q = np.rint(np.ldexp(a, -unit_exp))     # exact scaling, then RNE to an integer
+        r = np.ldexp(q, unit_exp)               # back on the bf16 grid (exact)
+        r32 = np.copysign(r, v).astype(np.float32)  # exact: every bf16 value is a float32 value
+        bits = (r32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(v)
+    if np.any(nan):
+        sign = (np.signbit(v[nan]).astype(np.uint16) << np.uint16(15))
+        bits[nan] = np.uint16(0x7FC0) | sign
+    out[...] = bits
+    return out
+
+
+def round_to_fp32(v) -> np.ndarray:
+    """Round float64 to float32 (IEEE round-to-nearest-even, as numpy's cast does)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(v, dtype=np.float64).astype(np.float32)
+
+
+def per_row(values_per_sequence, L: int) -> np.ndarray:
+    """Broadcast a per-sequence array [B] to the B*L token rows (row r = b*L + l)."""
+    return np.repeat(np.asarray(values_per_sequence, dtype=np.float64), L)
+
+
+# ---------------------------------------------------------------------------
+# row statistics: temperature-scaled log-softmax, selective gather, entropy
+# ---------------------------------------------------------------------------
+
+def log_softmax_rows(x: np.ndarray, T: float):
+    """z = x / T and lse = log sum_j exp(z_j) for every row of x [n, V] (fp64).
+
+    The temperature divides the logits before the softmax; [Liger-bwd], "Code
+    analysis", divides the per-row gradient by the same TEMPERATURE, which is
+    the chain-rule image of this scaling.  The sum is shifted by the row
+    maximum so that exp never overflows; the shift cancels exactly in exact
+    arithmetic.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    z = x / np.float64(T)
+    with np.errstate(invalid="ignore", over="ignore"):
+        m = np.max(z, axis=-1, keepdims=True)
+        s = np.sum(np.exp(z - m), axis=-1, keepdims=True)
+        lse = (m + np.log(s))[..., 0]
+    return z, lse
+
+
+def selective_log_softmax(x: np.ndarray, idx: np.ndarray, T: float):
+    """logp_r = log_softmax(x_r / T)[idx_r]; also returns lse_r.
+
+    [axolotl], "2. benchmarks/bench_selective_logsoftmax.py": the operation
+    evaluates the log-softmax only at the given index of each row.
+    """
+    z, lse = log_softmax_rows(x, T)
+    rows = np.arange(z.shape[0])
+    logp = z[rows, np.asarray(idx, dtype=np.int64)] - lse
+    return logp, lse
+
+
+def entropy_from_logits(x: np.ndarray, T: float = 1.0) -> np.ndarray:
+    """H_r = sum_j p_j (lse - z_j)  (= -sum_j p_j log p_j), per row.
+
+    [axolotl], "1. benchmarks/bench_entropy.py": the original implementation
+    takes ``log_softmax`` of each row and returns minus the sum of
+    ``exp(logps) * logps``.  Written here as sum_j p_j (lse - z_j) so every
+    term is non-negative; the two are the same sum term by term.  The page's
+    eager version has no temperature; T = 1 reproduces it.
+    """
+    z, lse = log_softmax_rows(x, T)
+    with np.errstate(invalid="ignore"):
+        p = np.exp(z - lse[:, None])
+        return np.sum(p * (lse[:, None] - z), axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# GRPO per-token loss and its gradient with respect to logp
+# ---------------------------------------------------------------------------
+
+def grpo_token_terms(logp, old_logp, ref_logp, adv_row, mask, beta, eps_low, eps_high):
+    """Per-token GRPO loss terms from logp (fp64).
+
+    ratio  = exp(logp - old_logp)                       (old_logp None => ratio 1)
+    pg     = -min(ratio * A, clip(ratio, 1 - eps_low, 1 + eps_high) * A)
+    kl     = beta * (exp(ref - logp) - (ref - logp) - 1)   (beta == 0 => 0)
+    loss   = pg + kl, and every output is +0.0 on a masked token.
+
+    The pages print the gradient of the KL term, beta * (1 - exp(ref_logp -
+    logp)) ([Liger-bwd], "Code analysis", both kernel diffs); the value above
+    is the estimator whose derivative with respect to logp is exactly that.
+    The clipped ratio objective is the PPO clip that [Liger-bwd], "Why it's
+    good", names as the source of zero-gradient ("PPO-clipped") tokens; eps is
+    taken asymmetric (eps_low, eps_high).  is_clipped marks tokens where the
+    clipped branch is strictly the smaller one, i.e. where the policy-gradient
+    term has zero gradient.
+    """
+    logp = np.asarray(logp, dtype=np.float64)
+    n = logp.shape[0]
+    A = np.asarray(adv_row, dtype=np.float64)
+    mask = np.ones(n, dtype=bool) if mask is None else (np.asarray(mask) != 0)
+    with np.errstate(over="ignore", invalid="ignore"):
+        if old_logp is None:
+            ratio = np.ones(n)
+        else:
+            ratio = np.exp(logp - np.asarray(old_logp, dtype=np.float64))
+        clipped = np.clip(ratio, 1.0 - eps_low, 1.0 + eps_high)
+        obj_unclipped = ratio * A
+        obj_clipped = clipped * A
+        pg = -np.minimum(obj_unclipped, obj_clipped)
+        is_clipped = obj_clipped < obj_unclipped
+        if beta != 0.0:
+            d = np.asarray(ref_logp, dtype=np.float64) - logp
+            kl = beta * (np.expm1(d) - d)          # exp(d) - d - 1 without cancellation
+        else:
+            kl = np.zeros(n)
+        loss = pg + kl
+    z = np.zeros(n)
+    return {
+        "ratio": ratio,
+        "pg": np.where(mask, pg, z),
+        "kl": np.where(mask, kl, z),
+        "loss": np.where(mask, loss, z),
+        "is_clipped": np.where(mask, is_clipped, False),
+    }
+
+
+def grpo_dlogp(logp, old_logp, ref_logp, adv_row, mask, beta, eps_low, eps_high):
+    """d loss / d logp per token (fp64); 0 on masked tokens.
+
+    Policy-gradient part: -A * ratio where the unclipped branch is the minimum
+    (ties included: inside the clip range both branches have that derivative),
+    0 where the clipped branch is strictly smaller (the clipped ratio is then
+    constant in logp).  KL part: beta * (1 - exp(ref_logp - logp)), the term
+    printed in [Liger-bwd], "Code analysis"; omitted when beta == 0.
+    """
+    logp = np.asarray(logp, dtype=np.float64)
+    n = logp.shape[0]
+    A = np.asarray(adv_row, dtype=np.float64)
+    mask = np.ones(n, dtype=bool) if mask is None else (np.asarray(mask) != 0)
+    with np.errstate(over="ignore", invalid="ignore"):
+        if old_logp is None:
+            ratio = np.ones(n)
+        else:
+            ratio = np.exp(logp - np.asarray(old_logp, dtype=np.float64))
+        clipped = np.clip(ratio, 1.0 - eps_low, 1.0 + eps_high)
+        unclipped_binds = (ratio * A) <= (clipped * A)
+        dpg = np.where(unclipped_binds, -A * ratio, 0.0)
+        if beta != 0.0:
+            dkl = beta * (1.0 - np.exp(np.asarray(ref_logp, dtype=np.float64) - logp))
+        else:
+            dkl = np.zeros(n)
+        dlogp = dpg + dkl
+    return np.where(mask, dlogp, 0.0)
+
+
+def softmax_gather_grad(x: np.ndarray, idx: np.ndarray, g: np.ndarray, T: float) -> np.ndarray:
+    """dlogits_j = g * (1[j == idx] - p_j) per row, with rows where g == 0 all +0.0.
+
+    g is the per-row factor (d loss / d logp) * (upstream) / T: d logp / d x_j
+    = (1[j == idx] - p_j) / T.  A row whose g is exactly zero (either sign) is
+    stored as +0.0 everywhere: [Liger-bwd], "Code analysis", adds an early
+    return that stores 0.0 over the whole DLOGITS row when dlogp == 0.0, and
+    "Why it's good" states outputs and gradients stay identical.
+    """
+    z, lse = log_softmax_rows(x, T)
+    n, V = z.shape
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        p = np.exp(z - lse[:, None])
+        onehot = np.zeros((n, V))
+        rows = np.arange(n)
+        idx = np.asarray(idx, dtype=np.int64)
+        ok = (idx >= 0) & (idx < V)
+        onehot[rows[ok], idx[ok]] = 1.0
+        d = g[:, None] * (onehot - p)
+    d[g == 0.0, :] = 0.0                      # +0.0 bits (also for g == -0.0)
+    return d
+
+
+def grpo_loss_fwd(x, idx, old_logp, ref_logp, adv_row, mask, T, beta, eps_low, eps_high):
+    """Forward of the GRPO row pass for rows x [n, V] (fp64).
+
+    Returns loss, logp, lse, kl, is_clipped and entropy per row.  Masked rows
+    have every output equal to +0.0 (and is_clipped False): their logits are
+    not part of the objective.
+    """
+    n = np.asarray(x).shape[0]
+    mask_b = np.ones(n, dtype=bool) if mask is None else (np.asarray(mask) != 0)
+    logp, lse = selective_log_softmax(x, np.where(mask_b, idx, 0), T)
+    H = entropy_from_logits(x, T)
+    terms = grpo_token_terms(logp, old_logp, ref_logp, adv_row, mask_b, beta, eps_low, eps_high)
+    z = np.zeros(n)
+    return {
+        "loss": terms["loss"],
+        "logp": np.where(mask_b, logp, z),
+        "lse": np.where(mask_b, lse, z),
+        "kl": terms["kl"],
+        "is_clipped": terms["is_clipped"],
+        "entropy": np.where(mask_b, H, z),
+        "ratio": terms["ratio"],
+    }
+
+
+def grpo_loss_bwd(x, idx, old_logp, ref_logp, adv_row, mask, dloss, T, beta, eps_low, eps_high):
+    """Backward of sum_r dloss_r * loss_r with respect to the logits (fp64).
+
+    g_r = dlogp_r * dloss_r / T ([Liger-bwd], "Code analysis":
+    ``dlogp * dloss / TEMPERATURE``); dlogits_r = g_r * (onehot(idx_r) - p_r);
+    rows with g_r == 0 are +0.0.  Returns (dlogits, g).
+    """
+    n = np.asarray(x).shape[0]
+    mask_b = np.ones(n, dtype=bool) if mask is None else (np.asarray(mask) != 0)
+    safe_idx = np.where(mask_b, idx, 0)
+    logp, _ = selective_log_softmax(x, safe_idx, T)
+    dlogp = grpo_dlogp(logp, old_logp, ref_logp, adv_row, mask_b, beta, eps_low, eps_high)
+    g = dlogp * np.asarray(dloss, dtype=np.float64) / np.float64(T)
+    g = np.where(mask_b, g, 0.0)
+    return softmax_gather_grad(x, safe_idx, g, T), g
+
+
+def selective_log_softmax_bwd(x, idx, dlogp_upstream, T):
+    """Gradient of sum_r u_r * logp_r with respect to the logits (fp64).
+
+    [axolotl], "2. benchmarks/bench_selective_logsoftmax.py": the backward of
+    the selective log-softmax.  g_r = u_r / T; rows with g_r == 0 are +0.0.
+    Returns (dlogits, g).
+    """
+    g = np.asarray(dlogp_upstream, dtype=np.float64) / np.float64(T)
+    return softmax_gather_grad(x, idx, g, T), g
