@@ -1,0 +1,647 @@
+#!/usr/bin/env python3
+"""Benchmark of the GRPO row pass on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic logits:
+
+* GRPO workloads (default ``grpo_b4_l512_v32000``, the GRPO backward workload of the
+  Liger-Kernel GRPO Loss Backward write-up: (B, L, V, zero-grad%) = (4, 512, 32000, 50%)):
+  ``grpo_loss_fwd`` (loss, logp, lse, kl, is_clipped, entropy) then ``grpo_loss_bwd``.
+* ``entropy_slsm_b16_l4096_v32000``: ``entropy_from_logits``, ``selective_log_softmax_fwd``
+  and ``selective_log_softmax_bwd``.
+
+The metric is algorithmic HBM bytes per second (the minimal bytes of the step: each
+unmasked row's logits read once by the forward; each backward row with a non-zero
+factor read once and written once; each zero row written once; plus the per-row
+scalars), and rows per second.  Inputs are resident in HBM when the timed region
+starts; L2 is flushed (a 256 MB write) before every timed step and the flush is not
+timed.  ``e2e`` repeats the measurement through the public Python API with the inputs
+in pinned host memory and the outputs copied back, copies inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling; no collective on the
+data path) and rank 0 prints one JSON line with the aggregate over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rl_fine_tuning_pass_gb300 import binding as rp  # noqa: E402
+from rl_fine_tuning_pass_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GRPO fwd+bwd logits GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+GRPO_WORKLOADS = ("grpo_b4_l512_v32000", "grpo_qwen3_b16_l1024_v151936", "sweep_b16_l4096_v151936")
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rl_fine_tuning_pass_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            parts = [p for p in vis.split(",") if p.strip()]
+            self.sel = parts[device_index] if device_index < len(parts) else str(device_index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------
+# workloads: prebuilt C-ABI calls with preallocated outputs
+# ---------------------------------------------------------------------------
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def grpo_row_bytes(spec, live, zero_g, has_mask, has_old, has_ref):
+    """Minimal bytes per row of the GRPO forward and backward (numpy bool arrays in,
+    int arrays out).  Forward: an unmasked row reads its V logits, idx, old/ref; every
+    row reads its mask byte and writes loss, logp, lse, kl, entropy (4 B each) and
+    is_clipped (1 B).  Backward: every row reads its mask byte and writes V dlogits; an
+    unmasked row reads logp, old, ref, dloss; a row with a non-zero factor also reads
+    idx, lse and its V logits.  The per-sequence advantages (4 B each) are left out."""
+    V, s = spec.V, spec.elem_size
+    live = np.asarray(live, bool)
+    zero_g = np.asarray(zero_g, bool)
+    m = 1 if has_mask else 0
+    o = 4 if has_old else 0
+    r = 4 if has_ref else 0
+    fwd = m + 21 + live * (V * s + 8 + o + r)
+    bwd = m + V * s + live * (4 + o + r + 4) + (~zero_g) * (8 + 4 + V * s)
+    return fwd.astype(np.int64), bwd.astype(np.int64)
+
+
+SLSM_ROW_BYTES = {"entropy_from_logits": lambda V, s: V * s + 4,
+                  "selective_log_softmax_fwd": lambda V, s: V * s + 8 + 8,
+                  "selective_log_softmax_bwd": lambda V, s: 2 * V * s + 8 + 4 + 4}
+
+
+class GrpoStep:
+    """grpo_loss_fwd (+entropy, kl, is_clipped) then grpo_loss_bwd over one batch."""
+
+    def __init__(self, spec, seed, device, inputs=None):
+        self.spec = spec
+        lib = rp.load_library()
+        inp = inputs if inputs is not None else W.generate(spec, seed, device=device)
+        self.inp = inp
+        T, beta = spec.T, spec.beta
+        R = spec.rows
+        # old/ref placed near the current logp with our own forward (setup, not timed)
+        logp0, _ = rp.selective_log_softmax_fwd(inp.logits, inp.idx, T=T)
+        self.old = (logp0 + inp.old_offset).contiguous() if inp.old_offset is not None else None
+        self.ref = (logp0 + inp.ref_offset).contiguous() if (inp.ref_offset is not None and beta != 0) else None
+        f32 = dict(dtype=torch.float32, device=device)
+        self.out = {k: torch.empty(R, **f32) for k in ("loss", "logp", "lse", "kl", "entropy")}
+        self.out["is_clipped"] = torch.empty(R, dtype=torch.uint8, device=device)
+        self.dlogits = torch.empty(inp.logits.shape, dtype=inp.logits.dtype, device=device)
+        self.x_desc = rp.rows_of(inp.logits)
+        self.dx_desc = rp.rows_of(self.dlogits)
+        self.stream = torch.cuda.current_stream(device).cuda_stream
+        o = self.out
+        self._fwd = lib.grpo_loss_fwd
+        self._bwd = lib.grpo_loss_bwd
+        self.fwd_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(self.old), _p(self.ref), _p(inp.adv),
+                         _p(inp.mask), T, beta, spec.eps_low, spec.eps_high, _p(o["loss"]), _p(o["logp"]),
+                         _p(o["lse"]), _p(o["kl"]), _p(o["is_clipped"]), _p(o["entropy"]), None, self.stream)
+        self.bwd_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(self.old), _p(self.ref), _p(inp.adv),
+                         _p(inp.mask), _p(inp.dloss), _p(o["logp"]), _p(o["lse"]), T, beta, spec.eps_low,
+                         spec.eps_high, ctypes.byref(self.dx_desc), None, self.stream)
+        self.kernels = [("grpo_loss_fwd", self.fwd), ("grpo_loss_bwd", self.bwd)]
+
+    def fwd(self):
+        st = self._fwd(*self.fwd_args)
+        if st:
+            raise rp.GrpoError("grpo_loss_fwd", st)
+
+    def bwd(self):
+        st = self._bwd(*self.bwd_args)
+        if st:
+            raise rp.GrpoError("grpo_loss_bwd", st)
+
+    def account(self):
+        """Minimal bytes per launch from the row classes of this batch (after one step):
+        masked rows, rows whose backward factor is exactly zero, and the rest.  The zero
+        factor is read off the inputs and the forward's is_clipped output: with beta == 0
+        a row's factor is zero iff it is masked, its dloss is 0, A == 0, or clipping binds."""
+        spec, inp = self.spec, self.inp
+        R = spec.rows
+        mask = torch.ones(R, dtype=torch.bool, device=inp.idx.device) if inp.mask is None else inp.mask.bool()
+        adv_row = inp.adv.repeat_interleave(spec.L)
+        zero = ~mask | (inp.dloss == 0)
+        if spec.beta == 0:
+            zero = zero | (adv_row == 0) | self.out["is_clipped"].bool()
+        live, zero = mask.cpu().numpy(), zero.cpu().numpy()
+        fwd, bwd = grpo_row_bytes(spec, live, zero, inp.mask is not None, self.old is not None, self.ref is not None)
+        n_zero = int(zero.sum())
+        self.classes = {"rows": R, "masked": int(R - live.sum()), "zero_grad_rows": n_zero,
+                        "zero_grad_frac": round(n_zero / R, 4)}
+        return {"grpo_loss_fwd": int(fwd.sum()), "grpo_loss_bwd": int(bwd.sum())}
+
+    # -- end-to-end through the public API with host buffers --------------------
+    def e2e_setup(self):
+        inp = self.inp
+        pin = lambda t: None if t is None else t.detach().cpu().pin_memory()
+        self.h = {"logits": pin(inp.logits.contiguous()), "idx": pin(inp.idx), "adv": pin(inp.adv),
+                  "mask": pin(inp.mask), "dloss": pin(inp.dloss), "old": pin(self.old), "ref": pin(self.ref)}
+        self.h_dl = torch.empty(self.dlogits.shape, dtype=self.dlogits.dtype).pin_memory()
+        self.h_loss = torch.empty(self.spec.rows, dtype=torch.float32).pin_memory()
+        self.d_logits = torch.empty(inp.logits.shape, dtype=inp.logits.dtype, device=inp.logits.device)
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h.values() if t is not None)
+        self.d2h = self.h_dl.numel() * self.h_dl.element_size() + self.h_loss.numel() * 4
+
+    def e2e_step(self):
+        spec, dev = self.spec, self.d_logits.device
+        h = self.h
+        up = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        self.d_logits.copy_(h["logits"], non_blocking=True)
+        idx, adv, mask, dloss, old, ref = up(h["idx"]), up(h["adv"]), up(h["mask"]), up(h["dloss"]), up(h["old"]), up(h["ref"])
+        f = rp.grpo_loss_fwd(self.d_logits, idx, adv, T=spec.T, beta=spec.beta, eps_low=spec.eps_low,
+                             eps_high=spec.eps_high, old_logp=old, ref_logp=ref, mask=mask, with_entropy=True)
+        dl = rp.grpo_loss_bwd(self.d_logits, idx, adv, dloss, f["logp"], f["lse"], T=spec.T, beta=spec.beta,
+                              eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=old, ref_logp=ref,
+                              mask=mask, dlogits=self.dlogits)
+        self.h_dl.copy_(dl, non_blocking=True)
+        self.h_loss.copy_(f["loss"], non_blocking=True)
+
+
+class EntropySlsmStep:
+    """entropy_from_logits, selective_log_softmax_fwd, selective_log_softmax_bwd."""
+
+    def __init__(self, spec, seed, device):
+        self.spec = spec
+        lib = rp.load_library()
+        inp = W.generate(spec, seed, device=device)
+        self.inp = inp
+        R = spec.rows
+        f32 = dict(dtype=torch.float32, device=device)
+        self.H, self.logp, self.lse = torch.empty(R, **f32), torch.empty(R, **f32), torch.empty(R, **f32)
+        self.dlogits = torch.empty(inp.logits.shape, dtype=inp.logits.dtype, device=device)
+        self.x_desc, self.dx_desc = rp.rows_of(inp.logits), rp.rows_of(self.dlogits)
+        self.stream = torch.cuda.current_stream(device).cuda_stream
+        T = spec.T
+        self._e, self._f, self._b = lib.entropy_from_logits, lib.selective_log_softmax_fwd, lib.selective_log_softmax_bwd
+        self.e_args = (ctypes.byref(self.x_desc), T, _p(self.H), self.stream)
+        self.f_args = (ctypes.byref(self.x_desc), _p(inp.idx), T, _p(self.logp), _p(self.lse), None, self.stream)
+        self.b_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(inp.upstream), _p(self.lse), T,
+                       ctypes.byref(self.dx_desc), None, self.stream)
+        self.kernels = [("entropy_from_logits", lambda: self._call(self._e, self.e_args)),
+                        ("selective_log_softmax_fwd", lambda: self._call(self._f, self.f_args)),
+                        ("selective_log_softmax_bwd", lambda: self._call(self._b, self.b_args))]
+
+    @staticmethod
+    def _call(fn, args):
+        st = fn(*args)
+        if st:
+            raise rp.GrpoError(fn.__name__, st)
+
+    def account(self):
+        spec = self.spec
+        R, V, s = spec.rows, spec.V, spec.elem_size
+        self.classes = {"rows": R, "zero_grad_rows": 0, "strided": spec.strided}
+        return {k: R * f(V, s) for k, f in SLSM_ROW_BYTES.items()}
+
+    def e2e_setup(self):
+        inp = self.inp
+        self.h = {"logits": inp.logits.contiguous().cpu().pin_memory(), "idx": inp.idx.cpu().pin_memory(),
+                  "up": inp.upstream.cpu().pin_memory()}
+        self.h_dl = torch.empty(self.dlogits.shape, dtype=self.dlogits.dtype).pin_memory()
+        self.h_out = torch.empty(3 * self.spec.rows, dtype=torch.float32).pin_memory()
+        self.d_logits = torch.empty(inp.logits.shape, dtype=inp.logits.dtype, device=inp.logits.device)
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h.values())
+        self.d2h = self.h_dl.numel() * self.h_dl.element_size() + self.h_out.numel() * 4
+
+    def e2e_step(self):
+        dev, T, R = self.d_logits.device, self.spec.T, self.spec.rows
+        self.d_logits.copy_(self.h["logits"], non_blocking=True)
+        idx = self.h["idx"].to(dev, non_blocking=True)
+        up = self.h["up"].to(dev, non_blocking=True)
+        H = rp.entropy_from_logits(self.d_logits, T=T)
+        lp, lse = rp.selective_log_softmax_fwd(self.d_logits, idx, T=T)
+        dl = rp.selective_log_softmax_bwd(self.d_logits, idx, up, lse, T=T, dlogits=self.dlogits)
+        self.h_dl.copy_(dl, non_blocking=True)
+        self.h_out[:R].copy_(H, non_blocking=True)
+        self.h_out[R:2 * R].copy_(lp, non_blocking=True)
+        self.h_out[2 * R:].copy_(lse, non_blocking=True)
+
+
+def make_spec(args):
+    over = {}
+    if args.beta is not None:
+        over["beta"] = args.beta
+    if args.zero_seqs is not None:
+        over["zero_adv_seqs"] = args.zero_seqs
+    if args.strided:
+        over["strided"] = True
+    return W.get(args.workload, **over)
+
+
+def make_step(spec, seed, device):
+    if spec.name.startswith("entropy_slsm"):
+        return EntropySlsmStep(spec, seed, device)
+    return GrpoStep(spec, seed, device)
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+
+def timed_run(step, K, Wm, flush_buf, world):
+    """Warm up, then time exactly K steps with CUDA events around every kernel (L2 flushed
+    before each step, outside the events).  Returns per-kernel times [K] in ms and the wall
+    time of the barrier-bracketed region."""
+    names = [n for n, _ in step.kernels]
+    for i in range(Wm):
+        flush_buf.fill_(i & 0x7F)
+        for _, fn in step.kernels:
+            fn()
+    torch.cuda.synchronize()
+    nk = len(step.kernels)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush_buf.fill_((i + 1) & 0x7F)
+        e = ev[i]
+        e[0].record()
+        for k, (_, fn) in enumerate(step.kernels):
+            fn()
+            e[k + 1].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    per = {n: [ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(K)] for k, n in enumerate(names)}
+    return per, wall
+
+
+def e2e_run(step, K, Wm):
+    step.e2e_setup()
+    for _ in range(max(1, Wm)):
+        step.e2e_step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(K):
+        step.e2e_step()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / K
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(step, rows):
+    """Host copies of one sample of the workload's rows, ready for the oracle."""
+    import oracle
+    spec, inp = step.spec, step.inp
+    r = torch.as_tensor(rows, dtype=torch.int64, device=inp.idx.device)
+    x = inp.logits[r // spec.L, r % spec.L].cpu()
+    xb = oracle.bf16_bits_to_fp64(x.view(torch.int16).numpy().view(np.uint16)) if x.dtype == torch.bfloat16 \
+        else x.double().numpy()
+    g = lambda t: None if t is None else t[r].double().cpu().numpy()
+    smp = {"x": xb, "idx": inp.idx[r].cpu().numpy(), "adv": oracle.per_row(inp.adv.cpu().numpy(), spec.L)[rows],
+           "mask": None if inp.mask is None else inp.mask[r].cpu().numpy()}
+    if isinstance(step, GrpoStep):
+        smp.update(old=g(step.old), ref=g(step.ref), dloss=g(inp.dloss))
+    else:
+        smp.update(up=g(inp.upstream))
+    return smp
+
+
+def oracle_step(spec, smp):
+    import oracle
+    if spec.name.startswith("entropy_slsm"):
+        oracle.entropy_from_logits(smp["x"], spec.T)
+        oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
+        d, _ = oracle.selective_log_softmax_bwd(smp["x"], smp["idx"], smp["up"], spec.T)
+    else:
+        oracle.grpo_loss_fwd(smp["x"], smp["idx"], smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.T,
+                             spec.beta, spec.eps_low, spec.eps_high)
+        d, _ = oracle.grpo_loss_bwd(smp["x"], smp["idx"], smp["old"], smp["ref"], smp["adv"], smp["mask"],
+                                    smp["dloss"], spec.T, spec.beta, spec.eps_low, spec.eps_high)
+    if spec.dtype == "bf16":
+        oracle.round_to_bf16_bits(d)
+    else:
+        oracle.round_to_fp32(d)
+
+
+def cpu_baseline(step, bytes_per_row, budget_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of rows of this workload."""
+    spec = step.spec
+    probe = W.sample_rows(spec.rows, 16, 7)
+    smp = oracle_sample(step, probe)
+    t = time.perf_counter()
+    oracle_step(spec, smp)
+    per_row = (time.perf_counter() - t) / len(probe)
+    n = int(max(16, min(spec.rows, budget_s / max(per_row, 1e-9))))
+    rows = W.sample_rows(spec.rows, n, 11)
+    smp = oracle_sample(step, rows)
+    t = time.perf_counter()
+    oracle_step(spec, smp)
+    dt = time.perf_counter() - t
+    return {"value": round(bytes_per_row * len(rows) / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "rows_per_s": round(len(rows) / dt, 2),
+            "sample": f"{len(rows)} of {spec.rows} rows of {spec.name} (fwd+bwd, fp64 numpy, one thread), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 2 s of steps)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="grpo_b4_l512_v32000",
+                    choices=list(GRPO_WORKLOADS) + ["entropy_slsm_b16_l4096_v32000"])
+    ap.add_argument("--beta", type=float, default=None)
+    ap.add_argument("--zero-seqs", type=int, default=None)
+    ap.add_argument("--strided", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def base_line(args, spec, world):
+    return {"metric": METRIC, "unit": "GB/s", "n_gpus": world, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "data": "synthetic",
+            "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "V": spec.V, "T": spec.T,
+                       "beta": spec.beta, "eps_low": spec.eps_low, "eps_high": spec.eps_high,
+                       "logits_dtype": spec.dtype, "strided": spec.strided,
+                       "l2": "flushed before every timed step (256 MB write, not timed)",
+                       "parallelism": f"{world} independent batch(es), one per GPU"}}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores only: inputs drawn on the CPU
+    from the same generators, old/ref placed with the oracle's own logp, and each step
+    one bounded sample of the workload's rows (fwd + bwd)."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import oracle  # the one other place bench.py runs the oracle
+    spec = make_spec(args)
+    inp = W.generate(spec, args.seed, device="cpu")
+    R, L = spec.rows, spec.L
+    grpo = not spec.name.startswith("entropy_slsm")
+    adv_rows = oracle.per_row(inp.adv.numpy(), L)
+
+    def sample(rows):
+        x = inp.logits.reshape(-1, spec.V) if not spec.strided else inp.logits[rows // L, rows % L]
+        x = x[rows] if not spec.strided else x
+        xd = oracle.bf16_bits_to_fp64(x.view(torch.int16).numpy().view(np.uint16)) if x.dtype == torch.bfloat16 \
+            else x.double().numpy()
+        smp = {"x": xd, "idx": inp.idx.numpy()[rows], "adv": adv_rows[rows],
+               "mask": None if inp.mask is None else inp.mask.numpy()[rows]}
+        if grpo:
+            lp, _ = oracle.selective_log_softmax(xd, smp["idx"], spec.T)
+            add = lambda off: None if off is None else oracle.round_to_fp32(lp + off.numpy()[rows]).astype(np.float64)
+            smp["old"] = add(inp.old_offset)
+            smp["ref"] = add(inp.ref_offset) if spec.beta != 0 else None
+            smp["dloss"] = inp.dloss.numpy().astype(np.float64)[rows]
+        else:
+            smp["up"] = inp.upstream.numpy().astype(np.float64)[rows]
+        return smp
+
+    def sample_bytes(smp):
+        n = len(smp["idx"])
+        if not grpo:
+            return n * sum(f(spec.V, spec.elem_size) for f in SLSM_ROW_BYTES.values())
+        live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
+        lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
+        g = oracle.grpo_dlogp(lp, smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.beta, spec.eps_low,
+                              spec.eps_high) * smp["dloss"]
+        f, b = grpo_row_bytes(spec, live, g == 0, smp["mask"] is not None, smp["old"] is not None,
+                              smp["ref"] is not None)
+        return int(f.sum() + b.sum())
+
+    K = args.steps if args.steps is not None else 10
+    Wm = args.warmup
+    probe = sample(W.sample_rows(R, 8, 3))
+    t = time.perf_counter()
+    oracle_step(spec, probe)
+    per_row = (time.perf_counter() - t) / 8
+    rows_per_step = int(max(1, min(R, 150.0 / max(1, K + Wm) / max(per_row, 1e-9))))
+    times, nbytes = [], 0
+    for i in range(Wm + K):
+        smp = sample(W.sample_rows(R, rows_per_step, 100 + i))
+        t = time.perf_counter()
+        oracle_step(spec, smp)
+        dt = time.perf_counter() - t
+        if i >= Wm:
+            times.append(dt)
+            nbytes += sample_bytes(smp)
+    total = sum(times)
+    value = nbytes / total / 1e9
+    line = base_line(args, spec, 1)
+    line.update({"impl": "reference", "value": round(value, 6), "steps": K, "warmup": Wm,
+                 "ms_per_step": round(1e3 * total / K, 3), "dtype": "f64",
+                 "rows_per_s": round(rows_per_step * K / total, 2)})
+    sample_txt = f"{rows_per_step} of {R} rows of {spec.name} per step (fwd+bwd, fp64 numpy, one thread)"
+    line["cpu_baseline"] = {"value": line["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": sample_txt}
+    line["e2e"] = {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU: the row pass has no CPU path")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    spec = make_spec(args)
+    step = make_step(spec, args.seed + rank, device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    # one untimed step to classify rows, then calibrate the step count
+    for _, fn in step.kernels:
+        fn()
+    torch.cuda.synchronize()
+    per_launch = step.account()
+    step_bytes = sum(per_launch.values())
+    if args.steps is None:
+        probe, _ = timed_run(step, 5, 1, flush_buf, 1)
+        step_ms = sum(statistics.mean(v) for v in probe.values()) + 0.05
+        K = int(min(20000, max(20, math.ceil(2000.0 / step_ms))))
+    else:
+        K = args.steps
+    Wm = max(3, args.warmup)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    per, wall = timed_run(step, K, Wm, flush_buf, world)
+    clk = clocks.stop()
+
+    kern_ms = {n: statistics.mean(v) for n, v in per.items()}
+    step_ms = sum(kern_ms.values())
+    total_ms = sum(sum(v) for v in per.values())
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
+    rows_per_s = spec.rows * K * world / (total_ms * 1e-3)
+
+    peak, peak_src = load_peaks()
+    dom = max(kern_ms, key=kern_ms.get)
+    achieved = per_launch[dom] / (kern_ms[dom] * 1e-3) / 1e9
+    traffic = measured_traffic(dom, spec.name)
+
+    e2e = None
+    if not args.no_e2e:
+        Ke = min(K, max(5, int(1500.0 / max(step_ms, 1e-3) / 10)), 200)
+        ms = e2e_run(step, Ke, 2)
+        e2e_val = step_bytes * world / (ms * 1e-3) / 1e9
+        e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": int(step.h2d),
+               "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4), "steps": Ke,
+               "path": "public Python API, pinned host inputs, outputs copied back"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(step, step_bytes / spec.rows)
+
+    if rank == 0:
+        line = base_line(args, spec, world)
+        line["config"].update(step.classes)
+        line.update({
+            "value": round(value, 2), "steps": K, "warmup": Wm, "ms_per_step": round(step_ms, 5),
+            "dtype": spec.dtype, "rows_per_s": round(rows_per_s, 1),
+            "hbm_frac": round(value / world / peak, 4),
+            "bytes_per_step": int(step_bytes),
+            "kernels": {n: {"ms": round(kern_ms[n], 5), "bytes": int(per_launch[n]),
+                            "GB_per_s": round(per_launch[n] / (kern_ms[n] * 1e-3) / 1e9, 1)} for n in kern_ms},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": int(per_launch[dom])},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": len(step.kernels) * K,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "timed_wall_s": round(wall, 3), "kernel_source": kernel_source_hash(),
+        })
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,200 @@
+/*
+ * grpo_rowpass.h -- C ABI of the GB300 (sm_103a) row pass over LM-head logits.
+ *
+ * One row r = one token (b, l) of a [B, L, V] logits tensor, r = b*L + l.  With
+ * z_j = x_j / T (T the sampling temperature):
+ *
+ *   lse_r   = log sum_j exp(z_j)
+ *   logp_r  = z_idx - lse_r                  (selective log-softmax)
+ *   H_r     = sum_j p_j (lse_r - z_j)        (entropy, p_j = exp(z_j - lse_r))
+ *   ratio_r = exp(logp_r - old_logp_r)
+ *   pg_r    = -min(ratio_r * A_b, clip(ratio_r, 1 - eps_low, 1 + eps_high) * A_b)
+ *   kl_r    = beta * (exp(d_r) - d_r - 1),   d_r = ref_logp_r - logp_r
+ *   loss_r  = (pg_r + kl_r) on unmasked tokens, +0.0 on masked ones
+ *
+ * and the backward  dlogits_rj = g_r * (1[j == idx_r] - p_j)  with one scalar g_r
+ * per row.  A row whose g_r is exactly zero is stored as +0.0 and its logits are
+ * never read.
+ *
+ * Sources (web pages the method is described on):
+ *   [Liger-bwd]  "LinkedIn Liger-Kernel GRPO Loss Backward optimisation" (write-up of
+ *                Liger-Kernel PR #1550), sections "Code analysis" and "Why it's good".
+ *   [axolotl]    "Axolotl: entropy and selective log-softmax with Triton kernels"
+ *                (write-up of axolotl PR #3510), sections "1. benchmarks/bench_entropy.py",
+ *                "2. benchmarks/bench_selective_logsoftmax.py", "Why it's good".
+ *   [Liger-TRL]  "Liger GRPO meets TRL", sections 2 and 4.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer (cudaMalloc'd, or any memory the GPU
+ *   can address) owned by the caller.  The library allocates nothing, keeps no state
+ *   between calls, and launches its kernels asynchronously on `stream` (NULL = the
+ *   legacy default stream).  Results are visible once the stream is synchronised.
+ * - Per-row arrays ([B*L]) are contiguous, indexed by r = b*L + l.  Per-sequence
+ *   arrays ([B]) are contiguous.  float arrays need 4-byte, int64 arrays 8-byte
+ *   alignment.
+ * - The logits are described by grpo_rows: element (b, l, j) lives at
+ *   ptr + b*stride_b + l*stride_l + j (strides in ELEMENTS, vocab stride 1), so a
+ *   non-contiguous view such as logits[:, :-1, :] of a [B, L+1, V] tensor is read in
+ *   place, with no copy.  Rows may start at any element boundary; rows whose start is
+ *   16-byte aligned take the fastest path.
+ * - Return value: GRPO_OK, or an error found on the host BEFORE any launch
+ *   (GRPO_ERR_INVALID_ARG / GRPO_ERR_UNSUPPORTED; nothing is written), or
+ *   GRPO_ERR_CUDA when the launch itself failed (cudaGetLastError after the launch).
+ *   B*L == 0 is valid and launches nothing.
+ * - `dev_err` (nullable) is a device int32 word the kernels OR error bits into
+ *   (GRPO_DEVERR_*).  The library never clears it and never traps: a row with an
+ *   out-of-range idx gets NaN in its idx-dependent outputs and the bit is set.
+ * - NaN / Inf logits propagate to that row's outputs the way the definitions above
+ *   propagate them; nothing faults.  Finite logits are supported up to |x / T| < 2^30;
+ *   beyond that the fp32 exponent offset can overflow and a row may read Inf/NaN.
+ *   The saved lse is fp32, so the backward's bf16 outputs are within 1 ulp of the
+ *   exact result while |lse| < 2^15.
+ */
+#ifndef GRPO_ROWPASS_H_
+#define GRPO_ROWPASS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* grpo_stream_t;
+
+typedef enum {
+  GRPO_OK = 0,
+  GRPO_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, bad size, stride, scalar or aliasing */
+  GRPO_ERR_UNSUPPORTED = 2, /* valid arguments this build does not handle (e.g. B*L >= 2^31) */
+  GRPO_ERR_CUDA = 3         /* the kernel launch failed */
+} grpo_status;
+
+typedef enum { GRPO_FP32 = 0, GRPO_BF16 = 1 } grpo_dtype;
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define GRPO_DEVERR_IDX_OUT_OF_RANGE 1
+
+/* A [B, L, V] logits (or dlogits) tensor: ptr + b*stride_b + l*stride_l + j. */
+typedef struct {
+  void* ptr;         /* device pointer, aligned to the element size */
+  int32_t dtype;     /* grpo_dtype */
+  int32_t reserved;  /* must be 0 */
+  int64_t B, L, V;   /* sequences, tokens per sequence, vocabulary (V >= 1) */
+  int64_t stride_b;  /* elements between (b, l, 0) and (b+1, l, 0); >= 0 */
+  int64_t stride_l;  /* elements between (b, l, 0) and (b, l+1, 0); >= 0 */
+} grpo_rows;
+
+/*
+ * grpo_loss_fwd -- forward of the GRPO per-token loss, one pass over each unmasked row.
+ *
+ * Defined by: the clipped-ratio objective whose zero-gradient ("PPO-clipped") tokens
+ * [Liger-bwd] "Why it's good" names, the k3 KL term whose gradient
+ * beta*(1 - exp(ref_logp - logp)) [Liger-bwd] "Code analysis" prints, and the
+ * temperature division of the same section; the entropy is the definition in
+ * [axolotl] "1. benchmarks/bench_entropy.py".
+ *
+ *   logits      [B, L, V] bf16 or fp32 (read only)
+ *   idx         [B*L] int64 sampled token per row; read only on unmasked rows
+ *   old_logp    [B*L] fp32, or NULL meaning old_logp == logp (ratio 1)
+ *   ref_logp    [B*L] fp32; may be NULL only when beta == 0 (then never read)
+ *   adv         [B]   fp32 advantage per sequence
+ *   mask        [B*L] uint8 completion mask (0 = padding), or NULL = every token counts
+ *   T > 0 finite; beta >= 0 finite; 0 <= eps_low <= 1; eps_high >= 0 finite
+ *   loss, logp, lse   [B*L] fp32 outputs (required); lse is what grpo_loss_bwd needs
+ *   kl, entropy       [B*L] fp32 outputs, or NULL to skip
+ *   is_clipped        [B*L] uint8 output (1 where the clipped branch is strictly the
+ *                     smaller one, so the policy-gradient term has zero gradient), or NULL
+ *   dev_err           nullable device int32 error word
+ *
+ * Masked rows write +0.0 to every output (0 to is_clipped) and read no logits.  With
+ * beta == 0 the KL term is never evaluated (kl = +0.0).  An unmasked row whose idx is
+ * outside [0, V) writes NaN to loss, logp and kl (lse and entropy stay valid) and sets
+ * GRPO_DEVERR_IDX_OUT_OF_RANGE.
+ */
+grpo_status grpo_loss_fwd(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                          const float* ref_logp, const float* adv, const uint8_t* mask, float T,
+                          float beta, float eps_low, float eps_high, float* loss, float* logp,
+                          float* lse, float* kl, uint8_t* is_clipped, float* entropy, int32_t* dev_err,
+                          grpo_stream_t stream);
+
+/*
+ * grpo_loss_bwd -- backward of sum_r dloss_r * loss_r with respect to the logits.
+ *
+ * Defined by [Liger-bwd] "Code analysis" (_grpo_loss_bwd_kernel): per row,
+ * dlogp = dpg/dlogp + beta*(1 - exp(ref_logp - logp)), scaled by dloss and divided by
+ * the temperature, then spread over the row as g * (1[j == idx] - p_j); when that
+ * scaled dlogp is exactly 0.0 the row is filled with 0.0 and nothing else is done.
+ * dpg/dlogp = -A * ratio where ratio*A <= clip(ratio)*A, else 0 (clipping binds).
+ *
+ *   logits, idx, old_logp, ref_logp, adv, mask, T, beta, eps_low, eps_high: as in
+ *               grpo_loss_fwd (same values)
+ *   dloss       [B*L] fp32 upstream gradient of each token's loss
+ *   logp, lse   [B*L] fp32 as written by grpo_loss_fwd for the same inputs
+ *   dlogits     [B, L, V] output, same dtype and B, L, V as logits, its own strides
+ *               (rows must not overlap).  It may alias logits exactly (same ptr and
+ *               strides) for an in-place backward; any other overlap is rejected.
+ *
+ * Rows where g == 0.0 (masked tokens; zero advantage or binding clip with beta == 0;
+ * dloss == 0) are written as +0.0 without reading logits, idx or lse.  Other rows are
+ * read once and written once; bf16 outputs are rounded to nearest even.  An idx
+ * outside [0, V) on a row with g != 0 fills that row with NaN and sets the error bit.
+ */
+grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                          const float* ref_logp, const float* adv, const uint8_t* mask,
+                          const float* dloss, const float* logp, const float* lse, float T,
+                          float beta, float eps_low, float eps_high, const grpo_rows* dlogits,
+                          int32_t* dev_err, grpo_stream_t stream);
+
+/*
+ * entropy_from_logits -- H_r = sum_j p_j (lse_r - z_j) per row, one fused pass.
+ *
+ * Defined by [axolotl] "1. benchmarks/bench_entropy.py": the original takes
+ * log_softmax of each row and sums -exp(logps)*logps; the fused kernel the same page
+ * describes reads strided logits in place.  T = 1 reproduces the page's definition.
+ *
+ *   logits   [B, L, V] bf16 or fp32;  T > 0 finite;  entropy [B*L] fp32 output
+ */
+grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy,
+                                grpo_stream_t stream);
+
+/*
+ * selective_log_softmax_fwd -- logp_r = log_softmax(x_r / T)[idx_r], and lse_r.
+ *
+ * Defined by [axolotl] "2. benchmarks/bench_selective_logsoftmax.py" (the log-softmax
+ * evaluated only at the given index of each row).
+ *
+ *   logits [B, L, V];  idx [B*L] int64;  T > 0 finite
+ *   logp, lse [B*L] fp32 outputs (lse feeds selective_log_softmax_bwd)
+ * An idx outside [0, V) writes NaN to logp (lse stays valid) and sets the error bit.
+ */
+grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* idx, float T,
+                                      float* logp, float* lse, int32_t* dev_err,
+                                      grpo_stream_t stream);
+
+/*
+ * selective_log_softmax_bwd -- dlogits_rj = (dlogp_r / T) * (1[j == idx_r] - p_j).
+ *
+ * Defined by [axolotl] "2. benchmarks/bench_selective_logsoftmax.py" (the backward
+ * kernel of the selective log-softmax), with the zero-row early-out of [Liger-bwd]
+ * "Code analysis": a row whose dlogp_r / T is exactly 0.0 is written as +0.0 without
+ * reading its logits.
+ *
+ *   logits [B, L, V];  idx [B*L] int64;  dlogp [B*L] fp32 upstream gradient of logp
+ *   lse [B*L] fp32 from selective_log_softmax_fwd;  T as in the forward
+ *   dlogits: as in grpo_loss_bwd (same dtype/B/L/V, may alias logits exactly)
+ */
+grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* idx,
+                                      const float* dlogp, const float* lse, float T,
+                                      const grpo_rows* dlogits, int32_t* dev_err,
+                                      grpo_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* grpo_status_string(grpo_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_ROWPASS_H_ */

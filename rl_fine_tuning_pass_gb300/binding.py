@@ -1,0 +1,211 @@
+"""Thin Python binding over the C ABI in ``include/grpo_rowpass.h``.
+
+Argument marshalling only: each function checks tensor devices/dtypes, allocates the
+outputs with torch (device memory is torch's job here), and calls the C entry point of
+the same name on the current CUDA stream.  Every step of the row pass runs in the CUDA
+kernels of ``libgrpo_rowpass.so``; there is no CPU fallback.  A missing library raises
+``RuntimeError`` on first use.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+GRPO_OK, GRPO_ERR_INVALID_ARG, GRPO_ERR_UNSUPPORTED, GRPO_ERR_CUDA = 0, 1, 2, 3
+GRPO_FP32, GRPO_BF16 = 0, 1
+GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
+
+EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "entropy_from_logits", "selective_log_softmax_fwd",
+            "selective_log_softmax_bwd", "grpo_status_string")
+
+
+class GrpoRows(ctypes.Structure):
+    """Mirror of ``grpo_rows``."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("B", ctypes.c_int64), ("L", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("stride_b", ctypes.c_int64), ("stride_l", ctypes.c_int64)]
+
+
+class GrpoError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_F = ctypes.c_float
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load ``libgrpo_rowpass.so`` (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m rl_fine_tuning_pass_gb300.build` "
+                           "(or __graft_entry__.build()); the row pass has no fallback")
+    lib = ctypes.CDLL(path)
+    rows_p = ctypes.POINTER(GrpoRows)
+    sig = {
+        "grpo_loss_fwd": [rows_p, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P],
+        "grpo_loss_bwd": [rows_p, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, rows_p, _P, _P],
+        "entropy_from_logits": [rows_p, _F, _P, _P],
+        "selective_log_softmax_fwd": [rows_p, _P, _F, _P, _P, _P, _P],
+        "selective_log_softmax_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P, _P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.grpo_status_string.argtypes = [ctypes.c_int]
+    lib.grpo_status_string.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().grpo_status_string(int(status)).decode()
+
+
+def rows_of(t: torch.Tensor) -> GrpoRows:
+    """Describe a [B, L, V] (or [R, V], read as B=1, L=R) tensor with vocab stride 1."""
+    if t.dim() == 2:
+        B, L, V = 1, t.shape[0], t.shape[1]
+        sb, sl = t.shape[0] * t.stride(0), t.stride(0)
+    elif t.dim() == 3:
+        B, L, V = t.shape
+        sb, sl = t.stride(0), t.stride(1)
+    else:
+        raise ValueError("logits must be [B, L, V] or [R, V]")
+    if V > 0 and t.stride(-1) != 1:
+        raise ValueError("the vocabulary dimension must have stride 1")
+    if t.dtype == torch.bfloat16:
+        dt = GRPO_BF16
+    elif t.dtype == torch.float32:
+        dt = GRPO_FP32
+    else:
+        raise TypeError(f"logits dtype {t.dtype} not supported (bf16 or fp32)")
+    return GrpoRows(t.data_ptr(), dt, 0, B, L, V, sb, sl)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype, n: Optional[int], name: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() != n:
+        raise ValueError(f"{name} must have {n} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != GRPO_OK:
+        raise GrpoError(fn, st)
+
+
+def _shape(logits: torch.Tensor):
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    if logits.dim() == 3:
+        return logits.shape[0], logits.shape[1]
+    return 1, logits.shape[0]
+
+
+def grpo_loss_fwd(logits, idx, adv, *, T, beta, eps_low, eps_high, old_logp=None, ref_logp=None,
+                  mask=None, with_kl=True, with_is_clipped=True, with_entropy=False, dev_err=None):
+    """GRPO forward; returns a dict with loss, logp, lse (+ kl, is_clipped, entropy)."""
+    B, L = _shape(logits)
+    R = B * L
+    dev = logits.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"loss": torch.empty(R, **f32), "logp": torch.empty(R, **f32), "lse": torch.empty(R, **f32)}
+    out["kl"] = torch.empty(R, **f32) if with_kl else None
+    out["is_clipped"] = torch.empty(R, dtype=torch.uint8, device=dev) if with_is_clipped else None
+    out["entropy"] = torch.empty(R, **f32) if with_entropy else None
+    x = rows_of(logits)
+    st = load_library().grpo_loss_fwd(
+        ctypes.byref(x), _ptr(idx, torch.int64, R, "idx"), _ptr(old_logp, torch.float32, R, "old_logp"),
+        _ptr(ref_logp, torch.float32, R, "ref_logp"), _ptr(adv, torch.float32, B, "adv"),
+        _ptr(mask, torch.uint8, R, "mask"), float(T), float(beta), float(eps_low), float(eps_high),
+        out["loss"].data_ptr(), out["logp"].data_ptr(), out["lse"].data_ptr(),
+        _ptr(out["kl"], torch.float32, R, "kl"), _ptr(out["is_clipped"], torch.uint8, R, "is_clipped"),
+        _ptr(out["entropy"], torch.float32, R, "entropy"), _ptr(dev_err, torch.int32, 1, "dev_err"),
+        _stream(dev))
+    _check("grpo_loss_fwd", st)
+    return {k: v for k, v in out.items() if v is not None}
+
+
+def grpo_loss_bwd(logits, idx, adv, dloss, logp, lse, *, T, beta, eps_low, eps_high, old_logp=None,
+                  ref_logp=None, mask=None, dlogits=None, dev_err=None):
+    """GRPO backward; returns dlogits (allocated [B, L, V] like logits unless given;
+    pass ``dlogits=logits`` for an in-place backward)."""
+    B, L = _shape(logits)
+    R = B * L
+    if dlogits is None:
+        dlogits = torch.empty(logits.shape, dtype=logits.dtype, device=logits.device)
+    x, dx = rows_of(logits), rows_of(dlogits)
+    st = load_library().grpo_loss_bwd(
+        ctypes.byref(x), _ptr(idx, torch.int64, R, "idx"), _ptr(old_logp, torch.float32, R, "old_logp"),
+        _ptr(ref_logp, torch.float32, R, "ref_logp"), _ptr(adv, torch.float32, B, "adv"),
+        _ptr(mask, torch.uint8, R, "mask"), _ptr(dloss, torch.float32, R, "dloss"),
+        _ptr(logp, torch.float32, R, "logp"), _ptr(lse, torch.float32, R, "lse"), float(T), float(beta),
+        float(eps_low), float(eps_high), ctypes.byref(dx), _ptr(dev_err, torch.int32, 1, "dev_err"),
+        _stream(logits.device))
+    _check("grpo_loss_bwd", st)
+    return dlogits
+
+
+def entropy_from_logits(logits, *, T=1.0):
+    """Per-row entropy [B*L] fp32."""
+    B, L = _shape(logits)
+    out = torch.empty(B * L, dtype=torch.float32, device=logits.device)
+    x = rows_of(logits)
+    st = load_library().entropy_from_logits(ctypes.byref(x), float(T), out.data_ptr(), _stream(logits.device))
+    _check("entropy_from_logits", st)
+    return out
+
+
+def selective_log_softmax_fwd(logits, idx, *, T=1.0, dev_err=None):
+    """Returns (logp, lse), each [B*L] fp32."""
+    B, L = _shape(logits)
+    R = B * L
+    logp = torch.empty(R, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(R, dtype=torch.float32, device=logits.device)
+    x = rows_of(logits)
+    st = load_library().selective_log_softmax_fwd(
+        ctypes.byref(x), _ptr(idx, torch.int64, R, "idx"), float(T), logp.data_ptr(), lse.data_ptr(),
+        _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(logits.device))
+    _check("selective_log_softmax_fwd", st)
+    return logp, lse
+
+
+def selective_log_softmax_bwd(logits, idx, dlogp, lse, *, T=1.0, dlogits=None, dev_err=None):
+    """Returns dlogits of sum_r dlogp_r * logp_r (allocated like logits unless given)."""
+    B, L = _shape(logits)
+    R = B * L
+    if dlogits is None:
+        dlogits = torch.empty(logits.shape, dtype=logits.dtype, device=logits.device)
+    x, dx = rows_of(logits), rows_of(dlogits)
+    st = load_library().selective_log_softmax_bwd(
+        ctypes.byref(x), _ptr(idx, torch.int64, R, "idx"), _ptr(dlogp, torch.float32, R, "dlogp"),
+        _ptr(lse, torch.float32, R, "lse"), float(T), ctypes.byref(dx), _ptr(dev_err, torch.int32, 1, "dev_err"),
+        _stream(logits.device))
+    _check("selective_log_softmax_bwd", st)
+    return dlogits

@@ -1,0 +1,260 @@
+// C-ABI entry points declared in include/grpo_rowpass.h.  Host-side validation runs
+// completely before any CUDA call, so a rejected call has no effect on the device.
+#include <cmath>
+#include <cstdint>
+
+#include "grpo_rowpass.h"
+#include "rowpass_internal.h"
+
+namespace {
+
+using grpo::BwdParams;
+using grpo::FwdParams;
+
+constexpr double kLog2eD = 1.4426950408889634074;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;  // one CTA per row, 1-D grid
+constexpr int64_t kMaxV = (int64_t(1) << 30);         // in-row indices are 32-bit
+
+int elem_size(int32_t dtype) { return dtype == GRPO_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Offset (elements) of the last element of the last row, +1; -1 on overflow.
+int64_t extent_elems(const grpo_rows* t) {
+  const long double e = static_cast<long double>(t->B - 1) * t->stride_b +
+                        static_cast<long double>(t->L - 1) * t->stride_l + t->V;
+  if (e > 4.0e18L) return -1;
+  return (t->B - 1) * t->stride_b + (t->L - 1) * t->stride_l + t->V;
+}
+
+// Rows of an output tensor must not overlap: one of the two strides is the inner one.
+bool rows_disjoint(const grpo_rows* t) {
+  auto nested = [&](int64_t si, int64_t ni, int64_t so, int64_t no) {
+    if (ni > 1 && si < t->V) return false;
+    const int64_t span = (ni > 0 ? ni - 1 : 0) * si + t->V;
+    return !(no > 1 && so < span);
+  };
+  return nested(t->stride_l, t->L, t->stride_b, t->B) || nested(t->stride_b, t->B, t->stride_l, t->L);
+}
+
+grpo_status check_rows(const grpo_rows* t) {
+  if (t == nullptr || t->ptr == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (t->dtype != GRPO_FP32 && t->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
+  if (t->reserved != 0) return GRPO_ERR_INVALID_ARG;
+  if (t->B < 0 || t->L < 0 || t->V < 1) return GRPO_ERR_INVALID_ARG;
+  if (t->stride_b < 0 || t->stride_l < 0) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(t->ptr, elem_size(t->dtype))) return GRPO_ERR_INVALID_ARG;
+  if (t->V > kMaxV) return GRPO_ERR_UNSUPPORTED;
+  if (t->B > 0 && t->L > 0) {
+    if (static_cast<long double>(t->B) * t->L > kMaxRows) return GRPO_ERR_UNSUPPORTED;
+    if (extent_elems(t) < 0) return GRPO_ERR_INVALID_ARG;
+  }
+  return GRPO_OK;
+}
+
+bool finite_pos(float v) { return std::isfinite(v) && v > 0.f; }
+
+grpo_status check_scalars_grpo(float T, float beta, float eps_low, float eps_high) {
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  if (!std::isfinite(beta) || beta < 0.f) return GRPO_ERR_INVALID_ARG;
+  if (!std::isfinite(eps_low) || eps_low < 0.f || eps_low > 1.f) return GRPO_ERR_INVALID_ARG;
+  if (!std::isfinite(eps_high) || eps_high < 0.f) return GRPO_ERR_INVALID_ARG;
+  return GRPO_OK;
+}
+
+bool ok_f32(const void* p) { return p != nullptr && aligned(p, 4); }
+bool ok_i64(const void* p) { return p != nullptr && aligned(p, 8); }
+bool ok_opt_f32(const void* p) { return p == nullptr || aligned(p, 4); }
+bool ok_opt_i32(const void* p) { return p == nullptr || aligned(p, 4); }
+
+grpo::RowsView view_of(const grpo_rows* t) {
+  return grpo::RowsView{t->ptr, t->L, t->stride_b, t->stride_l, static_cast<int>(t->V)};
+}
+
+// dlogits: same dtype and shape as logits, disjoint rows, and either exactly the same
+// tensor (in-place) or no byte in common with it.
+grpo_status check_dlogits(const grpo_rows* x, const grpo_rows* dx, bool* same_phase) {
+  grpo_status st = check_rows(dx);
+  if (st != GRPO_OK) return st;
+  if (dx->dtype != x->dtype || dx->B != x->B || dx->L != x->L || dx->V != x->V)
+    return GRPO_ERR_INVALID_ARG;
+  const int es = elem_size(x->dtype);
+  const int64_t rows = x->B * x->L;
+  if (rows > 1 && !rows_disjoint(dx)) return GRPO_ERR_INVALID_ARG;
+  if (rows > 0) {
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x->ptr);
+    const uintptr_t da = reinterpret_cast<uintptr_t>(dx->ptr);
+    const uintptr_t xe = xa + static_cast<uintptr_t>(extent_elems(x)) * es;
+    const uintptr_t de = da + static_cast<uintptr_t>(extent_elems(dx)) * es;
+    const bool overlap = xa < de && da < xe;
+    const bool same = xa == da && (x->B <= 1 || x->stride_b == dx->stride_b) &&
+                      (x->L <= 1 || x->stride_l == dx->stride_l);
+    if (overlap && !same) return GRPO_ERR_INVALID_ARG;
+  }
+  // every row of dx starts at the same address mod 16 as the matching row of x
+  const int64_t ph = (static_cast<int64_t>(reinterpret_cast<uintptr_t>(x->ptr) & 15) -
+                      static_cast<int64_t>(reinterpret_cast<uintptr_t>(dx->ptr) & 15));
+  const bool b_ok = x->B <= 1 || ((x->stride_b - dx->stride_b) * es) % 16 == 0;
+  const bool l_ok = x->L <= 1 || ((x->stride_l - dx->stride_l) * es) % 16 == 0;
+  *same_phase = ph == 0 && b_ok && l_ok;
+  return GRPO_OK;
+}
+
+grpo_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_loss_fwd(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                          const float* ref_logp, const float* adv, const uint8_t* mask, float T,
+                          float beta, float eps_low, float eps_high, float* loss, float* logp,
+                          float* lse, float* kl, uint8_t* is_clipped, float* entropy, int32_t* dev_err,
+                          grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
+  if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(loss) || !ok_f32(logp) ||
+      !ok_f32(lse) || !ok_opt_f32(kl) || !ok_opt_f32(entropy) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  if (rows == 0) return GRPO_OK;
+  FwdParams p{};
+  p.x = view_of(logits);
+  p.idx = idx;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.logp = logp;
+  p.lse = lse;
+  p.kl = kl;
+  p.is_clipped = is_clipped;
+  p.entropy = entropy;
+  p.dev_err = dev_err;
+  const int mode = entropy ? grpo::kFwdGrpoH : grpo::kFwdGrpo;
+  return from_cuda(grpo::launch_fwd(mode, logits->dtype, p, rows, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                          const float* ref_logp, const float* adv, const uint8_t* mask,
+                          const float* dloss, const float* logp, const float* lse, float T,
+                          float beta, float eps_low, float eps_high, const grpo_rows* dlogits,
+                          int32_t* dev_err, grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(logp) ||
+      !ok_f32(lse) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  if (rows == 0) return GRPO_OK;
+  BwdParams p{};
+  p.x = view_of(logits);
+  p.dx = grpo::OutView{dlogits->ptr, dlogits->L, dlogits->stride_b, dlogits->stride_l,
+                       static_cast<int>(dlogits->V)};
+  p.idx = idx;
+  p.lse = lse;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.dloss = dloss;
+  p.logp = logp;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.T = T;
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.dev_err = dev_err;
+  return from_cuda(grpo::launch_bwd(true, logits->dtype, same_phase, p, rows,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy,
+                                grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T) || !ok_f32(entropy)) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  if (rows == 0) return GRPO_OK;
+  FwdParams p{};
+  p.x = view_of(logits);
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.entropy = entropy;
+  return from_cuda(grpo::launch_fwd(grpo::kFwdEntropy, logits->dtype, p, rows,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* idx, float T,
+                                      float* logp, float* lse, int32_t* dev_err,
+                                      grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T) || !ok_i64(idx) || !ok_f32(logp) || !ok_f32(lse) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  if (rows == 0) return GRPO_OK;
+  FwdParams p{};
+  p.x = view_of(logits);
+  p.idx = idx;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.logp = logp;
+  p.lse = lse;
+  p.dev_err = dev_err;
+  return from_cuda(grpo::launch_fwd(grpo::kFwdSlsm, logits->dtype, p, rows,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* idx,
+                                      const float* dlogp, const float* lse, float T,
+                                      const grpo_rows* dlogits, int32_t* dev_err,
+                                      grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (!ok_i64(idx) || !ok_f32(dlogp) || !ok_f32(lse) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  if (rows == 0) return GRPO_OK;
+  BwdParams p{};
+  p.x = view_of(logits);
+  p.dx = grpo::OutView{dlogits->ptr, dlogits->L, dlogits->stride_b, dlogits->stride_l,
+                       static_cast<int>(dlogits->V)};
+  p.idx = idx;
+  p.lse = lse;
+  p.dlogp_up = dlogp;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.T = T;
+  p.dev_err = dev_err;
+  return from_cuda(grpo::launch_bwd(false, logits->dtype, same_phase, p, rows,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* grpo_status_string(grpo_status status) {
+  switch (status) {
+    case GRPO_OK: return "GRPO_OK";
+    case GRPO_ERR_INVALID_ARG: return "GRPO_ERR_INVALID_ARG: invalid pointer, size, stride, scalar or aliasing";
+    case GRPO_ERR_UNSUPPORTED: return "GRPO_ERR_UNSUPPORTED: valid arguments outside what this build handles";
+    case GRPO_ERR_CUDA: return "GRPO_ERR_CUDA: the kernel launch failed";
+    default: return "unknown grpo_status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+"""The C ABI on the CPU: the library loads, exports every function the header declares,
+and rejects bad arguments on the host before any CUDA call (fake device addresses are
+never dereferenced: each case fails validation, or has zero rows, before a launch)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from rl_fine_tuning_pass_gb300 import binding
+from rl_fine_tuning_pass_gb300.build import ROOT, build
+
+HEADER = os.path.join(ROOT, "include", "grpo_rowpass.h")
+FAKE = 0x7F0000100000          # 16-byte aligned, never dereferenced
+P = ctypes.c_void_p
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_functions_are_exported(lib):
+    names = header_functions()
+    assert set(names) == set(binding.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(4):
+        s = binding.status_string(code)
+        assert s.startswith("GRPO_")
+    assert "unknown" in binding.status_string(99)
+
+
+def rows(ptr=FAKE, dtype=binding.GRPO_BF16, B=2, L=3, V=64, sb=None, sl=None, reserved=0):
+    sl = V if sl is None else sl
+    sb = L * sl if sb is None else sb
+    return binding.GrpoRows(ptr, dtype, reserved, B, L, V, sb, sl)
+
+
+def fwd(lib, x, T=1.0, beta=0.0, el=0.2, eh=0.2, idx=FAKE, adv=FAKE, ref=None, outs=FAKE):
+    return lib.grpo_loss_fwd(ctypes.byref(x), idx, None, ref, adv, None, T, beta, el, eh,
+                             outs, outs + 64, outs + 128, None, None, None, None, None)
+
+
+def bwd(lib, x, dx, T=1.0, beta=0.0):
+    return lib.grpo_loss_bwd(ctypes.byref(x), FAKE, None, None, FAKE, None, FAKE, FAKE, FAKE,
+                             T, beta, 0.2, 0.2, ctypes.byref(dx), None, None)
+
+
+INV, UNS = binding.GRPO_ERR_INVALID_ARG, binding.GRPO_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(ptr=None), INV), (dict(dtype=7), INV), (dict(reserved=1), INV), (dict(V=0), INV),
+    (dict(B=-1), INV), (dict(sl=-64), INV), (dict(ptr=FAKE + 1), INV),
+    (dict(V=(1 << 30) + 1), UNS), (dict(B=1 << 16, L=1 << 15), UNS),
+])
+def test_bad_logits_rejected(lib, case, want):
+    assert fwd(lib, rows(**case)) == want
+
+
+@pytest.mark.parametrize("kw", [dict(T=0.0), dict(T=-1.0), dict(T=math.inf), dict(T=math.nan),
+                                dict(beta=-0.1), dict(beta=math.nan), dict(el=1.5), dict(el=-0.1),
+                                dict(eh=math.inf), dict(idx=None), dict(idx=FAKE + 4), dict(adv=None),
+                                dict(beta=0.04, ref=None), dict(outs=FAKE + 2)])
+def test_bad_scalars_and_pointers_rejected(lib, kw):
+    assert fwd(lib, rows(), **kw) == INV
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert fwd(lib, rows(B=0)) == binding.GRPO_OK
+    assert fwd(lib, rows(L=0)) == binding.GRPO_OK
+    x0 = rows(B=0)
+    assert lib.entropy_from_logits(ctypes.byref(x0), 1.0, FAKE, None) == binding.GRPO_OK
+
+
+def test_dlogits_validation(lib):
+    x = rows()
+    # partial overlap with the logits
+    assert bwd(lib, x, rows(ptr=FAKE + 128)) == INV
+    # dtype / shape mismatch
+    assert bwd(lib, x, rows(ptr=FAKE + (1 << 20), dtype=binding.GRPO_FP32)) == INV
+    assert bwd(lib, x, rows(ptr=FAKE + (1 << 20), V=32)) == INV
+    # overlapping output rows
+    assert bwd(lib, x, rows(ptr=FAKE + (1 << 20), sl=16)) == INV
+    # zero rows with valid descriptors: accepted, nothing launched
+    assert bwd(lib, rows(B=0), rows(B=0, ptr=FAKE + (1 << 20))) == binding.GRPO_OK
+    assert bwd(lib, rows(L=0), rows(L=0)) == binding.GRPO_OK  # exact alias, no rows
+    assert bwd(lib, x, rows(ptr=FAKE + (1 << 20)), T=0.0) == INV
+
+
+def test_slsm_and_entropy_validation(lib):
+    x = rows()
+    assert lib.selective_log_softmax_fwd(ctypes.byref(x), None, 1.0, FAKE, FAKE, None, None) == INV
+    assert lib.selective_log_softmax_fwd(ctypes.byref(x), FAKE, 0.0, FAKE, FAKE, None, None) == INV
+    assert lib.selective_log_softmax_fwd(ctypes.byref(x), FAKE, 1.0, FAKE, FAKE, FAKE + 2, None) == INV
+    assert lib.entropy_from_logits(ctypes.byref(x), 1.0, None, None) == INV
+    assert lib.entropy_from_logits(ctypes.byref(x), math.nan, FAKE, None) == INV
+    dx = rows(ptr=FAKE + 64)
+    assert lib.selective_log_softmax_bwd(ctypes.byref(x), FAKE, FAKE, FAKE, 1.0, ctypes.byref(dx),
+                                         None, None) == INV
+    assert lib.selective_log_softmax_bwd(ctypes.byref(x), FAKE, None, FAKE, 1.0,
+                                         ctypes.byref(rows(ptr=FAKE + (1 << 20))), None, None) == INV
+
+
+def test_rows_of_strides():
+    import torch
+    base = torch.empty(4, 9, 16, dtype=torch.bfloat16)
+    v = base[:, :-1, :]
+    r = binding.rows_of(v)
+    assert (r.B, r.L, r.V, r.stride_b, r.stride_l, r.dtype) == (4, 8, 16, 144, 16, binding.GRPO_BF16)
+    r2 = binding.rows_of(torch.empty(5, 7, dtype=torch.float32))
+    assert (r2.B, r2.L, r2.V, r2.stride_l) == (1, 5, 7, 7)
+    with pytest.raises(ValueError):
+        binding.rows_of(torch.empty(4, 8, dtype=torch.float32).t())
