@@ -380,6 +380,22 @@ def timed_run(step, K, Wm, flush_buf, world):
     return per, wall
 
 
+def aggregate_max_ms(local_ms: float, world: int, device) -> float:
+    """The timed region's length for the whole job: the maximum over ranks."""
+    if world <= 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rates(step_bytes: int, rows: int, K: int, world: int, total_ms: float):
+    """(GB/s, rows/s) of the whole job: every rank processed K steps of its own batch of
+    the same size, in at most total_ms."""
+    sec = total_ms * 1e-3
+    return step_bytes * K * world / sec / 1e9, rows * K * world / sec
+
+
 def e2e_run(step, K, Wm):
     step.e2e_setup()
     for _ in range(max(1, Wm)):
@@ -592,13 +608,8 @@ def main(argv=None):
 
     kern_ms = {n: statistics.mean(v) for n, v in per.items()}
     step_ms = sum(kern_ms.values())
-    total_ms = sum(sum(v) for v in per.values())
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
-    rows_per_s = spec.rows * K * world / (total_ms * 1e-3)
+    total_ms = aggregate_max_ms(sum(sum(v) for v in per.values()), world, device)
+    value, rows_per_s = whole_job_rates(step_bytes, spec.rows, K, world, total_ms)
 
     peak, peak_src = load_peaks()
     dom = max(kern_ms, key=kern_ms.get)

@@ -1,0 +1,86 @@
+"""bench.py host logic on the CPU: byte accounting, whole-job aggregation over ranks
+(world size 2 with the gloo backend), and the reference arm's rank handling."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from rl_fine_tuning_pass_gb300 import workloads as W  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    local_ms = [10.0, 25.0][rank]
+    total = bench.aggregate_max_ms(local_ms, world, "cpu")
+    gbs, rps = bench.whole_job_rates(1_000_000, 64, 10, world, total)
+    q.put((rank, total, gbs, rps))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_aggregation_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, total, gbs, rps in res:
+        assert total == 25.0                      # max over ranks, on every rank
+        assert abs(gbs - 1_000_000 * 10 * 2 / 0.025 / 1e9) < 1e-9
+        assert abs(rps - 64 * 10 * 2 / 0.025) < 1e-6
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.aggregate_max_ms(7.5, 1, "cpu") == 7.5
+
+
+def test_grpo_row_bytes_classes():
+    spec = W.get("grpo_b4_l512_v32000")
+    live = np.array([1, 1, 0, 1], bool)
+    zero = np.array([0, 1, 1, 0], bool)
+    f, b = bench.grpo_row_bytes(spec, live, zero, has_mask=True, has_old=True, has_ref=False)
+    Vs = spec.V * 2
+    assert list(f) == [1 + 21 + Vs + 12, 1 + 21 + Vs + 12, 1 + 21, 1 + 21 + Vs + 12]
+    # full row: write + read + scalars; zero row: write only (+ its factor inputs); masked: write + mask
+    assert list(b) == [1 + Vs + 12 + 12 + Vs, 1 + Vs + 12, 1 + Vs, 1 + Vs + 12 + 12 + Vs]
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_shape():
+    """Rank 0 of the reference arm: one JSON line with the oracle's throughput (small steps)."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "0"], capture_output=True, text=True, env=env,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "grpo_b4_l512_v32000"
