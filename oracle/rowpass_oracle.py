@@ -140,12 +140,14 @@ def log_softmax_rows(x: np.ndarray, T: float):
     analysis", divides the per-row gradient by the same TEMPERATURE, which is
     the chain-rule image of this scaling.  The sum is shifted by the row
     maximum so that exp never overflows; the shift cancels exactly in exact
-    arithmetic.
+    arithmetic.  A row whose logits are all -inf has an empty sum: lse = log 0
+    = -inf (the shift is then 0, since -inf - (-inf) has no value).
     """
     x = np.asarray(x, dtype=np.float64)
     z = x / np.float64(T)
-    with np.errstate(invalid="ignore", over="ignore"):
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
         m = np.max(z, axis=-1, keepdims=True)
+        m = np.where(np.isneginf(m), 0.0, m)
         s = np.sum(np.exp(z - m), axis=-1, keepdims=True)
         lse = (m + np.log(s))[..., 0]
     return z, lse
@@ -170,12 +172,14 @@ def entropy_from_logits(x: np.ndarray, T: float = 1.0) -> np.ndarray:
     takes ``log_softmax`` of each row and returns minus the sum of
     ``exp(logps) * logps``.  Written here as sum_j p_j (lse - z_j) so every
     term is non-negative; the two are the same sum term by term.  The page's
-    eager version has no temperature; T = 1 reproduces it.
+    eager version has no temperature; T = 1 reproduces it.  A term with p_j = 0
+    (a -inf logit, e.g. a vocabulary entry masked out) contributes 0, the limit
+    of p log p as p -> 0.
     """
     z, lse = log_softmax_rows(x, T)
     with np.errstate(invalid="ignore"):
         p = np.exp(z - lse[:, None])
-        return np.sum(p * (lse[:, None] - z), axis=-1)
+        return np.sum(np.where(p == 0.0, 0.0, p * (lse[:, None] - z)), axis=-1)
 
 
 # ---------------------------------------------------------------------------

@@ -37,6 +37,8 @@ bool rows_disjoint(const grpo_rows* t) {
   return nested(t->stride_l, t->L, t->stride_b, t->B) || nested(t->stride_b, t->B, t->stride_l, t->L);
 }
 
+int64_t rows_of(const grpo_rows* t) { return t->B * t->L; }
+
 grpo_status check_rows(const grpo_rows* t) {
   if (t == nullptr || t->ptr == nullptr) return GRPO_ERR_INVALID_ARG;
   if (t->dtype != GRPO_FP32 && t->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
@@ -114,6 +116,7 @@ grpo_status grpo_loss_fwd(const grpo_rows* logits, const int64_t* idx, const flo
   grpo_status st = check_rows(logits);
   if (st != GRPO_OK) return st;
   if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
+  if (rows_of(logits) == 0) return GRPO_OK;  // nothing to read or write; pointers may be NULL
   if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(loss) || !ok_f32(logp) ||
       !ok_f32(lse) || !ok_opt_f32(kl) || !ok_opt_f32(entropy) || !ok_opt_i32(dev_err))
     return GRPO_ERR_INVALID_ARG;
@@ -154,6 +157,7 @@ grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const flo
   if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
   bool same_phase = false;
   if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (rows_of(logits) == 0) return GRPO_OK;
   if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(logp) ||
       !ok_f32(lse) || !ok_opt_i32(dev_err))
     return GRPO_ERR_INVALID_ARG;
@@ -187,7 +191,9 @@ grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy
                                 grpo_stream_t stream) {
   grpo_status st = check_rows(logits);
   if (st != GRPO_OK) return st;
-  if (!finite_pos(T) || !ok_f32(entropy)) return GRPO_ERR_INVALID_ARG;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  if (rows_of(logits) == 0) return GRPO_OK;
+  if (!ok_f32(entropy)) return GRPO_ERR_INVALID_ARG;
   const int64_t rows = logits->B * logits->L;
   if (rows == 0) return GRPO_OK;
   FwdParams p{};
@@ -204,8 +210,9 @@ grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* id
                                       grpo_stream_t stream) {
   grpo_status st = check_rows(logits);
   if (st != GRPO_OK) return st;
-  if (!finite_pos(T) || !ok_i64(idx) || !ok_f32(logp) || !ok_f32(lse) || !ok_opt_i32(dev_err))
-    return GRPO_ERR_INVALID_ARG;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  if (rows_of(logits) == 0) return GRPO_OK;
+  if (!ok_i64(idx) || !ok_f32(logp) || !ok_f32(lse) || !ok_opt_i32(dev_err)) return GRPO_ERR_INVALID_ARG;
   const int64_t rows = logits->B * logits->L;
   if (rows == 0) return GRPO_OK;
   FwdParams p{};
@@ -229,6 +236,7 @@ grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* id
   if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
   bool same_phase = false;
   if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (rows_of(logits) == 0) return GRPO_OK;
   if (!ok_i64(idx) || !ok_f32(dlogp) || !ok_f32(lse) || !ok_opt_i32(dev_err))
     return GRPO_ERR_INVALID_ARG;
   const int64_t rows = logits->B * logits->L;

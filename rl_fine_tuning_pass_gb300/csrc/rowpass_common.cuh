@@ -82,6 +82,14 @@ struct BF16 {
     }
     return fmaxf(__low2float(m), __high2float(m));
   }
+  // Raise every element below -2^60 (i.e. -inf) to -2^60; NaN stays NaN.  Used before
+  // the entropy accumulation so that a -inf logit adds 2^t * t = 0 instead of 0 * -inf.
+  __device__ __forceinline__ static void clamp_low(uint4& v) {
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(-1.152921504606847e18f, -1.152921504606847e18f);
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+    h[0] = __hmax2_nan(h[0], lo2); h[1] = __hmax2_nan(h[1], lo2);
+    h[2] = __hmax2_nan(h[2], lo2); h[3] = __hmax2_nan(h[3], lo2);
+  }
   __device__ __forceinline__ static uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // RNE; a -> low half
     return *reinterpret_cast<uint32_t*>(&h);
@@ -123,6 +131,12 @@ struct F32 {
       m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
                          fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
     return m;
+  }
+  __device__ __forceinline__ static void clamp_low(uint4& v) {
+    constexpr float lo = -1.152921504606847e18f;  // -2^60
+    float* f = reinterpret_cast<float*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) f[q] = f[q] < lo ? lo : f[q];  // NaN stays NaN
   }
   __device__ __forceinline__ static uint4 pack(const float (&e)[kVec], uint32_t flip) {
     return make_uint4(__float_as_uint(e[0]) ^ flip, __float_as_uint(e[1]) ^ flip,

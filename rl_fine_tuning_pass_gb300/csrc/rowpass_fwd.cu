@@ -51,7 +51,8 @@ __device__ __forceinline__ void stat_accumulate(Stat& st, const float (&f)[N], f
 template <bool kH>
 __device__ __forceinline__ void stat_scalar(Running& rs, float x, float c) {
   if (x > rs.m) stat_rescale<kH>(rs, x, c);
-  float f[1] = {x};
+  // entropy: a -inf logit must add 0, not 0 * -inf (see clamp_low)
+  float f[1] = {kH && x < -1.152921504606847e18f ? -1.152921504606847e18f : x};
   stat_accumulate<kH>(rs.st, f, c);
 }
 
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
     if (cm > rs.m) stat_rescale<kH>(rs, cm, c);
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
+      if (kH) E::clamp_low(v[k]);
       float f[VEC];
       E::unpack(v[k], f);
       stat_accumulate<kH>(rs.st, f, c);
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
     v[0] = ld_nc_v4(vb + i);
     const float cm = E::template chunk_max<1>(v);
     if (cm > rs.m) stat_rescale<kH>(rs, cm, c);
+    if (kH) E::clamp_low(v[0]);
     float f[VEC];
     E::unpack(v[0], f);
     stat_accumulate<kH>(rs.st, f, c);

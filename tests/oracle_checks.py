@@ -192,6 +192,24 @@ def check_entropy_bounds_and_spike(orc):
     _close(logp, [0.0], 0, 1e-12, "spike logp")
 
 
+def check_special_rows(orc):
+    """An all -inf row: lse = log(0) = -inf, logp and H undefined (NaN).  A NaN logit makes
+    the row NaN.  A -inf logit among finite ones contributes exp(-inf) = 0 to the sum and
+    0 to the entropy."""
+    x = np.array([[-np.inf] * 4, [0.0, np.nan, 1.0, 2.0], [0.0, -np.inf, 1.0, 2.0]])
+    with np.errstate(all="ignore"):
+        logp, lse = orc.selective_log_softmax(x, np.array([0, 0, 2]), 1.0)
+        H = orc.entropy_from_logits(x, 1.0)
+    assert np.isneginf(lse[0]) and np.isnan(logp[0]) and np.isnan(H[0])
+    assert np.isnan(lse[1]) and np.isnan(logp[1]) and np.isnan(H[1])
+    ref = math.log(1 + math.e + math.e ** 2)
+    _close(lse[2:], [ref], 1e-14, 0, "lse with a -inf logit")
+    _close(logp[2:], [1.0 - ref], 1e-14, 0, "logp with a -inf logit")
+    # the -inf entry has p = 0 and adds nothing (p log p -> 0): H of the other three
+    q = np.exp(np.array([0.0, 1.0, 2.0]) - ref)
+    _close(H[2:], [-np.sum(q * np.log(q))], 1e-13, 0, "entropy with a -inf logit")
+
+
 def check_shift_invariance(orc):
     """x + c leaves logp and H unchanged and shifts lse by c / T."""
     rng = np.random.default_rng(6)
@@ -406,6 +424,7 @@ ALL_CHECKS = [
     check_uniform_and_two_level_rows,
     check_entropy_vs_scipy_eager_definition,
     check_entropy_bounds_and_spike,
+    check_special_rows,
     check_shift_invariance,
     check_ppo_clip_textbook_cases,
     check_clip_boundary_ties,

@@ -33,8 +33,10 @@ MUTATIONS = [
     ("onehot_wrong_column", "onehot[rows[ok], idx[ok]] = 1.0", "onehot[rows[ok], (idx[ok] + 1) % V] = 1.0"),
     ("grad_sign", "d = g[:, None] * (onehot - p)", "d = g[:, None] * (p - onehot)"),
     ("zero_rows_not_forced", "d[g == 0.0, :] = 0.0", "pass"),
-    ("entropy_sign", "return np.sum(p * (lse[:, None] - z), axis=-1)", "return np.sum(p * (z - lse[:, None]), axis=-1)"),
+    ("entropy_zero_terms_not_skipped", "np.where(p == 0.0, 0.0, p * (lse[:, None] - z))", "p * (lse[:, None] - z)"),
+    ("entropy_sign", "np.where(p == 0.0, 0.0, p * (lse[:, None] - z))", "np.where(p == 0.0, 0.0, p * (z - lse[:, None]))"),
     ("lse_drops_max", "lse = (m + np.log(s))[..., 0]", "lse = np.log(s)[..., 0]"),
+    ("all_neginf_row_not_handled", "m = np.where(np.isneginf(m), 0.0, m)", "pass"),
     ("lse_no_shift", "s = np.sum(np.exp(z - m), axis=-1, keepdims=True)\n        lse = (m + np.log(s))[..., 0]",
      "s = np.sum(np.exp(z), axis=-1, keepdims=True)\n        lse = np.log(s)[..., 0]"),
     ("logp_sign_of_lse", "logp = z[rows, np.asarray(idx, dtype=np.int64)] - lse",

