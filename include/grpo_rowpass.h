@@ -41,8 +41,8 @@
  * - Return value: GRPO_OK, or an error found on the host BEFORE any launch
  *   (GRPO_ERR_INVALID_ARG / GRPO_ERR_UNSUPPORTED; nothing is written), or
  *   GRPO_ERR_CUDA when the launch itself failed (cudaGetLastError after the launch).
- *   B*L == 0 is valid and launches nothing; the data pointers (not the descriptors)
- *   may then be NULL.
+ *   B*L == 0 is valid and launches nothing; the data pointers (including the
+ *   descriptors' ptr fields, but not the descriptors themselves) may then be NULL.
  * - `dev_err` (nullable) is a device int32 word the kernels OR error bits into
  *   (GRPO_DEVERR_*).  The library never clears it and never traps: a row with an
  *   out-of-range idx gets NaN in its idx-dependent outputs and the bit is set.

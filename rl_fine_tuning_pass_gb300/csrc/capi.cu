@@ -40,7 +40,8 @@ bool rows_disjoint(const grpo_rows* t) {
 int64_t rows_of(const grpo_rows* t) { return t->B * t->L; }
 
 grpo_status check_rows(const grpo_rows* t) {
-  if (t == nullptr || t->ptr == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (t == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (t->ptr == nullptr && !(t->B == 0 || t->L == 0)) return GRPO_ERR_INVALID_ARG;
   if (t->dtype != GRPO_FP32 && t->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
   if (t->reserved != 0) return GRPO_ERR_INVALID_ARG;
   if (t->B < 0 || t->L < 0 || t->V < 1) return GRPO_ERR_INVALID_ARG;

@@ -80,6 +80,7 @@ def test_bad_scalars_and_pointers_rejected(lib, kw):
 
 def test_zero_rows_is_a_no_op(lib):
     assert fwd(lib, rows(B=0)) == binding.GRPO_OK
+    assert fwd(lib, rows(ptr=None, B=0), idx=None, adv=None, outs=0) == binding.GRPO_OK
     assert fwd(lib, rows(L=0)) == binding.GRPO_OK
     x0 = rows(B=0)
     assert lib.entropy_from_logits(ctypes.byref(x0), 1.0, FAKE, None) == binding.GRPO_OK
