@@ -13,8 +13,8 @@ The metric is algorithmic HBM bytes per second (the minimal bytes of the step: e
 unmasked row's logits read once by the forward; each backward row with a non-zero
 factor read once and written once; each zero row written once; plus the per-row
 scalars), and rows per second.  Inputs are resident in HBM when the timed region
-starts; L2 is flushed (a 256 MB write) before every timed step and the flush is not
-timed.  ``e2e`` repeats the measurement through the public Python API with the inputs
+starts; L2 is flushed (a 256 MB write, then a 256 MB read so no dirty lines remain)
+before every timed step and the flush is not timed.  ``e2e`` repeats the measurement through the public Python API with the inputs
 in pinned host memory and the outputs copied back, copies inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
@@ -48,6 +48,21 @@ from rl_fine_tuning_pass_gb300 import workloads as W  # noqa: E402
 METRIC = "GRPO fwd+bwd logits GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: a 256 MB write (larger than the 129 MB L2), then a
+    256 MB read of another buffer so that the written lines are written back during the
+    flush and none of the flush's dirty lines are left for the timed kernels to evict."""
+
+    def __init__(self, device):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self, i: int = 0):
+        self.w.fill_(i & 0x7F)
+        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
 GRPO_WORKLOADS = ("grpo_b4_l512_v32000", "grpo_qwen3_b16_l1024_v151936", "sweep_b16_l4096_v151936")
 
 
@@ -355,7 +370,7 @@ def timed_run(step, K, Wm, flush_buf, world):
     time of the barrier-bracketed region."""
     names = [n for n, _ in step.kernels]
     for i in range(Wm):
-        flush_buf.fill_(i & 0x7F)
+        flush_buf(i)
         for _, fn in step.kernels:
             fn()
     torch.cuda.synchronize()
@@ -366,7 +381,7 @@ def timed_run(step, K, Wm, flush_buf, world):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(K):
-        flush_buf.fill_((i + 1) & 0x7F)
+        flush_buf(i + 1)
         e = ev[i]
         e[0].record()
         for k, (_, fn) in enumerate(step.kernels):
@@ -495,7 +510,7 @@ def base_line(args, spec, world):
             "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "V": spec.V, "T": spec.T,
                        "beta": spec.beta, "eps_low": spec.eps_low, "eps_high": spec.eps_high,
                        "logits_dtype": spec.dtype, "strided": spec.strided,
-                       "l2": "flushed before every timed step (256 MB write, not timed)",
+                       "l2": "flushed before every timed step (256 MB write + 256 MB read, not timed)",
                        "parallelism": f"{world} independent batch(es), one per GPU"}}
 
 
@@ -585,7 +600,7 @@ def main(argv=None):
         torch.distributed.init_process_group("nccl", device_id=device)
     spec = make_spec(args)
     step = make_step(spec, args.seed + rank, device)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_buf = L2Flush(device)
 
     # one untimed step to classify rows, then calibrate the step count
     for _, fn in step.kernels:

@@ -105,6 +105,20 @@ grpo_status check_dlogits(const grpo_rows* x, const grpo_rows* dx, bool* same_ph
 
 grpo_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA; }
 
+// Streaming multiprocessors of the current device (queried once per device; the
+// launch shape depends on how many rows can be resident at once).
+int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -145,7 +159,7 @@ grpo_status grpo_loss_fwd(const grpo_rows* logits, const int64_t* idx, const flo
   p.entropy = entropy;
   p.dev_err = dev_err;
   const int mode = entropy ? grpo::kFwdGrpoH : grpo::kFwdGrpo;
-  return from_cuda(grpo::launch_fwd(mode, logits->dtype, p, rows, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(grpo::launch_fwd(mode, logits->dtype, p, rows, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
@@ -184,7 +198,7 @@ grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const flo
   p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
   p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
   p.dev_err = dev_err;
-  return from_cuda(grpo::launch_bwd(true, logits->dtype, same_phase, p, rows,
+  return from_cuda(grpo::launch_bwd(true, logits->dtype, same_phase, p, rows, device_sms(),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -202,8 +216,7 @@ grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy
   p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
   p.invT = static_cast<float>(1.0 / static_cast<double>(T));
   p.entropy = entropy;
-  return from_cuda(grpo::launch_fwd(grpo::kFwdEntropy, logits->dtype, p, rows,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(grpo::launch_fwd(grpo::kFwdEntropy, logits->dtype, p, rows, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* idx, float T,
@@ -224,8 +237,7 @@ grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* id
   p.logp = logp;
   p.lse = lse;
   p.dev_err = dev_err;
-  return from_cuda(grpo::launch_fwd(grpo::kFwdSlsm, logits->dtype, p, rows,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(grpo::launch_fwd(grpo::kFwdSlsm, logits->dtype, p, rows, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* idx,
@@ -252,7 +264,7 @@ grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* id
   p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
   p.T = T;
   p.dev_err = dev_err;
-  return from_cuda(grpo::launch_bwd(false, logits->dtype, same_phase, p, rows,
+  return from_cuda(grpo::launch_bwd(false, logits->dtype, same_phase, p, rows, device_sms(),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -1,0 +1,196 @@
+// Backward row kernels: dlogits_j = g * (1[j == idx] - p_j) with one scalar g per row.
+//
+// g is decided before any logits address is formed ("LinkedIn Liger-Kernel GRPO Loss
+// Backward optimisation", section "Code analysis": dlogp from the policy-gradient and
+// KL terms, times dloss, divided by the temperature; when it is exactly 0.0 the row is
+// filled with 0.0 and the kernel returns).  Rows with g != 0 are read once and written
+// once:
+//
+//   |g| * p_j = 2^(x_j * c - K),   K = lse * log2(e) - log2|g|,   c = log2(e) / T
+//
+// so each element costs half a packed f32x2 FMA and one ex2; the sign of -g is applied
+// in the conversion to the output format.  The idx element needs g * (1 - p_idx);
+// 1 - p_idx is formed as the sum of the other columns' p_j (accumulated on the way,
+// reduced over the CTA at the end), which keeps full relative accuracy when p_idx is
+// close to 1.
+#pragma once
+
+#include <cmath>
+
+#include "rowpass_common.cuh"
+
+namespace grpo {
+namespace {
+
+// Per-row factor g of the GRPO loss (fp32, same operation order as the definition).
+__device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b) {
+  if (p.mask != nullptr && p.mask[r] == 0) return 0.f;
+  const float logp = p.logp[r];
+  const float ratio = p.old_logp ? expf(logp - p.old_logp[r]) : 1.f;
+  const float A = p.adv[b];
+  const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
+  // unclipped branch is the minimum (ties included): d(-ratio*A)/dlogp; else constant
+  const float dpg = (ratio * A <= clipped * A) ? -A * ratio : 0.f;
+  float dkl = 0.f;
+  if (p.beta != 0.f) dkl = -p.beta * expm1f(p.ref_logp[r] - logp);  // beta (1 - e^(ref - logp))
+  return (dpg + dkl) * p.dloss[r] / p.T;
+}
+
+// The part of a row one CTA handles: vectors [v0, v1), plus the scalar head and tail.
+struct Span {
+  int v0, v1;
+  bool head, tail;
+};
+
+__device__ __forceinline__ Span whole_row(const RowSplit& sp) { return Span{0, sp.nvec, true, true}; }
+
+template <class E, int THREADS>
+__device__ __forceinline__ void fill_span(typename E::storage* out, const RowSplit& sp, const Span& sn,
+                                          uint32_t pair) {
+  const int tid = threadIdx.x;
+  if (sn.head && tid < sp.head) E::store_bits(out + tid, pair);
+  if (sn.tail && tid < sp.tail) E::store_bits(out + sp.head + sp.nvec * E::kVec + tid, pair);
+  uint4* vb = reinterpret_cast<uint4*>(out + sp.head);
+  const uint4 v = make_uint4(pair, pair, pair, pair);
+#pragma unroll 4
+  for (int i = sn.v0 + tid; i < sn.v1; i += THREADS) st_v4(vb + i, v);
+}
+
+// Load the VEC input elements of output vector i (input rows may be out of phase with
+// the output rows; then the elements are loaded one by one).
+template <class E, bool SAME_PHASE>
+__device__ __forceinline__ uint4 load_vec(const typename E::storage* in_body, int i) {
+  if (SAME_PHASE) return ld_v4(reinterpret_cast<const uint4*>(in_body) + i);
+  float f[E::kVec];
+#pragma unroll
+  for (int q = 0; q < E::kVec; ++q) f[q] = E::load_scalar_coherent(in_body + i * E::kVec + q);
+  return E::pack(f, 0u);  // exact: the values came from this format
+}
+
+// Stream one row with g != 0: out_j = -sign(g) |g| p_j (NEG: g > 0), accumulating
+// sum_{j != idx} |g| p_j for the idx element.  Returns this thread's partial sum and
+// whether it wrote the idx element.
+template <class E, int THREADS, int UNROLL, bool SAME_PHASE, bool NEG>
+__device__ __forceinline__ float stream_span(const typename E::storage* in, typename E::storage* out,
+                                             const RowSplit& sp, const Span& sn, int idx, float c, float nK,
+                                             bool& owner) {
+  constexpr int VEC = E::kVec;
+  using S = typename E::storage;
+  const int tid = threadIdx.x;
+  float q_acc = 0.f;
+  float2 q2 = make_float2(0.f, 0.f);
+
+  auto scalar = [&](int j) {
+    const float x = E::load_scalar_coherent(in + j);
+    const float e = ex2(fmaf(x, c, nK));
+    if (j == idx) owner = true; else q_acc += e;
+    E::store_scalar(out + j, NEG ? -e : e);
+  };
+  if (sn.head && tid < sp.head) scalar(tid);
+  if (sn.tail && tid < sp.tail) scalar(sp.head + sp.nvec * VEC + tid);
+
+  const S* in_body = in + sp.head;
+  uint4* ob = reinterpret_cast<uint4*>(out + sp.head);
+  const int idx_body = idx - sp.head;  // idx relative to the body start
+  const float2 c2 = make_float2(c, c), nK2 = make_float2(nK, nK);
+
+  auto process = [&](const uint4& v, int i) {
+    float2 e[E::kPairs];
+#pragma unroll
+    for (int q = 0; q < E::kPairs; ++q) {
+      const float2 t = __ffma2_rn(E::pair(v, q), c2, nK2);
+      e[q] = make_float2(ex2(t.x), ex2(t.y));
+    }
+    const unsigned k = static_cast<unsigned>(idx_body - i * VEC);
+    if (k < static_cast<unsigned>(VEC)) {  // this vector holds idx: leave it out of the sum
+      owner = true;
+#pragma unroll
+      for (int q = 0; q < E::kPairs; ++q) {
+        if (2 * q != static_cast<int>(k)) q_acc += e[q].x;
+        if (2 * q + 1 != static_cast<int>(k)) q_acc += e[q].y;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < E::kPairs; ++q) q2 = __fadd2_rn(q2, e[q]);
+    }
+    st_v4(ob + i, E::template pack_pairs<NEG>(e));
+  };
+
+  int i = sn.v0 + tid;
+  for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) v[k] = load_vec<E, SAME_PHASE>(in_body, i + k * THREADS);
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
+  }
+  for (; i < sn.v1; i += THREADS) process(load_vec<E, SAME_PHASE>(in_body, i), i);
+  return q_acc + (q2.x + q2.y);
+}
+
+template <class E, int THREADS, int UNROLL, bool GRPO, bool SAME_PHASE>
+__global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
+  using S = typename E::storage;
+  const int64_t r = blockIdx.x;
+  const int64_t b = r / p.x.L;
+  const int64_t l = r - b * p.x.L;
+  const int tid = threadIdx.x;
+  const int V = p.x.V;
+
+  // row factor, computed redundantly by every thread from broadcast loads
+  const float g = GRPO ? grpo_row_factor(p, r, b) : p.dlogp_up[r] / p.T;
+  S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
+  const RowSplit sp = split_row<E>(out, V);
+  const Span sn = whole_row(sp);
+
+  if (g == 0.f) {  // early-out: +0.0 over the row, nothing read
+    fill_span<E, THREADS>(out, sp, sn, 0u);
+    return;
+  }
+  const int64_t id64 = p.idx[r];
+  if (id64 < 0 || id64 >= V) {
+    fill_span<E, THREADS>(out, sp, sn, E::kNaNPair);
+    if (tid == 0 && p.dev_err) atomicOr(p.dev_err, GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT);
+    return;
+  }
+  const int idx = static_cast<int>(id64);
+  const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
+  const float nK = fmaf(-p.lse[r], kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
+  bool owner = false;
+  // d_j = -sign(g) |g| p_j: negated when g > 0
+  const float q_part =
+      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true>(in, out, sp, sn, idx, p.c, nK, owner)
+              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false>(in, out, sp, sn, idx, p.c, nK, owner);
+
+  // g (1 - p_idx) = sign(g) * sum_{j != idx} |g| p_j; written by the thread that wrote
+  // the idx element's provisional value, so its two stores stay in program order.
+  const float q_total = block_sum_all<THREADS>(q_part);
+  if (owner) E::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
+}
+
+template <class E, int THREADS, int U, bool GRPO, bool SAME_PHASE>
+cudaError_t launch4(const BwdParams& p, int64_t rows, cudaStream_t s) {
+  rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE><<<dim3(static_cast<unsigned>(rows)), THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <class E, int THREADS, int U>
+cudaError_t launch3(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, cudaStream_t s) {
+  if (grpo) return same_phase ? launch4<E, THREADS, U, true, true>(p, rows, s)
+                              : launch4<E, THREADS, U, true, false>(p, rows, s);
+  return same_phase ? launch4<E, THREADS, U, false, true>(p, rows, s)
+                    : launch4<E, THREADS, U, false, false>(p, rows, s);
+}
+
+template <class E>
+cudaError_t launch2(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t s) {
+  switch (pick_threads_bwd(p.x.V, sizeof(typename E::storage), rows, sms)) {
+    case 32: return launch3<E, 32, kUnrollSmall>(grpo, same_phase, p, rows, s);
+    case 64: return launch3<E, 64, kUnroll>(grpo, same_phase, p, rows, s);
+    case 128: return launch3<E, 128, kUnroll>(grpo, same_phase, p, rows, s);
+    default: return launch3<E, 256, kUnroll>(grpo, same_phase, p, rows, s);
+  }
+}
+
+}  // namespace
+}  // namespace grpo

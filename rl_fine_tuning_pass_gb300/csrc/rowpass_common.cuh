@@ -70,6 +70,22 @@ struct BF16 {
     f[0] = lo(v.x); f[1] = hi(v.x); f[2] = lo(v.y); f[3] = hi(v.y);
     f[4] = lo(v.z); f[5] = hi(v.z); f[6] = lo(v.w); f[7] = hi(v.w);
   }
+  // the vector as kVec / 2 pairs of floats (elements 2i, 2i+1), for the packed f32x2 math
+  static constexpr int kPairs = 4;
+  __device__ __forceinline__ static float2 pair(const uint4& v, int i) {
+    const uint32_t w = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+    return make_float2(lo(w), hi(w));
+  }
+  // pairs -> one 16-byte vector, RNE; NEG stores the negated values
+  template <bool NEG>
+  __device__ __forceinline__ static uint4 pack_pairs(const float2 (&e)[kPairs]) {
+    uint4 o;
+    o.x = NEG ? pack2(-e[0].x, -e[0].y) : pack2(e[0].x, e[0].y);
+    o.y = NEG ? pack2(-e[1].x, -e[1].y) : pack2(e[1].x, e[1].y);
+    o.z = NEG ? pack2(-e[2].x, -e[2].y) : pack2(e[2].x, e[2].y);
+    o.w = NEG ? pack2(-e[3].x, -e[3].y) : pack2(e[3].x, e[3].y);
+    return o;
+  }
   // Maximum of the vectors' elements.  max.bf16x2 is exact and returns the non-NaN
   // operand when one operand is NaN (NaN rows still end as NaN through the sums).
   template <int N>
@@ -122,6 +138,18 @@ struct F32 {
   __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[kVec]) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  static constexpr int kPairs = 2;
+  __device__ __forceinline__ static float2 pair(const uint4& v, int i) {
+    return i == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  template <bool NEG>
+  __device__ __forceinline__ static uint4 pack_pairs(const float2 (&e)[kPairs]) {
+    return NEG ? make_uint4(__float_as_uint(-e[0].x), __float_as_uint(-e[0].y), __float_as_uint(-e[1].x),
+                            __float_as_uint(-e[1].y))
+               : make_uint4(__float_as_uint(e[0].x), __float_as_uint(e[0].y), __float_as_uint(e[1].x),
+                            __float_as_uint(e[1].y));
   }
   template <int N>
   __device__ __forceinline__ static float chunk_max(const uint4 (&v)[N]) {
@@ -194,14 +222,26 @@ __device__ __forceinline__ Stat stat_combine(const Stat& x, const Stat& y) {
   return r;
 }
 
+// Re-express a partial relative to the offset A >= v.a (empty partials stay empty).
+__device__ __forceinline__ Stat stat_shift(const Stat& v, float A) {
+  if (v.s == 0.f) return Stat{A, 0.f, 0.f};
+  const float d = v.a - A;
+  const float e = ex2(d);
+  return Stat{A, e * v.s, e * fmaf(d, v.s, v.u)};
+}
+
+// Warp-wide merge, result in every lane: the largest offset first (one max per
+// round), then every lane moves to it once, then plain sums.
 __device__ __forceinline__ Stat stat_warp_reduce(Stat v) {
+  float A = v.s == 0.f ? -INFINITY : v.a;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) A = fmaxf(A, __shfl_xor_sync(0xFFFFFFFFu, A, off));
+  if (A == -INFINITY) return Stat{-INFINITY, 0.f, 0.f};  // every lane empty
+  v = stat_shift(v, A);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    Stat o;
-    o.a = __shfl_xor_sync(0xFFFFFFFFu, v.a, off);
-    o.s = __shfl_xor_sync(0xFFFFFFFFu, v.s, off);
-    o.u = __shfl_xor_sync(0xFFFFFFFFu, v.u, off);
-    v = stat_combine(v, o);
+    v.s += __shfl_xor_sync(0xFFFFFFFFu, v.s, off);
+    v.u += __shfl_xor_sync(0xFFFFFFFFu, v.u, off);
   }
   return v;
 }
@@ -210,10 +250,10 @@ __device__ __forceinline__ Stat stat_warp_reduce(Stat v) {
 template <int THREADS>
 __device__ __forceinline__ Stat stat_block_reduce(Stat v) {
   constexpr int kWarps = THREADS / 32;
-  __shared__ Stat sh[kWarps];
   v = stat_warp_reduce(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (kWarps == 1) return v;
+  __shared__ Stat sh[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) sh[warp] = v;
   __syncthreads();
   if (warp == 0) {
@@ -227,10 +267,11 @@ __device__ __forceinline__ Stat stat_block_reduce(Stat v) {
 template <int THREADS>
 __device__ __forceinline__ float block_sum_all(float v) {
   constexpr int kWarps = THREADS / 32;
-  __shared__ float sh[kWarps];
-  __shared__ float total;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  if (kWarps == 1) return v;
+  __shared__ float sh[kWarps];
+  __shared__ float total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) sh[warp] = v;
   __syncthreads();

@@ -11,14 +11,27 @@ namespace grpo {
 // Error bit OR-ed into the caller's device error word (GRPO_DEVERR_IDX_OUT_OF_RANGE).
 constexpr int GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT = 1;
 
-// Threads per CTA for a row of V elements of `esize` bytes: enough 16-byte vectors per
-// thread to keep several loads in flight, and a whole row per CTA.
-inline int pick_threads(int V, int esize) {
+// 16-byte loads in flight per thread: single-warp CTAs keep more of them so that a
+// warp streaming a whole row still covers the memory latency.
+constexpr int kUnroll = 4;
+constexpr int kUnrollSmall = 8;
+
+// Threads per CTA (one CTA per row), from measurements on GB300 (L2 flushed):
+// forward: 64 threads per row when every row can be resident at once (up to 24 such
+//   CTAs per SM) or the row is short (8 KB or less): all rows stream concurrently, with
+//   no CTA-granularity tail; otherwise 256-thread CTAs, several per SM.
+// backward: 256-thread CTAs (64 for short rows); rows whose factor is zero finish early
+//   and the block scheduler refills their slots.
+inline int pick_threads_fwd(int V, int esize, long long rows, int sms) {
   const long long bytes = static_cast<long long>(V) * esize;
-  if (bytes <= 4096) return 128;
-  if (bytes <= 32768) return 256;
-  if (bytes <= 131072) return 512;
-  return 1024;
+  if (rows <= 24LL * sms || bytes <= 8192) return 64;
+  return 256;
+}
+inline int pick_threads_bwd(int V, int esize, long long rows, int sms) {
+  (void)rows;
+  (void)sms;
+  const long long bytes = static_cast<long long>(V) * esize;
+  return bytes <= 8192 ? 64 : 256;
 }
 
 // Strided [B, L, V] view: element (b, l, j) at ptr + b*sb + l*sl + j.
@@ -84,11 +97,25 @@ struct BwdParams {
   int32_t* dev_err;
 };
 
-// Launch one CTA per row over `rows` rows.  dtype: 0 fp32, 1 bf16.
-cudaError_t launch_fwd(int mode, int dtype, const FwdParams& p, int64_t rows, cudaStream_t stream);
+// Kernel launchers, one translation unit per element type (compiled in parallel).
+cudaError_t launch_fwd_bf16(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
+cudaError_t launch_fwd_f32(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_f32(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                           cudaStream_t stream);
+
+// Launch the forward over `rows` rows.  dtype: 0 fp32, 1 bf16.
+inline cudaError_t launch_fwd(int mode, int dtype, const FwdParams& p, int64_t rows, int sms,
+                              cudaStream_t stream) {
+  return dtype == 1 ? launch_fwd_bf16(mode, p, rows, sms, stream) : launch_fwd_f32(mode, p, rows, sms, stream);
+}
 // grpo: GRPO row factor (true) or selective-log-softmax row factor (false).
 // same_phase: input and output rows have equal start addresses mod 16 for every row.
-cudaError_t launch_bwd(bool grpo, int dtype, bool same_phase, const BwdParams& p, int64_t rows,
-                       cudaStream_t stream);
+inline cudaError_t launch_bwd(bool grpo, int dtype, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                              cudaStream_t stream) {
+  return dtype == 1 ? launch_bwd_bf16(grpo, same_phase, p, rows, sms, stream)
+                    : launch_bwd_f32(grpo, same_phase, p, rows, sms, stream);
+}
 
 }  // namespace grpo
