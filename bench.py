@@ -5,7 +5,8 @@ One step = one pass of the whole hot path over one batch of synthetic logits:
 
 * GRPO workloads (default ``grpo_b4_l512_v32000``, the GRPO backward workload of the
   Liger-Kernel GRPO Loss Backward write-up: (B, L, V, zero-grad%) = (4, 512, 32000, 50%)):
-  ``grpo_loss_fwd`` (loss, logp, lse, kl, is_clipped, entropy) then ``grpo_loss_bwd``.
+  ``grpo_loss_fwd`` (loss, logp, lse, kl, is_clipped, entropy) then ``grpo_loss_bwd``;
+  with ``--fused``, the single kernel ``grpo_loss_fused`` (dloss known in advance).
 * ``entropy_slsm_b16_l4096_v32000``: ``entropy_from_logits``, ``selective_log_softmax_fwd``
   and ``selective_log_softmax_bwd``.
 
@@ -190,6 +191,18 @@ def grpo_row_bytes(spec, live, zero_g, has_mask, has_old, has_ref):
     return fwd.astype(np.int64), bwd.astype(np.int64)
 
 
+def fused_row_bytes(spec, live, has_mask, has_old, has_ref):
+    """Minimal bytes per row of the fused forward + backward: an unmasked row reads its V
+    logits once (and idx, old, ref, dloss), every row reads its mask byte, writes the
+    forward outputs (21 B) and its V dlogits."""
+    V, s = spec.V, spec.elem_size
+    live = np.asarray(live, bool)
+    m = 1 if has_mask else 0
+    o = 4 if has_old else 0
+    r = 4 if has_ref else 0
+    return (m + 21 + V * s + live * (V * s + 8 + o + r + 4)).astype(np.int64)
+
+
 SLSM_ROW_BYTES = {"entropy_from_logits": lambda V, s: V * s + 4,
                   "selective_log_softmax_fwd": lambda V, s: V * s + 8 + 8,
                   "selective_log_softmax_bwd": lambda V, s: 2 * V * s + 8 + 4 + 4}
@@ -283,6 +296,51 @@ class GrpoStep:
         self.h_loss.copy_(f["loss"], non_blocking=True)
 
 
+class FusedStep(GrpoStep):
+    """grpo_loss_fused: forward outputs and dlogits in one kernel (dloss known in advance)."""
+
+    def __init__(self, spec, seed, device, inputs=None):
+        super().__init__(spec, seed, device, inputs)
+        lib = rp.load_library()
+        inp, o = self.inp, self.out
+        self._fused = lib.grpo_loss_fused
+        self.fused_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(self.old), _p(self.ref), _p(inp.adv),
+                           _p(inp.mask), _p(inp.dloss), spec.T, spec.beta, spec.eps_low, spec.eps_high,
+                           _p(o["loss"]), _p(o["logp"]), _p(o["lse"]), _p(o["kl"]), _p(o["is_clipped"]),
+                           _p(o["entropy"]), ctypes.byref(self.dx_desc), None, self.stream)
+        self.kernels = [("grpo_loss_fused", self.fused)]
+
+    def fused(self):
+        st = self._fused(*self.fused_args)
+        if st:
+            raise rp.GrpoError("grpo_loss_fused", st)
+
+    def account(self):
+        spec, inp = self.spec, self.inp
+        R = spec.rows
+        live = np.ones(R, bool) if inp.mask is None else inp.mask.bool().cpu().numpy()
+        b = fused_row_bytes(spec, live, inp.mask is not None, self.old is not None, self.ref is not None)
+        zero = (~torch.from_numpy(live).to(inp.idx.device)) | (inp.dloss == 0)
+        if spec.beta == 0:
+            zero = zero | (inp.adv.repeat_interleave(spec.L) == 0) | self.out["is_clipped"].bool()
+        n_zero = int(zero.sum())
+        self.classes = {"rows": R, "masked": int(R - live.sum()), "zero_grad_rows": n_zero,
+                        "zero_grad_frac": round(n_zero / R, 4), "fused": True}
+        return {"grpo_loss_fused": int(b.sum())}
+
+    def e2e_step(self):
+        spec, dev = self.spec, self.d_logits.device
+        h = self.h
+        up = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        self.d_logits.copy_(h["logits"], non_blocking=True)
+        idx, adv, mask, dloss, old, ref = up(h["idx"]), up(h["adv"]), up(h["mask"]), up(h["dloss"]), up(h["old"]), up(h["ref"])
+        f = rp.grpo_loss_fused(self.d_logits, idx, adv, dloss, T=spec.T, beta=spec.beta, eps_low=spec.eps_low,
+                               eps_high=spec.eps_high, old_logp=old, ref_logp=ref, mask=mask, with_entropy=True,
+                               dlogits=self.dlogits)
+        self.h_dl.copy_(f["dlogits"], non_blocking=True)
+        self.h_loss.copy_(f["loss"], non_blocking=True)
+
+
 class EntropySlsmStep:
     """entropy_from_logits, selective_log_softmax_fwd, selective_log_softmax_bwd."""
 
@@ -354,10 +412,10 @@ def make_spec(args):
     return W.get(args.workload, **over)
 
 
-def make_step(spec, seed, device):
+def make_step(spec, seed, device, fused=False):
     if spec.name.startswith("entropy_slsm"):
         return EntropySlsmStep(spec, seed, device)
-    return GrpoStep(spec, seed, device)
+    return FusedStep(spec, seed, device) if fused else GrpoStep(spec, seed, device)
 
 
 # ---------------------------------------------------------------------------
@@ -498,6 +556,8 @@ def parse_args(argv=None):
     ap.add_argument("--beta", type=float, default=None)
     ap.add_argument("--zero-seqs", type=int, default=None)
     ap.add_argument("--strided", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="GRPO workloads: time grpo_loss_fused (one kernel) instead of grpo_loss_fwd + grpo_loss_bwd")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -599,7 +659,7 @@ def main(argv=None):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     spec = make_spec(args)
-    step = make_step(spec, args.seed + rank, device)
+    step = make_step(spec, args.seed + rank, device, fused=args.fused)
     flush_buf = L2Flush(device)
 
     # one untimed step to classify rows, then calibrate the step count

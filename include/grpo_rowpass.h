@@ -149,6 +149,29 @@ grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const flo
                           int32_t* dev_err, grpo_stream_t stream);
 
 /*
+ * grpo_loss_fused -- grpo_loss_fwd and grpo_loss_bwd in one kernel, for per-token loss
+ * weights dloss that are known before the forward (a fixed normalisation such as
+ * mask / (B * completion length)).
+ *
+ * Defined by "Liger GRPO meets TRL", section 4 ([Liger-TRL]: the loss computes the
+ * gradients during its forward so the logits are not kept for a later backward), with the
+ * forward and backward definitions of grpo_loss_fwd / grpo_loss_bwd above.  Each row is
+ * read once for its statistic; the row factor g is decided from the row's own logp (the
+ * value written to logp); a row with g == 0.0 is filled with +0.0, any other row is swept
+ * again (the same CTA re-reads what it just read, mostly from L2) to write dlogits.
+ *
+ * Arguments: those of grpo_loss_fwd, plus dloss [B*L] fp32 and dlogits as in
+ * grpo_loss_bwd (same dtype/B/L/V as logits; may alias logits exactly).  The outputs equal
+ * those of grpo_loss_fwd followed by grpo_loss_bwd on the same inputs (dlogits to within
+ * the rounding of the summation order of the idx element).
+ */
+grpo_status grpo_loss_fused(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                            const float* ref_logp, const float* adv, const uint8_t* mask, const float* dloss,
+                            float T, float beta, float eps_low, float eps_high, float* loss, float* logp,
+                            float* lse, float* kl, uint8_t* is_clipped, float* entropy,
+                            const grpo_rows* dlogits, int32_t* dev_err, grpo_stream_t stream);
+
+/*
  * entropy_from_logits -- H_r = sum_j p_j (lse_r - z_j) per row, one fused pass.
  *
  * Defined by [axolotl] "1. benchmarks/bench_entropy.py": the original takes

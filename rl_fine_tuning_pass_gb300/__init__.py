@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     GrpoError,
     entropy_from_logits,
     grpo_loss_bwd,
+    grpo_loss_fused,
     grpo_loss_fwd,
     load_library,
     selective_log_softmax_bwd,

@@ -21,8 +21,8 @@ GRPO_OK, GRPO_ERR_INVALID_ARG, GRPO_ERR_UNSUPPORTED, GRPO_ERR_CUDA = 0, 1, 2, 3
 GRPO_FP32, GRPO_BF16 = 0, 1
 GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
 
-EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "entropy_from_logits", "selective_log_softmax_fwd",
-            "selective_log_softmax_bwd", "grpo_status_string")
+EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_logits",
+            "selective_log_softmax_fwd", "selective_log_softmax_bwd", "grpo_status_string")
 
 
 class GrpoRows(ctypes.Structure):
@@ -57,6 +57,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     sig = {
         "grpo_loss_fwd": [rows_p, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P],
         "grpo_loss_bwd": [rows_p, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, rows_p, _P, _P],
+        "grpo_loss_fused": [rows_p, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, rows_p, _P, _P],
         "entropy_from_logits": [rows_p, _F, _P, _P],
         "selective_log_softmax_fwd": [rows_p, _P, _F, _P, _P, _P, _P],
         "selective_log_softmax_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P, _P],
@@ -170,6 +171,35 @@ def grpo_loss_bwd(logits, idx, adv, dloss, logp, lse, *, T, beta, eps_low, eps_h
         _stream(logits.device))
     _check("grpo_loss_bwd", st)
     return dlogits
+
+
+def grpo_loss_fused(logits, idx, adv, dloss, *, T, beta, eps_low, eps_high, old_logp=None, ref_logp=None,
+                    mask=None, with_kl=True, with_is_clipped=True, with_entropy=False, dlogits=None, dev_err=None):
+    """GRPO forward and backward in one pass (dloss known in advance); returns the forward's
+    dict plus "dlogits"."""
+    B, L = _shape(logits)
+    R = B * L
+    dev = logits.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"loss": torch.empty(R, **f32), "logp": torch.empty(R, **f32), "lse": torch.empty(R, **f32)}
+    out["kl"] = torch.empty(R, **f32) if with_kl else None
+    out["is_clipped"] = torch.empty(R, dtype=torch.uint8, device=dev) if with_is_clipped else None
+    out["entropy"] = torch.empty(R, **f32) if with_entropy else None
+    if dlogits is None:
+        dlogits = torch.empty(logits.shape, dtype=logits.dtype, device=dev)
+    x, dx = rows_of(logits), rows_of(dlogits)
+    st = load_library().grpo_loss_fused(
+        ctypes.byref(x), _ptr(idx, torch.int64, R, "idx"), _ptr(old_logp, torch.float32, R, "old_logp"),
+        _ptr(ref_logp, torch.float32, R, "ref_logp"), _ptr(adv, torch.float32, B, "adv"),
+        _ptr(mask, torch.uint8, R, "mask"), _ptr(dloss, torch.float32, R, "dloss"), float(T), float(beta),
+        float(eps_low), float(eps_high), out["loss"].data_ptr(), out["logp"].data_ptr(), out["lse"].data_ptr(),
+        _ptr(out["kl"], torch.float32, R, "kl"), _ptr(out["is_clipped"], torch.uint8, R, "is_clipped"),
+        _ptr(out["entropy"], torch.float32, R, "entropy"), ctypes.byref(dx),
+        _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(dev))
+    _check("grpo_loss_fused", st)
+    res = {k: v for k, v in out.items() if v is not None}
+    res["dlogits"] = dlogits
+    return res
 
 
 def entropy_from_logits(logits, *, T=1.0):

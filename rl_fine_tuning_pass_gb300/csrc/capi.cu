@@ -202,6 +202,50 @@ grpo_status grpo_loss_bwd(const grpo_rows* logits, const int64_t* idx, const flo
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+grpo_status grpo_loss_fused(const grpo_rows* logits, const int64_t* idx, const float* old_logp,
+                            const float* ref_logp, const float* adv, const uint8_t* mask, const float* dloss,
+                            float T, float beta, float eps_low, float eps_high, float* loss, float* logp,
+                            float* lse, float* kl, uint8_t* is_clipped, float* entropy,
+                            const grpo_rows* dlogits, int32_t* dev_err, grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (rows_of(logits) == 0) return GRPO_OK;
+  if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(loss) ||
+      !ok_f32(logp) || !ok_f32(lse) || !ok_opt_f32(kl) || !ok_opt_f32(entropy) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  grpo::FusedParams q{};
+  FwdParams& p = q.f;
+  p.x = view_of(logits);
+  p.idx = idx;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.logp = logp;
+  p.lse = lse;
+  p.kl = kl;
+  p.is_clipped = is_clipped;
+  p.entropy = entropy;
+  p.dev_err = dev_err;
+  q.dx = grpo::OutView{dlogits->ptr, dlogits->L, dlogits->stride_b, dlogits->stride_l, static_cast<int>(dlogits->V)};
+  q.dloss = dloss;
+  q.T = T;
+  return from_cuda(grpo::launch_fused(logits->dtype, q, rows, same_phase, device_sms(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy,
                                 grpo_stream_t stream) {
   grpo_status st = check_rows(logits);

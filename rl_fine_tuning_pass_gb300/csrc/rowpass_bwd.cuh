@@ -22,18 +22,22 @@
 namespace grpo {
 namespace {
 
-// Per-row factor g of the GRPO loss (fp32, same operation order as the definition).
-__device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b) {
-  if (p.mask != nullptr && p.mask[r] == 0) return 0.f;
-  const float logp = p.logp[r];
-  const float ratio = p.old_logp ? expf(logp - p.old_logp[r]) : 1.f;
-  const float A = p.adv[b];
-  const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
+// Per-row factor g of the GRPO loss of an unmasked token from its logp (fp32, same
+// operation order as the definition).
+__device__ __forceinline__ float grpo_factor(float logp, const float* old_logp, const float* ref_logp, float A,
+                                             float dloss, float beta, float lo, float hi, float T, int64_t r) {
+  const float ratio = old_logp ? expf(logp - old_logp[r]) : 1.f;
+  const float clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
   // unclipped branch is the minimum (ties included): d(-ratio*A)/dlogp; else constant
   const float dpg = (ratio * A <= clipped * A) ? -A * ratio : 0.f;
   float dkl = 0.f;
-  if (p.beta != 0.f) dkl = -p.beta * expm1f(p.ref_logp[r] - logp);  // beta (1 - e^(ref - logp))
-  return (dpg + dkl) * p.dloss[r] / p.T;
+  if (beta != 0.f) dkl = -beta * expm1f(ref_logp[r] - logp);  // beta (1 - e^(ref - logp))
+  return (dpg + dkl) * dloss / T;
+}
+
+__device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b) {
+  if (p.mask != nullptr && p.mask[r] == 0) return 0.f;
+  return grpo_factor(p.logp[r], p.old_logp, p.ref_logp, p.adv[b], p.dloss[r], p.beta, p.lo, p.hi, p.T, r);
 }
 
 // The part of a row one CTA handles: vectors [v0, v1), plus the scalar head and tail.

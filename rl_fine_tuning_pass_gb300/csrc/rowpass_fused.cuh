@@ -1,0 +1,132 @@
+// Fused single-read GRPO forward + backward, for per-token loss weights (dloss) that are
+// known before the forward ("Liger GRPO meets TRL", section 4: the chunked loss computes
+// the gradients during the forward, so the logits never have to be kept for a later
+// backward).  One CTA per row: the row is streamed once for the statistic and the
+// forward outputs; thread 0 decides the row factor g from this row's own logp (the same
+// fp32 value the forward writes); a row with g == 0 is filled with +0.0, any other row
+// is swept a second time to write g * (1[j == idx] - p_j).  The second sweep re-reads
+// the row the same CTA has just read, so on the GPU it is mostly served by L2.
+#pragma once
+
+#include "rowpass_bwd.cuh"
+#include "rowpass_fwd.cuh"
+
+namespace grpo {
+namespace {
+
+template <class E, int THREADS, int UNROLL, bool kH, bool SAME_PHASE>
+__global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
+  constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
+  constexpr int VEC = E::kVec;
+  using S = typename E::storage;
+  const FwdParams& p = q.f;
+
+  const int64_t r = blockIdx.x;
+  const int64_t b = r / p.x.L;
+  const int64_t l = r - b * p.x.L;
+  const int tid = threadIdx.x;
+  const int V = p.x.V;
+  const float c = p.c;
+  S* out = static_cast<S*>(q.dx.ptr) + b * q.dx.sb + l * q.dx.sl;
+  const RowSplit osp = split_row<E>(out, V);
+  const Span osn = whole_row(osp);
+
+  if (p.mask != nullptr && p.mask[r] == 0) {  // masked token: zero outputs, zero gradient row
+    if (tid == 0) masked_row_outputs(p, r);
+    fill_span<E, THREADS>(out, osp, osn, 0u);
+    return;
+  }
+
+  const S* row = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
+  int idx = 0;
+  bool bad_idx = false;
+  float x_idx = 0.f;
+  if (tid == 0) {
+    const int64_t id = p.idx[r];
+    bad_idx = id < 0 || id >= V;
+    idx = bad_idx ? 0 : static_cast<int>(id);
+    x_idx = E::load_scalar(row + idx);
+  }
+
+  // sweep 1: the online statistic (as in rowstats_kernel)
+  Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const RowSplit sp = split_row<E>(row, V);
+  if (tid < sp.head) run_scalar<kH>(rs, E::load_scalar(row + tid), c);
+  if (tid < sp.tail) run_scalar<kH>(rs, E::load_scalar(row + sp.head + sp.nvec * VEC + tid), c);
+  const uint4* vb = reinterpret_cast<const uint4*>(row + sp.head);
+  int i = tid;
+  for (; i + (UNROLL - 1) * THREADS < sp.nvec; i += UNROLL * THREADS) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) v[k] = ld_v4(vb + i + k * THREADS);  // coherent: dlogits may alias
+    run_vectors<E, kH>(rs, v, c);
+  }
+  for (; i < sp.nvec; i += THREADS) {
+    uint4 v[1];
+    v[0] = ld_v4(vb + i);
+    run_vectors<E, kH>(rs, v, c);
+  }
+  Stat mine;
+  mine.a = rs.a;
+  mine.s = rs.s.x + rs.s.y;
+  mine.u = rs.u.x + rs.u.y;
+  const Stat st = stat_block_reduce<THREADS>(mine);
+
+  // forward outputs and the row factor, decided once and shared with the CTA
+  __shared__ float sh_g, sh_nK;
+  __shared__ int sh_idx;
+  if (tid == 0) {
+    float logp = 0.f, lse = 0.f;
+    row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx, &logp, &lse);
+    const float g = grpo_factor(logp, p.old_logp, p.ref_logp, p.adv[b], q.dloss[r], p.beta, p.lo, p.hi, q.T, r);
+    sh_g = g;
+    sh_nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
+    sh_idx = bad_idx ? -1 : idx;
+  }
+  __syncthreads();
+  const float g = sh_g;
+  if (g == 0.f) {  // early-out: +0.0 over the row
+    fill_span<E, THREADS>(out, osp, osn, 0u);
+    return;
+  }
+  const int gidx = sh_idx;
+  if (gidx < 0) {  // out-of-range idx (already reported by the forward outputs)
+    fill_span<E, THREADS>(out, osp, osn, E::kNaNPair);
+    return;
+  }
+
+  // sweep 2: dlogits (d_j = -sign(g) |g| p_j, and g (1 - p_idx) at idx)
+  bool owner = false;
+  const float nK = sh_nK;
+  const float q_part =
+      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true>(row, out, osp, osn, gidx, c, nK, owner)
+              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false>(row, out, osp, osn, gidx, c, nK, owner);
+  const float q_total = block_sum_all<THREADS>(q_part);
+  if (owner) E::store_scalar(out + gidx, g > 0.f ? q_total : -q_total);
+}
+
+template <class E, int THREADS, int U, bool kH>
+cudaError_t launch_fused_h(const FusedParams& q, int64_t rows, bool same_phase, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(rows));
+  if (same_phase) fused_kernel<E, THREADS, U, kH, true><<<grid, THREADS, 0, s>>>(q);
+  else fused_kernel<E, THREADS, U, kH, false><<<grid, THREADS, 0, s>>>(q);
+  return cudaGetLastError();
+}
+
+template <class E, int THREADS, int U>
+cudaError_t launch_fused_t(const FusedParams& q, int64_t rows, bool same_phase, cudaStream_t s) {
+  return q.f.entropy ? launch_fused_h<E, THREADS, U, true>(q, rows, same_phase, s)
+                     : launch_fused_h<E, THREADS, U, false>(q, rows, same_phase, s);
+}
+
+template <class E>
+cudaError_t launch_fused_dtype(const FusedParams& q, int64_t rows, bool same_phase, int sms, cudaStream_t s) {
+  switch (pick_threads_fused(q.f.x.V, sizeof(typename E::storage), rows, sms)) {
+    case 64: return launch_fused_t<E, 64, kUnroll>(q, rows, same_phase, s);
+    case 128: return launch_fused_t<E, 128, kUnroll>(q, rows, same_phase, s);
+    default: return launch_fused_t<E, 256, kUnroll>(q, rows, same_phase, s);
+  }
+}
+
+}  // namespace
+}  // namespace grpo

@@ -73,10 +73,12 @@ __device__ __forceinline__ void run_vectors(Running& rs, uint4 (&v)[N], float c)
   }
 }
 
-// Outputs of one row from its merged statistic (thread 0).
+// Outputs of one row from its merged statistic (thread 0); returns logp and lse through
+// the optional pointers.
 template <int MODE>
 __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int64_t b, const Stat& st, float c,
-                                             float x_idx, bool bad_idx) {
+                                             float x_idx, bool bad_idx, float* logp_out = nullptr,
+                                             float* lse_out = nullptr) {
   constexpr bool kH = MODE == kFwdEntropy || MODE == kFwdGrpoH;
   constexpr bool kGrpo = MODE == kFwdGrpo || MODE == kFwdGrpoH;
   const float ln_s = logf(st.s);
@@ -92,6 +94,8 @@ __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int6
   if (bad_idx && p.dev_err) atomicOr(p.dev_err, GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT);
   p.logp[r] = logp;
   p.lse[r] = lse;
+  if (logp_out) *logp_out = logp;
+  if (lse_out) *lse_out = lse;
   if (!kGrpo) return;
 
   const float ratio = p.old_logp ? expf(logp - p.old_logp[r]) : 1.f;

@@ -27,6 +27,13 @@ inline int pick_threads_fwd(int V, int esize, long long rows, int sms) {
   if (rows <= 24LL * sms || bytes <= 8192) return 64;
   return 256;
 }
+// Fused forward + backward: 256-thread CTAs (64 for short rows), as for the backward.
+inline int pick_threads_fused(int V, int esize, long long rows, int sms) {
+  (void)rows;
+  (void)sms;
+  const long long bytes = static_cast<long long>(V) * esize;
+  return bytes <= 8192 ? 64 : 256;
+}
 inline int pick_threads_bwd(int V, int esize, long long rows, int sms) {
   (void)rows;
   (void)sms;
@@ -97,6 +104,15 @@ struct BwdParams {
   int32_t* dev_err;
 };
 
+// Fused forward + backward: the forward's inputs and outputs, the gradient rows and the
+// per-token loss weights, known before the forward.
+struct FusedParams {
+  FwdParams f;
+  OutView dx;
+  const float* dloss;
+  float T;
+};
+
 // Kernel launchers, one translation unit per element type (compiled in parallel).
 cudaError_t launch_fwd_bf16(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
 cudaError_t launch_fwd_f32(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
@@ -104,6 +120,15 @@ cudaError_t launch_bwd_bf16(bool grpo, bool same_phase, const BwdParams& p, int6
                             cudaStream_t stream);
 cudaError_t launch_bwd_f32(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
                            cudaStream_t stream);
+
+cudaError_t launch_fused_bf16(const FusedParams& q, int64_t rows, bool same_phase, int sms, cudaStream_t stream);
+cudaError_t launch_fused_f32(const FusedParams& q, int64_t rows, bool same_phase, int sms, cudaStream_t stream);
+
+inline cudaError_t launch_fused(int dtype, const FusedParams& q, int64_t rows, bool same_phase, int sms,
+                                cudaStream_t stream) {
+  return dtype == 1 ? launch_fused_bf16(q, rows, same_phase, sms, stream)
+                    : launch_fused_f32(q, rows, same_phase, sms, stream);
+}
 
 // Launch the forward over `rows` rows.  dtype: 0 fp32, 1 bf16.
 inline cudaError_t launch_fwd(int mode, int dtype, const FwdParams& p, int64_t rows, int sms,

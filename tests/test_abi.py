@@ -101,6 +101,23 @@ def test_dlogits_validation(lib):
     assert bwd(lib, x, rows(ptr=FAKE + (1 << 20)), T=0.0) == INV
 
 
+def test_fused_validation(lib):
+    x = rows()
+    def fused(dx, T=1.0, dloss=FAKE, beta=0.0, ref=None):
+        return lib.grpo_loss_fused(ctypes.byref(x), FAKE, None, ref, FAKE, None, dloss, T, beta, 0.2, 0.2,
+                                   FAKE, FAKE + 64, FAKE + 128, None, None, None, ctypes.byref(dx), None, None)
+    far = rows(ptr=FAKE + (1 << 20))
+    assert fused(rows(ptr=FAKE + 128)) == INV          # partial overlap with the logits
+    assert fused(far, dloss=None) == INV               # dloss required
+    assert fused(far, T=0.0) == INV
+    assert fused(far, beta=0.1) == INV                 # ref_logp required when beta > 0
+    assert fused(rows(ptr=FAKE + (1 << 20), V=32)) == INV
+    x0 = rows(B=0)
+    assert lib.grpo_loss_fused(ctypes.byref(x0), None, None, None, None, None, None, 1.0, 0.0, 0.2, 0.2,
+                               None, None, None, None, None, None, ctypes.byref(rows(B=0, ptr=None)),
+                               None, None) == binding.GRPO_OK
+
+
 def test_slsm_and_entropy_validation(lib):
     x = rows()
     assert lib.selective_log_softmax_fwd(ctypes.byref(x), None, 1.0, FAKE, FAKE, None, None) == INV

@@ -460,3 +460,80 @@ def test_empty_inputs_launch_nothing():
     assert lp.numel() == 0
     f = rp.grpo_loss_fwd(x, idx, torch.empty(0, device=DEV), T=1.0, beta=0.0, eps_low=0.2, eps_high=0.2)
     assert f["loss"].numel() == 0
+
+
+# ---------------------------------------------------------------------------
+# fused single-read forward + backward
+# ---------------------------------------------------------------------------
+
+def run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=None):
+    dev_err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t = lambda a: None if a is None else torch.as_tensor(a, dtype=torch.float32).to(DEV)
+    f = rp.grpo_loss_fused(inp.logits, inp.idx, inp.adv, inp.dloss, T=T, beta=beta, eps_low=el, eps_high=eh,
+                           old_logp=t(old), ref_logp=t(ref), mask=inp.mask, with_entropy=True, dlogits=dlogits,
+                           dev_err=dev_err)
+    torch.cuda.synchronize()
+    return f, f["dlogits"], int(dev_err.item())
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_fused_tiny_fp32_every_row(seed):
+    spec = W.get("tiny_fp32")
+    inp = W.generate(spec, seed, device=DEV)
+    T, beta, el, eh = f32(spec.T), f32(spec.beta), f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    f, dl, err = run_gpu_fused(inp, old, ref, T, beta, el, eh)
+    assert err == 0
+    compare_grpo_rows(inp, f, dl, np.arange(spec.rows), old, ref, T, beta, el, eh, f"fused tiny s{seed}")
+
+
+def test_fused_pages_workload_every_row_and_matches_separate():
+    spec = W.get("grpo_b4_l512_v32000")
+    inp = W.generate(spec, 0, device=DEV)
+    T, beta, el, eh = f32(spec.T), 0.0, f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    f, dl, err = run_gpu_fused(inp, old, ref, T, beta, el, eh)
+    assert err == 0
+    for r0 in range(0, spec.rows, 256):
+        compare_grpo_rows(inp, f, dl, np.arange(r0, r0 + 256), old, ref, T, beta, el, eh, "fused pages")
+    # same zero rows and (to within the idx element's summation order) the same gradient as fwd + bwd
+    fs, dls, _ = run_gpu_grpo(inp, old, ref, T, beta, el, eh)
+    assert torch.equal(f["is_clipped"], fs["is_clipped"])
+    zf = (dl.reshape(spec.rows, -1).view(torch.int16) == 0).all(dim=1)
+    zs = (dls.reshape(spec.rows, -1).view(torch.int16) == 0).all(dim=1)
+    assert torch.equal(zf, zs) and int(zf.sum()) > spec.rows // 2
+    diff = (dl.float() - dls.float()).abs()
+    ulp = torch.maximum(dls.float().abs(), dl.float().abs()) * 2.0 ** -7
+    assert bool((diff <= ulp + 1e-30).all())
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000])
+@pytest.mark.parametrize("offset,extra", [(0, 0), (3, 1)])
+def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
+    B, L = 2, 5
+    R = B * L
+    seed = V * 7 + offset
+    x, idx, adv, mask, dloss = edge_inputs(B, L, V, dtype, offset, extra, seed)
+    T, beta, el, eh = f32(0.8), f32(0.05), f32(0.2), f32(0.28)
+    xo = rows_f64(select_rows(x, np.arange(R)))
+    lp, _ = oracle.selective_log_softmax(xo, idx.cpu().numpy(), T)
+    g = torch.Generator().manual_seed(V)
+    old = oracle.round_to_fp32(lp + torch.randn(R, generator=g).double().numpy() * 0.3)
+    ref = oracle.round_to_fp32(lp + torch.randn(R, generator=g).double().numpy() * 0.1)
+    inp = W.Inputs(W.get("tiny_fp32", B=B, L=L, V=V), x, idx, adv, mask, dloss, None, None, None, None)
+    dl_buf = torch.empty(B * L * (V + 2) + 9, dtype=dtype, device=DEV)
+    dl_view = torch.as_strided(dl_buf, (B, L, V), (L * (V + 2), V + 2, 1), 1 + offset)  # out of phase
+    f, dl, err = run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=dl_view)
+    assert err == 0
+    compare_grpo_rows(inp, f, dl, np.arange(R), old, ref, T, beta, el, eh, f"fused edge V={V}")
+    x2, _ = strided_logits(B, L, V, dtype, offset, extra, seed)
+    same_layout, _ = strided_logits(B, L, V, dtype, offset, extra, seed + 99)
+    _, dl_same, _ = run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=same_layout)
+    inp2 = W.Inputs(inp.spec, x2, idx, adv, mask, dloss, None, None, None, None)
+    _, dl2, err2 = run_gpu_fused(inp2, old, ref, T, beta, el, eh, dlogits=x2)   # in place
+    assert err2 == 0 and dl2.data_ptr() == x2.data_ptr()
+    assert torch.equal(bf16_or_f32_bits(select_rows(dl2, np.arange(R))),
+                       bf16_or_f32_bits(select_rows(dl_same, np.arange(R))))
