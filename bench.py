@@ -357,7 +357,7 @@ class EntropySlsmStep:
         self.stream = torch.cuda.current_stream(device).cuda_stream
         T = spec.T
         self._e, self._f, self._b = lib.entropy_from_logits, lib.selective_log_softmax_fwd, lib.selective_log_softmax_bwd
-        self.e_args = (ctypes.byref(self.x_desc), T, _p(self.H), self.stream)
+        self.e_args = (ctypes.byref(self.x_desc), T, _p(self.H), None, self.stream)
         self.f_args = (ctypes.byref(self.x_desc), _p(inp.idx), T, _p(self.logp), _p(self.lse), None, self.stream)
         self.b_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(inp.upstream), _p(self.lse), T,
                        ctypes.byref(self.dx_desc), None, self.stream)

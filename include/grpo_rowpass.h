@@ -179,9 +179,27 @@ grpo_status grpo_loss_fused(const grpo_rows* logits, const int64_t* idx, const f
  * describes reads strided logits in place.  T = 1 reproduces the page's definition.
  *
  *   logits   [B, L, V] bf16 or fp32;  T > 0 finite;  entropy [B*L] fp32 output
+ *   lse      [B*L] fp32 output, or NULL (needed by entropy_from_logits_bwd)
+ * A logit of -inf has p = 0 and adds 0 (the limit of p log p).
  */
-grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy,
+grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy, float* lse,
                                 grpo_stream_t stream);
+
+/*
+ * entropy_from_logits_bwd -- gradient of sum_r dentropy_r * H_r with respect to the logits:
+ *   dlogits_rj = -(dentropy_r / T) p_j (log p_j + H_r).
+ *
+ * The derivative of the entropy definition of [axolotl] "1. benchmarks/bench_entropy.py"
+ * (the pages print no entropy backward).  A row whose dentropy_r / T is exactly 0.0 is
+ * written as +0.0 without reading its logits (as in the other backward passes).
+ *
+ *   logits [B, L, V];  dentropy [B*L] fp32 upstream gradient of H
+ *   lse, entropy [B*L] fp32 as written by entropy_from_logits (or grpo_loss_fwd) for the
+ *   same logits and T;  dlogits as in grpo_loss_bwd (may alias logits exactly)
+ */
+grpo_status entropy_from_logits_bwd(const grpo_rows* logits, const float* dentropy, const float* lse,
+                                    const float* entropy, float T, const grpo_rows* dlogits,
+                                    grpo_stream_t stream);
 
 /*
  * selective_log_softmax_fwd -- logp_r = log_softmax(x_r / T)[idx_r], and lse_r.

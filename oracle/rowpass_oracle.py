@@ -54,6 +54,7 @@ __all__ = [
     "grpo_loss_fwd",
     "grpo_loss_bwd",
     "selective_log_softmax_bwd",
+    "entropy_from_logits_bwd",
     "per_row",
 ]
 
@@ -336,3 +337,23 @@ def selective_log_softmax_bwd(x, idx, dlogp_upstream, T):
     """
     g = np.asarray(dlogp_upstream, dtype=np.float64) / np.float64(T)
     return softmax_gather_grad(x, idx, g, T), g
+
+
+def entropy_from_logits_bwd(x, dentropy, T):
+    """Gradient of sum_r u_r * H_r with respect to the logits (fp64), u = dentropy.
+
+    H = -sum_j p_j log p_j with p = softmax(x / T) (the entropy of [axolotl],
+    "1. benchmarks/bench_entropy.py"); dH/dx_k = -(p_k / T) (log p_k + H).  The pages
+    print no entropy backward: this is the derivative of their definition.  Rows with
+    u_r == 0 are +0.0 (as for the other backward passes).  Returns (dlogits, g) with
+    g_r = -u_r / T.
+    """
+    z, lse = log_softmax_rows(x, T)
+    H = entropy_from_logits(x, T)
+    g = -np.asarray(dentropy, dtype=np.float64) / np.float64(T)
+    with np.errstate(invalid="ignore", over="ignore"):
+        logp = z - lse[:, None]
+        p = np.exp(logp)
+        d = g[:, None] * np.where(p == 0.0, 0.0, p * (logp + H[:, None]))
+    d[g == 0.0] = 0.0                         # +0.0 rows, also for u == -0.0
+    return d, g

@@ -8,6 +8,7 @@ generators.  The library is loaded on first use; importing the package needs no 
 from .binding import (  # noqa: F401
     GrpoError,
     entropy_from_logits,
+    entropy_from_logits_bwd,
     grpo_loss_bwd,
     grpo_loss_fused,
     grpo_loss_fwd,

@@ -22,7 +22,8 @@ GRPO_FP32, GRPO_BF16 = 0, 1
 GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
 
 EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_logits",
-            "selective_log_softmax_fwd", "selective_log_softmax_bwd", "grpo_status_string")
+            "entropy_from_logits_bwd", "selective_log_softmax_fwd", "selective_log_softmax_bwd",
+            "grpo_status_string")
 
 
 class GrpoRows(ctypes.Structure):
@@ -58,7 +59,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "grpo_loss_fwd": [rows_p, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P],
         "grpo_loss_bwd": [rows_p, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, rows_p, _P, _P],
         "grpo_loss_fused": [rows_p, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, rows_p, _P, _P],
-        "entropy_from_logits": [rows_p, _F, _P, _P],
+        "entropy_from_logits": [rows_p, _F, _P, _P, _P],
+        "entropy_from_logits_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P],
         "selective_log_softmax_fwd": [rows_p, _P, _F, _P, _P, _P, _P],
         "selective_log_softmax_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P, _P],
     }
@@ -202,14 +204,30 @@ def grpo_loss_fused(logits, idx, adv, dloss, *, T, beta, eps_low, eps_high, old_
     return res
 
 
-def entropy_from_logits(logits, *, T=1.0):
-    """Per-row entropy [B*L] fp32."""
+def entropy_from_logits(logits, *, T=1.0, return_lse=False):
+    """Per-row entropy [B*L] fp32 (and lse [B*L] when return_lse)."""
     B, L = _shape(logits)
     out = torch.empty(B * L, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(B * L, dtype=torch.float32, device=logits.device) if return_lse else None
     x = rows_of(logits)
-    st = load_library().entropy_from_logits(ctypes.byref(x), float(T), out.data_ptr(), _stream(logits.device))
+    st = load_library().entropy_from_logits(ctypes.byref(x), float(T), out.data_ptr(),
+                                            None if lse is None else lse.data_ptr(), _stream(logits.device))
     _check("entropy_from_logits", st)
-    return out
+    return (out, lse) if return_lse else out
+
+
+def entropy_from_logits_bwd(logits, dentropy, lse, entropy, *, T=1.0, dlogits=None):
+    """dlogits of sum_r dentropy_r * H_r (allocated like logits unless given)."""
+    B, L = _shape(logits)
+    R = B * L
+    if dlogits is None:
+        dlogits = torch.empty(logits.shape, dtype=logits.dtype, device=logits.device)
+    x, dx = rows_of(logits), rows_of(dlogits)
+    st = load_library().entropy_from_logits_bwd(
+        ctypes.byref(x), _ptr(dentropy, torch.float32, R, "dentropy"), _ptr(lse, torch.float32, R, "lse"),
+        _ptr(entropy, torch.float32, R, "entropy"), float(T), ctypes.byref(dx), _stream(logits.device))
+    _check("entropy_from_logits_bwd", st)
+    return dlogits
 
 
 def selective_log_softmax_fwd(logits, idx, *, T=1.0, dev_err=None):

@@ -246,13 +246,13 @@ grpo_status grpo_loss_fused(const grpo_rows* logits, const int64_t* idx, const f
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
-grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy,
+grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy, float* lse,
                                 grpo_stream_t stream) {
   grpo_status st = check_rows(logits);
   if (st != GRPO_OK) return st;
   if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
   if (rows_of(logits) == 0) return GRPO_OK;
-  if (!ok_f32(entropy)) return GRPO_ERR_INVALID_ARG;
+  if (!ok_f32(entropy) || !ok_opt_f32(lse)) return GRPO_ERR_INVALID_ARG;
   const int64_t rows = logits->B * logits->L;
   if (rows == 0) return GRPO_OK;
   FwdParams p{};
@@ -260,7 +260,32 @@ grpo_status entropy_from_logits(const grpo_rows* logits, float T, float* entropy
   p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
   p.invT = static_cast<float>(1.0 / static_cast<double>(T));
   p.entropy = entropy;
+  p.lse = lse;
   return from_cuda(grpo::launch_fwd(grpo::kFwdEntropy, logits->dtype, p, rows, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status entropy_from_logits_bwd(const grpo_rows* logits, const float* dentropy, const float* lse,
+                                    const float* entropy, float T, const grpo_rows* dlogits,
+                                    grpo_stream_t stream) {
+  grpo_status st = check_rows(logits);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits, dlogits, &same_phase)) != GRPO_OK) return st;
+  if (rows_of(logits) == 0) return GRPO_OK;
+  if (!ok_f32(dentropy) || !ok_f32(lse) || !ok_f32(entropy)) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = logits->B * logits->L;
+  BwdParams p{};
+  p.x = view_of(logits);
+  p.dx = grpo::OutView{dlogits->ptr, dlogits->L, dlogits->stride_b, dlogits->stride_l,
+                       static_cast<int>(dlogits->V)};
+  p.lse = lse;
+  p.dentropy = dentropy;
+  p.entropy = entropy;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.T = T;
+  return from_cuda(grpo::launch_entgrad(logits->dtype, same_phase, p, rows, device_sms(),
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 grpo_status selective_log_softmax_fwd(const grpo_rows* logits, const int64_t* idx, float T,

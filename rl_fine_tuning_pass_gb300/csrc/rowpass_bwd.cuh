@@ -172,6 +172,89 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   if (owner) E::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
 
+// Entropy backward: d_j = g p_j (log p_j + H), g = -dH / T.  With |g| folded into the
+// exponent, |g| p_j = 2^{t_j}, t_j = x_j c - K, and log p_j + H = ln2 t_j + (H - ln|g|),
+// so each element costs a packed FMA, one ex2, a packed FMA and a packed multiply.  A
+// -inf logit is raised to -2^60 first, so that a p_j = 0 term is 0 and not 0 * -inf.
+template <class E, int THREADS, int UNROLL, bool SAME_PHASE, bool NEG>
+__device__ __forceinline__ void stream_span_entropy(const typename E::storage* in, typename E::storage* out,
+                                                    const RowSplit& sp, const Span& sn, float c, float nK,
+                                                    float h_shift) {
+  constexpr int VEC = E::kVec;
+  using S = typename E::storage;
+  constexpr float kNeg = -1.152921504606847e18f;  // -2^60
+  const int tid = threadIdx.x;
+  auto scalar = [&](int j) {
+    float x = E::load_scalar_coherent(in + j);
+    if (x < kNeg) x = kNeg;
+    const float t = fmaf(x, c, nK);
+    const float d = ex2(t) * fmaf(kLn2, t, h_shift);
+    E::store_scalar(out + j, NEG ? -d : d);
+  };
+  if (sn.head && tid < sp.head) scalar(tid);
+  if (sn.tail && tid < sp.tail) scalar(sp.head + sp.nvec * VEC + tid);
+  const S* in_body = in + sp.head;
+  uint4* ob = reinterpret_cast<uint4*>(out + sp.head);
+  const float2 c2 = make_float2(c, c), nK2 = make_float2(nK, nK);
+  const float2 ln2 = make_float2(kLn2, kLn2), hs2 = make_float2(h_shift, h_shift);
+  auto process = [&](uint4 v, int i) {
+    E::clamp_low(v);
+    float2 d[E::kPairs];
+#pragma unroll
+    for (int q = 0; q < E::kPairs; ++q) {
+      const float2 t = __ffma2_rn(E::pair(v, q), c2, nK2);
+      const float2 e = make_float2(ex2(t.x), ex2(t.y));
+      d[q] = __fmul2_rn(e, __ffma2_rn(ln2, t, hs2));
+    }
+    st_v4(ob + i, E::template pack_pairs<NEG>(d));
+  };
+  int i = sn.v0 + tid;
+  for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) v[k] = load_vec<E, SAME_PHASE>(in_body, i + k * THREADS);
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
+  }
+  for (; i < sn.v1; i += THREADS) process(load_vec<E, SAME_PHASE>(in_body, i), i);
+}
+
+template <class E, int THREADS, int UNROLL, bool SAME_PHASE>
+__global__ void __launch_bounds__(THREADS) entgrad_kernel(const BwdParams p) {
+  using S = typename E::storage;
+  const int64_t r = blockIdx.x;
+  const int64_t b = r / p.x.L;
+  const int64_t l = r - b * p.x.L;
+  const int V = p.x.V;
+  const float g = -p.dentropy[r] / p.T;
+  S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
+  const RowSplit sp = split_row<E>(out, V);
+  const Span sn = whole_row(sp);
+  if (g == 0.f) {  // early-out: +0.0 over the row, nothing read
+    fill_span<E, THREADS>(out, sp, sn, 0u);
+    return;
+  }
+  const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
+  const float lg = log2f(fabsf(g));
+  const float nK = fmaf(-p.lse[r], kLog2e, lg);        // -(lse*log2e - log2|g|)
+  const float h_shift = fmaf(-kLn2, lg, p.entropy[r]);  // H - ln|g|
+  if (g < 0.f) stream_span_entropy<E, THREADS, UNROLL, SAME_PHASE, true>(in, out, sp, sn, p.c, nK, h_shift);
+  else stream_span_entropy<E, THREADS, UNROLL, SAME_PHASE, false>(in, out, sp, sn, p.c, nK, h_shift);
+}
+
+template <class E>
+cudaError_t launch_entgrad_dtype(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(rows));
+  if (pick_threads_bwd(p.x.V, sizeof(typename E::storage), rows, sms) == 64) {
+    if (same_phase) entgrad_kernel<E, 64, kUnroll, true><<<grid, 64, 0, s>>>(p);
+    else entgrad_kernel<E, 64, kUnroll, false><<<grid, 64, 0, s>>>(p);
+  } else {
+    if (same_phase) entgrad_kernel<E, 256, kUnroll, true><<<grid, 256, 0, s>>>(p);
+    else entgrad_kernel<E, 256, kUnroll, false><<<grid, 256, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
 template <class E, int THREADS, int U, bool GRPO, bool SAME_PHASE>
 cudaError_t launch4(const BwdParams& p, int64_t rows, cudaStream_t s) {
   rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE><<<dim3(static_cast<unsigned>(rows)), THREADS, 0, s>>>(p);

@@ -87,6 +87,7 @@ __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int6
   if (kH) H = ln_s - kLn2 * st.u / st.s;
   if (MODE == kFwdEntropy) {
     p.entropy[r] = H;
+    if (p.lse) p.lse[r] = lse;
     return;
   }
   // z_idx - lse = ln2 * (x_idx * c - a) - ln s, with the same offset a as the stream

@@ -97,6 +97,9 @@ struct BwdParams {
   const float* logp;
   // selective-log-softmax row factor input
   const float* dlogp_up;
+  // entropy backward inputs: upstream gradient of H and the forward's H
+  const float* dentropy;
+  const float* entropy;
   float c;  // log2(e) / T
   float T;
   float beta;
@@ -120,6 +123,15 @@ cudaError_t launch_bwd_bf16(bool grpo, bool same_phase, const BwdParams& p, int6
                             cudaStream_t stream);
 cudaError_t launch_bwd_f32(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
                            cudaStream_t stream);
+
+cudaError_t launch_entgrad_bf16(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t stream);
+cudaError_t launch_entgrad_f32(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t stream);
+
+inline cudaError_t launch_entgrad(int dtype, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                                  cudaStream_t stream) {
+  return dtype == 1 ? launch_entgrad_bf16(same_phase, p, rows, sms, stream)
+                    : launch_entgrad_f32(same_phase, p, rows, sms, stream);
+}
 
 cudaError_t launch_fused_bf16(const FusedParams& q, int64_t rows, bool same_phase, int sms, cudaStream_t stream);
 cudaError_t launch_fused_f32(const FusedParams& q, int64_t rows, bool same_phase, int sms, cudaStream_t stream);

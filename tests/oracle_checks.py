@@ -415,6 +415,36 @@ def check_bwd_closed_form_on_policy(orc):
     _close(dl, (-adv * dloss / T)[:, None] * (onehot - p), 1e-12, 1e-15, "on-policy closed form")
 
 
+def check_entropy_bwd_finite_differences(orc):
+    """dlogits of J = sum_r u_r * H_r(x) against central differences, T != 1; rows sum to 0;
+    u = 0 rows are +0.0."""
+    rng, x, idx, _ = _fd_problem(seed=11, V=17)
+    R, V = x.shape
+    T = 0.6
+    u = rng.standard_normal(R)
+    u[2] = 0.0
+    dl, g = orc.entropy_from_logits_bwd(x, u, T)
+    h = 1e-6
+    for rr in range(R):
+        xp = np.repeat(x[rr:rr + 1], V, axis=0) + h * np.eye(V)
+        xm = np.repeat(x[rr:rr + 1], V, axis=0) - h * np.eye(V)
+        fd = u[rr] * (orc.entropy_from_logits(xp, T) - orc.entropy_from_logits(xm, T)) / (2 * h)
+        _close(dl[rr], fd, 1e-6, 1e-9, f"entropy dlogits row {rr}")
+    assert np.all(np.abs(dl.sum(axis=1)) <= 1e-12 * (1 + np.abs(g)))
+    assert np.all(dl[2] == 0.0) and not np.any(np.signbit(dl[2]))
+
+
+def check_entropy_bwd_closed_form_v2(orc):
+    """V = 2, T = 1: H(q) of a Bernoulli with q = sigmoid(x0 - x1); dH/dx0 = q(1-q) log((1-q)/q)."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((20, 2)) * 3.0
+    dl, _ = orc.entropy_from_logits_bwd(x, np.ones(20), 1.0)
+    q = 1.0 / (1.0 + np.exp(x[:, 1] - x[:, 0]))
+    ref0 = q * (1 - q) * np.log((1 - q) / q)
+    _close(dl[:, 0], ref0, 1e-11, 1e-14, "V=2 entropy gradient")
+    _close(dl[:, 1], -ref0, 1e-11, 1e-14, "V=2 entropy gradient (other column)")
+
+
 ALL_CHECKS = [
     check_bf16_decode_all_patterns,
     check_bf16_rounding_vs_torch,
@@ -434,4 +464,6 @@ ALL_CHECKS = [
     check_slsm_bwd_finite_differences,
     check_bwd_invariants,
     check_bwd_closed_form_on_policy,
+    check_entropy_bwd_finite_differences,
+    check_entropy_bwd_closed_form_v2,
 ]

@@ -83,7 +83,7 @@ def test_zero_rows_is_a_no_op(lib):
     assert fwd(lib, rows(ptr=None, B=0), idx=None, adv=None, outs=0) == binding.GRPO_OK
     assert fwd(lib, rows(L=0)) == binding.GRPO_OK
     x0 = rows(B=0)
-    assert lib.entropy_from_logits(ctypes.byref(x0), 1.0, FAKE, None) == binding.GRPO_OK
+    assert lib.entropy_from_logits(ctypes.byref(x0), 1.0, FAKE, None, None) == binding.GRPO_OK
 
 
 def test_dlogits_validation(lib):
@@ -123,8 +123,14 @@ def test_slsm_and_entropy_validation(lib):
     assert lib.selective_log_softmax_fwd(ctypes.byref(x), None, 1.0, FAKE, FAKE, None, None) == INV
     assert lib.selective_log_softmax_fwd(ctypes.byref(x), FAKE, 0.0, FAKE, FAKE, None, None) == INV
     assert lib.selective_log_softmax_fwd(ctypes.byref(x), FAKE, 1.0, FAKE, FAKE, FAKE + 2, None) == INV
-    assert lib.entropy_from_logits(ctypes.byref(x), 1.0, None, None) == INV
-    assert lib.entropy_from_logits(ctypes.byref(x), math.nan, FAKE, None) == INV
+    assert lib.entropy_from_logits(ctypes.byref(x), 1.0, None, None, None) == INV
+    assert lib.entropy_from_logits(ctypes.byref(x), math.nan, FAKE, None, None) == INV
+    assert lib.entropy_from_logits(ctypes.byref(x), 1.0, FAKE, FAKE + 2, None) == INV
+    far = rows(ptr=FAKE + (1 << 20))
+    assert lib.entropy_from_logits_bwd(ctypes.byref(x), None, FAKE, FAKE, 1.0, ctypes.byref(far), None) == INV
+    assert lib.entropy_from_logits_bwd(ctypes.byref(x), FAKE, FAKE, FAKE, 0.0, ctypes.byref(far), None) == INV
+    assert lib.entropy_from_logits_bwd(ctypes.byref(x), FAKE, FAKE, FAKE, 1.0,
+                                       ctypes.byref(rows(ptr=FAKE + 64)), None) == INV
     dx = rows(ptr=FAKE + 64)
     assert lib.selective_log_softmax_bwd(ctypes.byref(x), FAKE, FAKE, FAKE, 1.0, ctypes.byref(dx),
                                          None, None) == INV

@@ -42,6 +42,11 @@ MUTATIONS = [
     ("logp_sign_of_lse", "logp = z[rows, np.asarray(idx, dtype=np.int64)] - lse",
      "logp = z[rows, np.asarray(idx, dtype=np.int64)] + lse"),
     ("mask_ignored_in_loss", '"loss": np.where(mask, loss, z),', '"loss": loss,'),
+    ("entropy_bwd_sign_of_H", "d = g[:, None] * np.where(p == 0.0, 0.0, p * (logp + H[:, None]))",
+     "d = g[:, None] * np.where(p == 0.0, 0.0, p * (logp - H[:, None]))"),
+    ("entropy_bwd_drops_T", "g = -np.asarray(dentropy, dtype=np.float64) / np.float64(T)",
+     "g = -np.asarray(dentropy, dtype=np.float64)"),
+    ("entropy_zero_rows_not_forced", "    d[g == 0.0] = 0.0 ", "    pass  "),
     ("bf16_truncates", "q = np.rint(np.ldexp(a, -unit_exp))", "q = np.floor(np.ldexp(a, -unit_exp))"),
     ("bf16_ties_away", "q = np.rint(np.ldexp(a, -unit_exp))", "q = np.floor(np.ldexp(a, -unit_exp) + 0.5)"),
     ("bf16_mantissa_bits", "_BF16_MANT_BITS = 7 ", "_BF16_MANT_BITS = 8 "),

@@ -537,3 +537,110 @@ def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
     assert err2 == 0 and dl2.data_ptr() == x2.data_ptr()
     assert torch.equal(bf16_or_f32_bits(select_rows(dl2, np.arange(R))),
                        bf16_or_f32_bits(select_rows(dl_same, np.arange(R))))
+
+
+# ---------------------------------------------------------------------------
+# entropy backward
+# ---------------------------------------------------------------------------
+
+def check_entropy_grad(dl_gpu, x_orc, up, T, H_gpu, lse_gpu, what):
+    """GPU entropy gradient rows vs the oracle.  Each element is g p_j (log p_j + H); the
+    forward's fp32 lse and H enter it, so besides 1 bf16 ulp (or 1e-5 relative for fp32)
+    an element may differ by |g| p_j (|dlse| (|log p_j + H| + 1) + |dH|
+    + 4e-7 (|log p_j| + |H| + 1) (1 + |log p_j + H|)), with dlse, dH the forward's actual
+    deviations from the oracle on that row."""
+    odl, g = oracle.entropy_from_logits_bwd(x_orc, up, T)
+    z, lse = oracle.log_softmax_rows(x_orc, T)
+    H = oracle.entropy_from_logits(x_orc, T)
+    with np.errstate(all="ignore"):
+        logp = z - lse[:, None]
+        p = np.exp(logp)
+        w = np.abs(logp + H[:, None])
+        dlse = np.abs(np.asarray(lse_gpu, dtype=np.float64) - lse)[:, None]
+        dH = np.abs(np.asarray(H_gpu, dtype=np.float64) - H)[:, None]
+        bound = np.abs(g)[:, None] * p * (dlse * (w + 1) + dH + 4e-7 * (np.abs(logp) + np.abs(H)[:, None] + 1) * (1 + w))
+        bound = np.nan_to_num(bound, nan=0.0, posinf=0.0)
+    zero = g == 0.0
+    if np.any(zero):
+        assert_plus_zero(dl_gpu[torch.from_numpy(np.nonzero(zero)[0]).to(dl_gpu.device)], f"{what} zero rows")
+    live = np.nonzero(~zero)[0]
+    if len(live) == 0:
+        return
+    sub = rows_f64(dl_gpu[torch.from_numpy(live).to(dl_gpu.device)])
+    o, bd = odl[live], bound[live]
+    if dl_gpu.dtype == torch.bfloat16:
+        ob = oracle.bf16_bits_to_fp64(oracle.round_to_bf16_bits(o))
+        ulp = np.where(np.abs(ob) >= 2.0 ** -126, np.ldexp(1.0, np.frexp(np.abs(ob))[1] - 8), 2.0 ** -133)
+        tol = ulp + bd + np.where(np.abs(o) < 2.0 ** -126, 2.0 ** -126, 0.0)
+    else:
+        tol = 1e-5 * np.abs(o) + bd + np.where(np.abs(o) < 2.0 ** -126, 2.0 ** -126, 0.0)
+    err = np.abs(sub - o)
+    assert np.array_equal(np.isnan(sub), np.isnan(o)), f"{what}: NaN pattern differs"
+    bad = (err > tol) & ~np.isnan(o)
+    assert not np.any(bad), f"{what}: {int(bad.sum())} elements out of tolerance, worst {err[bad].max():.3g}"
+    assert np.all(np.abs(np.nansum(sub, axis=1)) <= np.abs(g[live]) * (1e-3 + sub.shape[1] * 2.0 ** -8))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_entropy_bwd_tiny_every_row(seed):
+    spec = W.get("tiny_fp32")
+    inp = W.generate(spec, seed, device=DEV)
+    T = 0.8
+    H, lse = rp.entropy_from_logits(inp.logits, T=T, return_lse=True)
+    up = torch.randn(spec.rows, generator=torch.Generator().manual_seed(seed)).float()
+    up[1] = 0.0
+    up[4] = -0.0
+    dl = rp.entropy_from_logits_bwd(inp.logits, up.to(DEV), lse, H, T=T)
+    torch.cuda.synchronize()
+    x = rows_f64(inp.logits.reshape(-1, spec.V))
+    assert_scalar_close(lse, oracle.log_softmax_rows(x, T)[1], "entropy lse output")
+    check_entropy_grad(dl.reshape(spec.rows, -1), x, up.double().numpy(), T, H.cpu().numpy(), lse.cpu().numpy(),
+                       "entropy bwd tiny")
+
+
+def test_entropy_bwd_v32000_sampled_rows_with_peaks():
+    spec = W.get("entropy_slsm_b16_l4096_v32000", L=256)
+    inp = W.generate(spec, 2, device=DEV)
+    T = 1.0
+    H, lse = rp.entropy_from_logits(inp.logits, T=T, return_lse=True)
+    up = torch.full((spec.rows,), 1.0 / spec.rows, device=DEV)
+    dl = rp.entropy_from_logits_bwd(inp.logits, up, lse, H, T=T)
+    torch.cuda.synchronize()
+    peaked = torch.nonzero(inp.logits.float().amax(dim=-1).reshape(-1) > 14.0)[:, 0].cpu().numpy()
+    rows = np.unique(np.concatenate([W.sample_rows(spec.rows, 24, 4), peaked[:16]]))
+    x = rows_f64(select_rows(inp.logits, rows))
+    r_t = torch.from_numpy(rows).to(DEV)
+    check_entropy_grad(select_rows(dl, rows), x, np.full(len(rows), 1.0 / spec.rows), T,
+                       H[r_t].cpu().numpy(), lse[r_t].cpu().numpy(), "entropy bwd v32000")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000])
+@pytest.mark.parametrize("offset,extra", [(0, 0), (3, 1)])
+def test_entropy_bwd_edge_shapes_every_row(dtype, V, offset, extra):
+    B, L = 2, 5
+    R = B * L
+    seed = V * 11 + offset
+    x, _ = strided_logits(B, L, V, dtype, offset, extra, seed)
+    if V > 4:
+        x[0, 1, 3] = float("-inf")        # a masked-out vocabulary entry: p = 0, adds 0
+    T = 1.3
+    H, lse = rp.entropy_from_logits(x, T=T, return_lse=True)
+    up = torch.randn(R, generator=torch.Generator().manual_seed(seed)).float()
+    up[2] = 0.0
+    dl_buf = torch.empty(B * L * (V + 2) + 9, dtype=dtype, device=DEV)
+    dl_view = torch.as_strided(dl_buf, (B, L, V), (L * (V + 2), V + 2, 1), 1 + offset)  # out of phase
+    dl = rp.entropy_from_logits_bwd(x, up.to(DEV), lse, H, T=T, dlogits=dl_view)
+    torch.cuda.synchronize()
+    xo = rows_f64(select_rows(x, np.arange(R)))
+    check_entropy_grad(select_rows(dl, np.arange(R)), xo, up.double().numpy(), T, H.cpu().numpy(),
+                       lse.cpu().numpy(), f"entropy bwd edge V={V}")
+    x2, _ = strided_logits(B, L, V, dtype, offset, extra, seed)
+    if V > 4:
+        x2[0, 1, 3] = float("-inf")
+    same, _ = strided_logits(B, L, V, dtype, offset, extra, seed + 5)
+    d_same = rp.entropy_from_logits_bwd(x2, up.to(DEV), lse, H, T=T, dlogits=same)
+    d_in = rp.entropy_from_logits_bwd(x2, up.to(DEV), lse, H, T=T, dlogits=x2)
+    torch.cuda.synchronize()
+    assert torch.equal(bf16_or_f32_bits(select_rows(d_in, np.arange(R))),
+                       bf16_or_f32_bits(select_rows(d_same, np.arange(R))))
