@@ -232,6 +232,35 @@ grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* id
                                       const grpo_rows* dlogits, int32_t* dev_err,
                                       grpo_stream_t stream);
 
+/*
+ * grpo_seq_terms -- sequence-level GRPO: per-sequence importance ratio and objective, and
+ * the per-token dlogp that selective_log_softmax_bwd turns into dlogits.
+ *
+ * [Liger-bwd] "Code analysis" shows a sequence-level backward kernel
+ * (_grpo_loss_bwd_kernel_seq) whose token KL gradient beta*(1 - exp(ref_logp - logp)) is
+ * weighted by the token's dloss while the policy-gradient part arrives computed per
+ * sequence; its ratio is not printed.  The ratio taken here is the length-normalised
+ * sequence ratio: for sequence b with n_b unmasked tokens,
+ *   s_b = exp(sum_t m_t (logp_t - old_t) / n_b),   pg_b = -min(s_b A_b, clip(s_b) A_b),
+ *   loss_t = pg_b + kl_t  (unmasked tokens; +0.0 on masked ones),
+ *   dlogp_t = W_b * dpg_b/dlogp_t + beta (1 - exp(ref_t - logp_t)) * dloss_t,
+ *   W_b = sum_t dloss_t,  dpg_b/dlogp_t = -A_b s_b / n_b, or 0 where clipping binds,
+ * i.e. dlogp_t = dJ/dlogp_t for J = sum_t dloss_t loss_t.  The full pass is:
+ *   selective_log_softmax_fwd (logp, lse) -> grpo_seq_terms -> selective_log_softmax_bwd
+ *   (dlogits = (dlogp/T)(onehot - p), +0.0 rows where dlogp == 0 without reading logits).
+ *
+ *   B, L         sequences and tokens per sequence (per-row arrays are [B*L], r = b*L + l)
+ *   logp         [B*L] fp32 (from selective_log_softmax_fwd);  old_logp: [B*L] or NULL (= logp)
+ *   ref_logp     [B*L], may be NULL when beta == 0;  adv [B];  mask [B*L] or NULL
+ *   dloss        [B*L] fp32 per-token loss weights
+ *   loss, dlogp  [B*L] fp32 outputs;  kl [B*L] or NULL;  seq_ratio [B] fp32 or NULL;
+ *   seq_is_clipped [B] uint8 or NULL.  A sequence with no unmasked token has ratio 1.
+ */
+grpo_status grpo_seq_terms(int64_t B, int64_t L, const float* logp, const float* old_logp,
+                           const float* ref_logp, const float* adv, const uint8_t* mask, const float* dloss,
+                           float beta, float eps_low, float eps_high, float* loss, float* kl, float* dlogp,
+                           float* seq_ratio, uint8_t* seq_is_clipped, grpo_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* grpo_status_string(grpo_status status);
 

@@ -55,6 +55,8 @@ __all__ = [
     "grpo_loss_bwd",
     "selective_log_softmax_bwd",
     "entropy_from_logits_bwd",
+    "grpo_seq_terms",
+    "grpo_seq_loss_bwd",
     "per_row",
 ]
 
@@ -357,3 +359,65 @@ def entropy_from_logits_bwd(x, dentropy, T):
         d = g[:, None] * np.where(p == 0.0, 0.0, p * (logp + H[:, None]))
     d[g == 0.0] = 0.0                         # +0.0 rows, also for u == -0.0
     return d, g
+
+
+def grpo_seq_terms(logp, old_logp, ref_logp, adv_seq, mask, dloss, B, L, beta, eps_low, eps_high):
+    """Sequence-level GRPO terms (fp64) for B sequences of L tokens.
+
+    [Liger-bwd], "Code analysis", shows a sequence-level backward kernel
+    (``_grpo_loss_bwd_kernel_seq``) whose token KL gradient beta * (1 - exp(ref - logp))
+    is weighted by that token's dloss inside the kernel while the policy-gradient part
+    arrives already computed per sequence; the pages print no ratio.  Reading taken
+    here: the importance ratio of sequence b is the length-normalised sequence ratio
+
+        s_b  = exp( sum_t m_bt (logp_bt - old_bt) / n_b ),   n_b = sum_t m_bt
+        pg_b = -min(s_b A_b, clip(s_b, 1 - eps_low, 1 + eps_high) A_b)
+
+    every unmasked token carries loss_t = pg_b + kl_t (kl_t the token k3 term), and the
+    objective is J = sum_t dloss_t loss_t.  Hence, for an unmasked token t of b,
+
+        dJ/dlogp_t = W_b dpg_b/dlogp_t + beta (1 - exp(ref_t - logp_t)) dloss_t,
+        W_b = sum_t dloss_bt,  dpg_b/dlogp_t = -A_b s_b / n_b (unclipped branch, ties
+        included) or 0 (clipping binds);
+
+    masked tokens have loss = kl = dlogp = +0.0; a sequence without tokens has s_b = 1.
+    """
+    logp = np.asarray(logp, dtype=np.float64).reshape(B, L)
+    m = np.ones((B, L), dtype=bool) if mask is None else (np.asarray(mask).reshape(B, L) != 0)
+    dl = np.asarray(dloss, dtype=np.float64).reshape(B, L)
+    A = np.asarray(adv_seq, dtype=np.float64)
+    old = logp if old_logp is None else np.asarray(old_logp, dtype=np.float64).reshape(B, L)
+    n = m.sum(axis=1)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        log_s = np.where(n > 0, np.where(m, logp - old, 0.0).sum(axis=1) / np.maximum(n, 1), 0.0)
+        s = np.exp(log_s)
+        clipped = np.clip(s, 1.0 - eps_low, 1.0 + eps_high)
+        pg = -np.minimum(s * A, clipped * A)
+        is_clipped = (clipped * A) < (s * A)
+        dpg = np.where((s * A) <= (clipped * A), -A * s / np.maximum(n, 1), 0.0)
+        W = np.where(m, dl, 0.0).sum(axis=1)
+        if beta != 0.0:
+            d = np.asarray(ref_logp, dtype=np.float64).reshape(B, L) - logp
+            kl = beta * (np.expm1(d) - d)
+            dkl = beta * (1.0 - np.exp(d))
+        else:
+            kl = np.zeros((B, L))
+            dkl = np.zeros((B, L))
+        loss = pg[:, None] + kl
+        dlogp = (W * dpg)[:, None] + dkl * dl
+    z = np.zeros((B, L))
+    return {
+        "seq_ratio": s, "seq_pg": pg, "seq_is_clipped": is_clipped,
+        "loss": np.where(m, loss, z).reshape(-1), "kl": np.where(m, kl, z).reshape(-1),
+        "dlogp": np.where(m, dlogp, z).reshape(-1),
+    }
+
+
+def grpo_seq_loss_bwd(x, idx, old_logp, ref_logp, adv_seq, mask, dloss, B, L, T, beta, eps_low, eps_high):
+    """dlogits of the sequence-level objective (fp64): the per-token dlogp of
+    grpo_seq_terms spread over each row as (dlogp / T) (1[j == idx] - p_j), with the
+    zero-row rule of softmax_gather_grad.  Returns (dlogits, g, terms)."""
+    logp, _ = selective_log_softmax(x, idx, T)
+    terms = grpo_seq_terms(logp, old_logp, ref_logp, adv_seq, mask, dloss, B, L, beta, eps_low, eps_high)
+    g = terms["dlogp"] / np.float64(T)
+    return softmax_gather_grad(x, idx, g, T), g, terms

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     grpo_loss_bwd,
     grpo_loss_fused,
     grpo_loss_fwd,
+    grpo_seq_terms,
     load_library,
     selective_log_softmax_bwd,
     selective_log_softmax_fwd,

@@ -23,7 +23,7 @@ GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
 
 EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_logits",
             "entropy_from_logits_bwd", "selective_log_softmax_fwd", "selective_log_softmax_bwd",
-            "grpo_status_string")
+            "grpo_seq_terms", "grpo_status_string")
 
 
 class GrpoRows(ctypes.Structure):
@@ -61,6 +61,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "grpo_loss_fused": [rows_p, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, rows_p, _P, _P],
         "entropy_from_logits": [rows_p, _F, _P, _P, _P],
         "entropy_from_logits_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P],
+        "grpo_seq_terms": [ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P],
         "selective_log_softmax_fwd": [rows_p, _P, _F, _P, _P, _P, _P],
         "selective_log_softmax_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P, _P],
     }
@@ -257,3 +258,21 @@ def selective_log_softmax_bwd(logits, idx, dlogp, lse, *, T=1.0, dlogits=None, d
         _stream(logits.device))
     _check("selective_log_softmax_bwd", st)
     return dlogits
+
+
+def grpo_seq_terms(logp, adv, dloss, *, B, L, beta, eps_low, eps_high, old_logp=None, ref_logp=None, mask=None):
+    """Sequence-level GRPO terms; returns dict(loss, kl, dlogp [B*L], seq_ratio [B],
+    seq_is_clipped [B]).  Feed dlogp to selective_log_softmax_bwd for the dlogits."""
+    R = B * L
+    dev = logp.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"loss": torch.empty(R, **f32), "kl": torch.empty(R, **f32), "dlogp": torch.empty(R, **f32),
+           "seq_ratio": torch.empty(B, **f32), "seq_is_clipped": torch.empty(B, dtype=torch.uint8, device=dev)}
+    st = load_library().grpo_seq_terms(
+        B, L, _ptr(logp, torch.float32, R, "logp"), _ptr(old_logp, torch.float32, R, "old_logp"),
+        _ptr(ref_logp, torch.float32, R, "ref_logp"), _ptr(adv, torch.float32, B, "adv"),
+        _ptr(mask, torch.uint8, R, "mask"), _ptr(dloss, torch.float32, R, "dloss"), float(beta), float(eps_low),
+        float(eps_high), out["loss"].data_ptr(), out["kl"].data_ptr(), out["dlogp"].data_ptr(),
+        out["seq_ratio"].data_ptr(), out["seq_is_clipped"].data_ptr(), _stream(dev))
+    _check("grpo_seq_terms", st)
+    return out

@@ -337,6 +337,41 @@ grpo_status selective_log_softmax_bwd(const grpo_rows* logits, const int64_t* id
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+grpo_status grpo_seq_terms(int64_t B, int64_t L, const float* logp, const float* old_logp,
+                           const float* ref_logp, const float* adv, const uint8_t* mask, const float* dloss,
+                           float beta, float eps_low, float eps_high, float* loss, float* kl, float* dlogp,
+                           float* seq_ratio, uint8_t* seq_is_clipped, grpo_stream_t stream) {
+  if (B < 0 || L < 0) return GRPO_ERR_INVALID_ARG;
+  if (static_cast<long double>(B) * L > kMaxRows) return GRPO_ERR_UNSUPPORTED;
+  if (!std::isfinite(beta) || beta < 0.f) return GRPO_ERR_INVALID_ARG;
+  if (!std::isfinite(eps_low) || eps_low < 0.f || eps_low > 1.f) return GRPO_ERR_INVALID_ARG;
+  if (!std::isfinite(eps_high) || eps_high < 0.f) return GRPO_ERR_INVALID_ARG;
+  if (B == 0 || L == 0) return GRPO_OK;
+  if (!ok_f32(logp) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(loss) ||
+      !ok_opt_f32(kl) || !ok_f32(dlogp) || !ok_opt_f32(seq_ratio))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  grpo::SeqParams p{};
+  p.B = B;
+  p.L = L;
+  p.logp = logp;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.dloss = dloss;
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.kl = kl;
+  p.dlogp = dlogp;
+  p.seq_ratio = seq_ratio;
+  p.seq_is_clipped = seq_is_clipped;
+  return from_cuda(grpo::launch_seq(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* grpo_status_string(grpo_status status) {
   switch (status) {
     case GRPO_OK: return "GRPO_OK";

@@ -116,6 +116,24 @@ struct FusedParams {
   float T;
 };
 
+// Sequence-level GRPO terms over B sequences of L tokens.
+struct SeqParams {
+  int64_t B, L;
+  const float* logp;
+  const float* old_logp;  // nullable: ratio 1
+  const float* ref_logp;  // read only when beta != 0
+  const float* adv;       // [B]
+  const uint8_t* mask;    // nullable
+  const float* dloss;
+  float beta, lo, hi;
+  float* loss;
+  float* kl;              // nullable
+  float* dlogp;
+  float* seq_ratio;       // [B], nullable
+  uint8_t* seq_is_clipped;  // [B], nullable
+};
+cudaError_t launch_seq(const SeqParams& p, cudaStream_t stream);
+
 // Kernel launchers, one translation unit per element type (compiled in parallel).
 cudaError_t launch_fwd_bf16(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
 cudaError_t launch_fwd_f32(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);

@@ -445,6 +445,60 @@ def check_entropy_bwd_closed_form_v2(orc):
     _close(dl[:, 1], -ref0, 1e-11, 1e-14, "V=2 entropy gradient (other column)")
 
 
+def check_seq_bwd_finite_differences(orc):
+    """Sequence-level objective J = sum_t dloss_t loss_t(x): its dlogits against central
+    differences over every logit of every sequence (the sequence ratio couples the rows)."""
+    rng = np.random.default_rng(13)
+    B, L, V = 2, 4, 7
+    R = B * L
+    x = rng.standard_normal((R, V)) * 1.5
+    idx = rng.integers(0, V, R)
+    A = np.array([0.9, -1.4])
+    T, beta, el, eh = 0.8, 0.07, 0.2, 0.28
+    lp0, _ = orc.selective_log_softmax(x, idx, T)
+    old = lp0 + rng.standard_normal(R) * 0.05
+    ref = lp0 + rng.standard_normal(R) * 0.2
+    mask = np.array([1, 1, 1, 0, 1, 1, 0, 0], dtype=np.uint8)
+    dloss = rng.uniform(0.2, 1.0, R) * mask
+    dl, g, terms = orc.grpo_seq_loss_bwd(x, idx, old, ref, A, mask, dloss, B, L, T, beta, el, eh)
+    s = terms["seq_ratio"]
+    assert np.all(np.abs(s - (1 - el)) > 0.02) and np.all(np.abs(s - (1 + eh)) > 0.02)
+
+    def J(xx):
+        lp, _ = orc.selective_log_softmax(xx, idx, T)
+        t = orc.grpo_seq_terms(lp, old, ref, A, mask, dloss, B, L, beta, el, eh)
+        return float(np.sum(dloss * t["loss"]))
+
+    h = 1e-6
+    fd = np.zeros((R, V))
+    for r in range(R):
+        for j in range(V):
+            xp = x.copy(); xp[r, j] += h
+            xm = x.copy(); xm[r, j] -= h
+            fd[r, j] = (J(xp) - J(xm)) / (2 * h)
+    _close(dl, fd, 1e-6, 1e-9, "sequence-level dlogits")
+    assert np.all(dl[mask == 0] == 0.0)
+
+
+def check_seq_terms_closed_forms(orc):
+    """old = logp: s = 1, pg = -A, dpg/dlogp_t = -A / n; a clipped sequence (A > 0, s > 1 + eps)
+    has a zero policy gradient; a sequence without tokens has ratio 1 and zero terms."""
+    B, L = 3, 4
+    lp = np.linspace(-3.0, -1.0, B * L)
+    mask = np.array([1, 1, 1, 1, 1, 1, 0, 0, 0, 0, 0, 0], dtype=np.uint8)
+    dloss = mask / 4.0
+    A = np.array([2.0, 1.0, 5.0])
+    old = lp.copy()
+    old[4:6] = lp[4:6] - 1.0                    # sequence 1: s = e (> 1 + eps_high)
+    t = orc.grpo_seq_terms(lp, old, None, A, mask, dloss, B, L, 0.0, 0.2, 0.28)
+    _close(t["seq_ratio"], [1.0, math.e, 1.0], 1e-14, 0, "seq ratio")
+    _close(t["seq_pg"][:2], [-2.0, -1.28 * 1.0], 1e-14, 0, "seq pg")
+    assert list(t["seq_is_clipped"]) == [False, True, False]
+    W0 = 1.0                                     # sum of dloss over sequence 0
+    _close(t["dlogp"][:4], np.full(4, W0 * -2.0 * 1.0 / 4), 1e-14, 0, "seq dlogp, on-policy")
+    assert np.all(t["dlogp"][4:] == 0.0) and np.all(t["loss"][8:] == 0.0)
+
+
 ALL_CHECKS = [
     check_bf16_decode_all_patterns,
     check_bf16_rounding_vs_torch,
@@ -466,4 +520,6 @@ ALL_CHECKS = [
     check_bwd_closed_form_on_policy,
     check_entropy_bwd_finite_differences,
     check_entropy_bwd_closed_form_v2,
+    check_seq_bwd_finite_differences,
+    check_seq_terms_closed_forms,
 ]

@@ -118,6 +118,20 @@ def test_fused_validation(lib):
                                None, None) == binding.GRPO_OK
 
 
+def test_seq_terms_validation(lib):
+    def seq(B=2, L=3, logp=FAKE, beta=0.0, ref=None, el=0.2, dlogp=FAKE):
+        return lib.grpo_seq_terms(B, L, logp, None, ref, FAKE, None, FAKE, beta, el, 0.2, FAKE, None, dlogp,
+                                  None, None, None)
+    assert seq(B=-1) == INV
+    assert seq(logp=None) == INV
+    assert seq(dlogp=None) == INV
+    assert seq(beta=0.1) == INV
+    assert seq(el=2.0) == INV
+    assert seq(logp=FAKE + 2) == INV
+    assert seq(B=1 << 16, L=1 << 16) == UNS
+    assert seq(B=0, logp=None, dlogp=None) == binding.GRPO_OK
+
+
 def test_slsm_and_entropy_validation(lib):
     x = rows()
     assert lib.selective_log_softmax_fwd(ctypes.byref(x), None, 1.0, FAKE, FAKE, None, None) == INV

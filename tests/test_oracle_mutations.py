@@ -17,9 +17,11 @@ MUTATIONS = [
     ("temperature_multiplies", "z = x / np.float64(T)", "z = x * np.float64(T)"),
     ("bwd_drops_1_over_T", "g = dlogp * np.asarray(dloss, dtype=np.float64) / np.float64(T)",
      "g = dlogp * np.asarray(dloss, dtype=np.float64)"),
-    ("kl_grad_sign", "dkl = beta * (1.0 - np.exp(", "dkl = beta * (-1.0 + np.exp("),
-    ("kl_value_sign_of_d", "kl = beta * (np.expm1(d) - d)", "kl = beta * (np.expm1(d) + d)"),
-    ("kl_value_dropped", "kl = beta * (np.expm1(d) - d)", "kl = beta * np.expm1(d)"),
+    ("kl_grad_sign", "dkl = beta * (1.0 - np.exp(np.asarray", "dkl = beta * (-1.0 + np.exp(np.asarray"),
+    ("kl_value_sign_of_d", "kl = beta * (np.expm1(d) - d)          #", "kl = beta * (np.expm1(d) + d)          #"),
+    ("kl_value_dropped", "kl = beta * (np.expm1(d) - d)          #", "kl = beta * np.expm1(d)          #"),
+    ("seq_kl_value_sign", "            kl = beta * (np.expm1(d) - d)\n            dkl", "            kl = beta * (np.expm1(d) + d)\n            dkl"),
+    ("seq_kl_grad_sign", "dkl = beta * (1.0 - np.exp(d))", "dkl = beta * (np.exp(d) - 1.0)"),
     ("tie_counts_as_clipped", "unclipped_binds = (ratio * A) <= (clipped * A)",
      "unclipped_binds = (ratio * A) < (clipped * A)"),
     ("is_clipped_reversed", "is_clipped = obj_clipped < obj_unclipped", "is_clipped = obj_clipped > obj_unclipped"),
@@ -47,6 +49,10 @@ MUTATIONS = [
     ("entropy_bwd_drops_T", "g = -np.asarray(dentropy, dtype=np.float64) / np.float64(T)",
      "g = -np.asarray(dentropy, dtype=np.float64)"),
     ("entropy_zero_rows_not_forced", "    d[g == 0.0] = 0.0 ", "    pass  "),
+    ("seq_ratio_not_length_normalised", "np.where(m, logp - old, 0.0).sum(axis=1) / np.maximum(n, 1)",
+     "np.where(m, logp - old, 0.0).sum(axis=1)"),
+    ("seq_dpg_missing_weight", "dlogp = (W * dpg)[:, None] + dkl * dl", "dlogp = dpg[:, None] + dkl * dl"),
+    ("seq_kl_grad_unweighted", "dlogp = (W * dpg)[:, None] + dkl * dl", "dlogp = (W * dpg)[:, None] + dkl"),
     ("bf16_truncates", "q = np.rint(np.ldexp(a, -unit_exp))", "q = np.floor(np.ldexp(a, -unit_exp))"),
     ("bf16_ties_away", "q = np.rint(np.ldexp(a, -unit_exp))", "q = np.floor(np.ldexp(a, -unit_exp) + 0.5)"),
     ("bf16_mantissa_bits", "_BF16_MANT_BITS = 7 ", "_BF16_MANT_BITS = 8 "),

@@ -644,3 +644,109 @@ def test_entropy_bwd_edge_shapes_every_row(dtype, V, offset, extra):
     torch.cuda.synchronize()
     assert torch.equal(bf16_or_f32_bits(select_rows(d_in, np.arange(R))),
                        bf16_or_f32_bits(select_rows(d_same, np.arange(R))))
+
+
+# ---------------------------------------------------------------------------
+# sequence-level GRPO: slsm fwd -> grpo_seq_terms -> slsm bwd
+# ---------------------------------------------------------------------------
+
+def run_seq_pipeline(inp, old, ref, T, beta, el, eh):
+    spec = inp.spec
+    t = lambda a: None if a is None else torch.as_tensor(a, dtype=torch.float32).to(DEV)
+    logp, lse = rp.selective_log_softmax_fwd(inp.logits, inp.idx, T=T)
+    st = rp.grpo_seq_terms(logp, inp.adv, inp.dloss, B=spec.B, L=spec.L, beta=beta, eps_low=el, eps_high=eh,
+                           old_logp=t(old), ref_logp=t(ref), mask=inp.mask)
+    dl = rp.selective_log_softmax_bwd(inp.logits, inp.idx, st["dlogp"], lse, T=T)
+    torch.cuda.synchronize()
+    return logp, lse, st, dl
+
+
+def compare_seq(inp, old, ref, T, beta, el, eh, logp, lse, st, dl, tag, rows=None):
+    """Every sequence's terms and the dlogits of `rows` (default: every row) against the oracle.
+    The per-sequence ratio depends on the forward's fp32 logp of all the sequence's tokens,
+    so the budget of each term includes |A| s max|dlogp| (and the KL's own dependence)."""
+    spec = inp.spec
+    B, L = spec.B, spec.L
+    R = B * L
+    x_all = None
+    idx = inp.idx.cpu().numpy()
+    mask = None if inp.mask is None else inp.mask.cpu().numpy()
+    dloss = inp.dloss.cpu().numpy().astype(np.float64)
+    A = inp.adv.cpu().numpy().astype(np.float64)
+    o_old = None if old is None else np.asarray(old, dtype=np.float64)
+    o_ref = None if ref is None else np.asarray(ref, dtype=np.float64)
+    lp_o = oracle_logp(inp.logits, idx, T)
+    terms = oracle.grpo_seq_terms(lp_o, o_old, o_ref, A, mask, dloss, B, L, beta, el, eh)
+    dlp = np.abs(logp.double().cpu().numpy() - lp_o)
+    m = np.ones((B, L), bool) if mask is None else mask.reshape(B, L) != 0
+    dmax = np.where(m, dlp.reshape(B, L), 0.0).max(axis=1)                       # per sequence
+    s = terms["seq_ratio"]
+    assert_scalar_close(st["seq_ratio"], s, f"{tag} seq ratio", atol=0.0,
+                        rtol=1e-5 + float(np.max(dmax) * 1.01))
+    lo, hi = 1 - el, 1 + eh
+    amb_seq = (A != 0) & ((np.abs(s - lo) <= 1e-5 * lo) | (np.abs(s - hi) <= 1e-5 * hi))
+    assert np.array_equal(st["seq_is_clipped"].cpu().numpy().astype(bool)[~amb_seq], terms["seq_is_clipped"][~amb_seq])
+    W = np.where(m, dloss.reshape(B, L), 0.0).sum(axis=1)
+    n = np.maximum(m.sum(axis=1), 1)
+    pg_sens = (np.abs(A) * s)[:, None] * dmax[:, None]                             # |d pg| bound
+    kl_sens = (beta * np.exp(np.asarray(o_ref).reshape(B, L) - lp_o.reshape(B, L)) * dlp.reshape(B, L)
+               if (beta != 0 and o_ref is not None) else np.zeros((B, L)))
+    loss_budget = (pg_sens + kl_sens).reshape(-1) * 1.01
+    assert_scalar_close(st["loss"], terms["loss"], f"{tag} loss", atol=1e-5 + float(loss_budget.max()))
+    dlogp_budget = ((W * np.abs(A) * s / n * 2 * dmax)[:, None] + kl_sens * np.abs(dloss.reshape(B, L))).reshape(-1)
+    got = st["dlogp"].double().cpu().numpy()
+    err = np.abs(got - terms["dlogp"])
+    assert np.all(err <= 1e-5 * np.abs(terms["dlogp"]) + 1e-7 * np.abs(W).max() + dlogp_budget * 1.01), \
+        f"{tag} dlogp: worst {err.max():.3g}"
+    # dlogits: the row factor is dlogp / T with the GPU's own dlogp; its deviation is the budget
+    rows = np.arange(R) if rows is None else rows
+    x = rows_f64(select_rows(inp.logits, rows))
+    odl = oracle.softmax_gather_grad(x, idx[rows], terms["dlogp"][rows] / T, T)
+    g = terms["dlogp"][rows] / T
+    with np.errstate(divide="ignore", invalid="ignore"):
+        rho = np.where(g != 0, err[rows] / np.abs(terms["dlogp"][rows]), 0.0)
+    rho = rho + np.abs(lse.double().cpu().numpy()[rows] - oracle.selective_log_softmax(x, idx[rows], T)[1]) + 1e-6
+    amb = (rho > 2.0 ** -10) | np.repeat(amb_seq, L)[rows]
+    assert amb.sum() <= max(2, 0.01 * len(rows)), f"{tag}: {amb.sum()} ambiguous rows"
+    assert_grad_rows(select_rows(dl, rows), odl, g, amb, f"{tag} dlogits", rho=rho)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_seq_level_tiny_every_row(seed):
+    spec = W.get("tiny_fp32", L=16)
+    inp = W.generate(spec, seed, device=DEV)
+    T, beta, el, eh = f32(spec.T), f32(spec.beta), f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    out = run_seq_pipeline(inp, old, ref, T, beta, el, eh)
+    compare_seq(inp, old, ref, T, beta, el, eh, *out, f"seq tiny s{seed}")
+
+
+def test_seq_level_pages_shape_every_row():
+    """B=4, L=512, V=32000 bf16 with a completion mask; beta = 0: zero-advantage and clipped
+    sequences give +0.0 rows for all their tokens."""
+    spec = W.get("grpo_b4_l512_v32000", old_sigma=0.02)
+    inp = W.generate(spec, 3, device=DEV)
+    T, beta, el, eh = f32(spec.T), 0.0, f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    logp, lse, st, dl = run_seq_pipeline(inp, old, ref, T, beta, el, eh)
+    for r0 in range(0, spec.rows, 512):
+        compare_seq(inp, old, ref, T, beta, el, eh, logp, lse, st, dl, "seq pages", rows=np.arange(r0, r0 + 512))
+    zero_seq = torch.nonzero(inp.adv == 0)[:, 0]
+    assert len(zero_seq) == 2
+    assert_plus_zero(dl[zero_seq], "zero-advantage sequences")
+
+
+def test_seq_level_beta_and_all_masked_sequence():
+    spec = W.get("grpo_qwen3_b16_l1024_v151936", B=4, L=64, V=1000, group_size=4)
+    inp = W.generate(spec, 4, device=DEV)
+    inp.mask.view(4, 64)[2] = 0                      # a sequence with no tokens: ratio 1, zero terms
+    inp.dloss.view(4, 64)[2] = 0.0
+    T, beta, el, eh = f32(spec.T), f32(spec.beta), f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    out = run_seq_pipeline(inp, old, ref, T, beta, el, eh)
+    compare_seq(inp, old, ref, T, beta, el, eh, *out, "seq beta")
+    assert float(out[2]["seq_ratio"][2]) == 1.0
+    assert_plus_zero(out[3][2], "all-masked sequence")
