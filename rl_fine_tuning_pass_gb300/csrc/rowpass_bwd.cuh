@@ -35,9 +35,22 @@ __device__ __forceinline__ float grpo_factor(float logp, const float* old_logp, 
   return (dpg + dkl) * dloss / T;
 }
 
+// All of a row's scalars are loaded before any of them is used, so the row waits for
+// one round trip to memory before its first logits load, not several.
 __device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b) {
-  if (p.mask != nullptr && p.mask[r] == 0) return 0.f;
-  return grpo_factor(p.logp[r], p.old_logp, p.ref_logp, p.adv[b], p.dloss[r], p.beta, p.lo, p.hi, p.T, r);
+  const bool live = p.mask == nullptr || p.mask[r] != 0;
+  const float logp = p.logp[r];
+  const float old = p.old_logp ? p.old_logp[r] : logp;
+  const float ref = p.beta != 0.f ? p.ref_logp[r] : 0.f;
+  const float A = p.adv[b];
+  const float dloss = p.dloss[r];
+  if (!live) return 0.f;
+  const float ratio = p.old_logp ? expf(logp - old) : 1.f;
+  const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
+  const float dpg = (ratio * A <= clipped * A) ? -A * ratio : 0.f;
+  float dkl = 0.f;
+  if (p.beta != 0.f) dkl = -p.beta * expm1f(ref - logp);  // beta (1 - e^(ref - logp))
+  return (dpg + dkl) * dloss / p.T;
 }
 
 // The part of a row one CTA handles: vectors [v0, v1), plus the scalar head and tail.
@@ -141,7 +154,10 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   const int tid = threadIdx.x;
   const int V = p.x.V;
 
-  // row factor, computed redundantly by every thread from broadcast loads
+  // row factor, computed redundantly by every thread from broadcast loads; idx and lse
+  // are loaded in the same round trip (they are only used when g != 0)
+  const int64_t id64 = p.idx[r];
+  const float lse = p.lse[r];
   const float g = GRPO ? grpo_row_factor(p, r, b) : p.dlogp_up[r] / p.T;
   S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
   const RowSplit sp = split_row<E>(out, V);
@@ -151,7 +167,6 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
     fill_span<E, THREADS>(out, sp, sn, 0u);
     return;
   }
-  const int64_t id64 = p.idx[r];
   if (id64 < 0 || id64 >= V) {
     fill_span<E, THREADS>(out, sp, sn, E::kNaNPair);
     if (tid == 0 && p.dev_err) atomicOr(p.dev_err, GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT);
@@ -159,7 +174,7 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   }
   const int idx = static_cast<int>(id64);
   const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
-  const float nK = fmaf(-p.lse[r], kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
+  const float nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
   bool owner = false;
   // d_j = -sign(g) |g| p_j: negated when g > 0
   const float q_part =
@@ -226,6 +241,8 @@ __global__ void __launch_bounds__(THREADS) entgrad_kernel(const BwdParams p) {
   const int64_t b = r / p.x.L;
   const int64_t l = r - b * p.x.L;
   const int V = p.x.V;
+  const float lse = p.lse[r];  // same round trip as dentropy (used only when g != 0)
+  const float H = p.entropy[r];
   const float g = -p.dentropy[r] / p.T;
   S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
   const RowSplit sp = split_row<E>(out, V);
@@ -236,8 +253,8 @@ __global__ void __launch_bounds__(THREADS) entgrad_kernel(const BwdParams p) {
   }
   const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
   const float lg = log2f(fabsf(g));
-  const float nK = fmaf(-p.lse[r], kLog2e, lg);        // -(lse*log2e - log2|g|)
-  const float h_shift = fmaf(-kLn2, lg, p.entropy[r]);  // H - ln|g|
+  const float nK = fmaf(-lse, kLog2e, lg);        // -(lse*log2e - log2|g|)
+  const float h_shift = fmaf(-kLn2, lg, H);       // H - ln|g|
   if (g < 0.f) stream_span_entropy<E, THREADS, UNROLL, SAME_PHASE, true>(in, out, sp, sn, p.c, nK, h_shift);
   else stream_span_entropy<E, THREADS, UNROLL, SAME_PHASE, false>(in, out, sp, sn, p.c, nK, h_shift);
 }

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   const RowSplit osp = split_row<E>(out, V);
   const Span osn = whole_row(osp);
 
+  const int64_t id64 = p.idx[r];  // loaded with the mask, before either is waited on
   if (p.mask != nullptr && p.mask[r] == 0) {  // masked token: zero outputs, zero gradient row
     if (tid == 0) masked_row_outputs(p, r);
     fill_span<E, THREADS>(out, osp, osn, 0u);
@@ -38,15 +39,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   }
 
   const S* row = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
-  int idx = 0;
-  bool bad_idx = false;
-  float x_idx = 0.f;
-  if (tid == 0) {
-    const int64_t id = p.idx[r];
-    bad_idx = id < 0 || id >= V;
-    idx = bad_idx ? 0 : static_cast<int>(id);
-    x_idx = E::load_scalar(row + idx);
-  }
+  const bool bad_idx = id64 < 0 || id64 >= V;
+  const int idx = bad_idx ? 0 : static_cast<int>(id64);
 
   // sweep 1: the online statistic (as in rowstats_kernel)
   Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -66,6 +60,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
     v[0] = ld_v4(vb + i);
     run_vectors<E, kH>(rs, v, c);
   }
+  // the selected logit, loaded after the stream so that no dependent load delays it
+  const float x_idx = tid == 0 ? E::load_scalar_coherent(row + idx) : 0.f;
   Stat mine;
   mine.a = rs.a;
   mine.s = rs.s.x + rs.s.y;

@@ -150,16 +150,10 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   const int V = p.x.V;
   const float c = p.c;
 
-  // the selected logit: one scalar load, issued before the stream so it overlaps it
-  int idx = 0;
-  bool bad_idx = false;
-  float x_idx = 0.f;
-  if (kIdx && tid == 0) {
-    const int64_t id = p.idx[r];
-    bad_idx = id < 0 || id >= V;
-    idx = bad_idx ? 0 : static_cast<int>(id);
-    x_idx = E::load_scalar(row + idx);
-  }
+  // idx is loaded now; the selected logit x[idx] only after the stream, so that no
+  // dependent load delays the first logits loads of this warp
+  int64_t id = 0;
+  if (kIdx && tid == 0) id = p.idx[r];
 
   Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const RowSplit sp = split_row<E>(row, V);
@@ -181,6 +175,12 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
     run_vectors<E, kH>(rs, v, c);
   }
 
+  bool bad_idx = false;
+  float x_idx = 0.f;
+  if (kIdx && tid == 0) {
+    bad_idx = id < 0 || id >= V;
+    x_idx = E::load_scalar(row + (bad_idx ? 0 : static_cast<int>(id)));
+  }
   Stat mine;
   mine.a = rs.a;
   mine.s = rs.s.x + rs.s.y;
