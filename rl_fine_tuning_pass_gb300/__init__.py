@@ -18,3 +18,4 @@ from .binding import (  # noqa: F401
     selective_log_softmax_fwd,
     status_string,
 )
+from .autograd import entropy, grpo_loss, selective_log_softmax  # noqa: F401,E402

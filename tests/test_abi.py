@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from rl_fine_tuning_pass_gb300 import binding
 from rl_fine_tuning_pass_gb300.build import ROOT, build
@@ -162,3 +163,17 @@ def test_rows_of_strides():
     assert (r2.B, r2.L, r2.V, r2.stride_l) == (1, 5, 7, 7)
     with pytest.raises(ValueError):
         binding.rows_of(torch.empty(4, 8, dtype=torch.float32).t())
+
+
+def test_autograd_wrappers_have_no_cpu_path():
+    """The autograd wrappers marshal into the CUDA library only: CPU tensors are refused
+    before any call, never computed some other way."""
+    from rl_fine_tuning_pass_gb300 import autograd as ag
+    x = torch.randn(2, 3, 8, requires_grad=True)
+    idx = torch.zeros(6, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA"):
+        ag.selective_log_softmax(x, idx)
+    with pytest.raises(ValueError, match="CUDA"):
+        ag.entropy(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        ag.grpo_loss(x, idx, torch.zeros(2))
