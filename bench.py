@@ -58,12 +58,14 @@ class L2Flush:
 
     def __init__(self, device):
         self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
-        self.sink = torch.empty((), dtype=torch.int64, device=device)
+        # fp32, so that the sum reads the buffer directly (an int32 sum into int64 would
+        # first write a 512 MB cast copy)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
 
     def __call__(self, i: int = 0):
         self.w.fill_(i & 0x7F)
-        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
+        torch.sum(self.r, dim=0, out=self.sink)
 GRPO_WORKLOADS = ("grpo_b4_l512_v32000", "grpo_qwen3_b16_l1024_v151936", "sweep_b16_l4096_v151936")
 
 

@@ -36,14 +36,16 @@ __device__ __forceinline__ float grpo_factor(float logp, const float* old_logp, 
 }
 
 // All of a row's scalars are loaded before any of them is used, so the row waits for
-// one round trip to memory before its first logits load, not several.
-__device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b) {
+// one round trip to memory before its first logits load, not several.  `kept` tells
+// whether the GRPO forward read the row with L2 priority evict_last.
+__device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, int64_t b, bool& kept) {
   const bool live = p.mask == nullptr || p.mask[r] != 0;
   const float logp = p.logp[r];
   const float old = p.old_logp ? p.old_logp[r] : logp;
   const float ref = p.beta != 0.f ? p.ref_logp[r] : 0.f;
   const float A = p.adv[b];
   const float dloss = p.dloss[r];
+  kept = live && !(p.beta == 0.f && A == 0.f);
   if (!live) return 0.f;
   const float ratio = p.old_logp ? expf(logp - old) : 1.f;
   const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
@@ -70,24 +72,30 @@ __device__ __forceinline__ void fill_span(typename E::storage* out, const RowSpl
   uint4* vb = reinterpret_cast<uint4*>(out + sp.head);
   const uint4 v = make_uint4(pair, pair, pair, pair);
 #pragma unroll 4
-  for (int i = sn.v0 + tid; i < sn.v1; i += THREADS) st_v4(vb + i, v);
+  for (int i = sn.v0 + tid; i < sn.v1; i += THREADS) st_v4_evict_first(vb + i, v);
 }
 
 // Load the VEC input elements of output vector i (input rows may be out of phase with
 // the output rows; then the elements are loaded one by one).
-template <class E, bool SAME_PHASE>
+// LAST_READ: with L2 priority evict_first.
+template <class E, bool SAME_PHASE, bool LAST_READ = false>
 __device__ __forceinline__ uint4 load_vec(const typename E::storage* in_body, int i) {
-  if (SAME_PHASE) return ld_v4(reinterpret_cast<const uint4*>(in_body) + i);
-  float f[E::kVec];
+  if constexpr (SAME_PHASE) {
+    const uint4* q = reinterpret_cast<const uint4*>(in_body) + i;
+    return LAST_READ ? ld_v4_evict_first(q) : ld_v4(q);
+  } else {
+    float f[E::kVec];
 #pragma unroll
-  for (int q = 0; q < E::kVec; ++q) f[q] = E::load_scalar_coherent(in_body + i * E::kVec + q);
-  return E::pack(f, 0u);  // exact: the values came from this format
+    for (int q = 0; q < E::kVec; ++q) f[q] = E::load_scalar_coherent(in_body + i * E::kVec + q);
+    return E::pack(f, 0u);  // exact: the values came from this format
+  }
 }
 
 // Stream one row with g != 0: out_j = -sign(g) |g| p_j (NEG: g > 0), accumulating
 // sum_{j != idx} |g| p_j for the idx element.  Returns this thread's partial sum and
-// whether it wrote the idx element.
-template <class E, int THREADS, int UNROLL, bool SAME_PHASE, bool NEG>
+// whether it wrote the idx element.  The gradient is stored with L2 priority evict_first;
+// LAST_READ loads the logits with evict_first too.
+template <class E, int THREADS, int UNROLL, bool SAME_PHASE, bool NEG, bool LAST_READ = false>
 __device__ __forceinline__ float stream_span(const typename E::storage* in, typename E::storage* out,
                                              const RowSplit& sp, const Span& sn, int idx, float c, float nK,
                                              bool& owner) {
@@ -130,18 +138,18 @@ __device__ __forceinline__ float stream_span(const typename E::storage* in, type
 #pragma unroll
       for (int q = 0; q < E::kPairs; ++q) q2 = __fadd2_rn(q2, e[q]);
     }
-    st_v4(ob + i, E::template pack_pairs<NEG>(e));
+    st_v4_evict_first(ob + i, E::template pack_pairs<NEG>(e));
   };
 
   int i = sn.v0 + tid;
   for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {
     uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = load_vec<E, SAME_PHASE>(in_body, i + k * THREADS);
+    for (int k = 0; k < UNROLL; ++k) v[k] = load_vec<E, SAME_PHASE, LAST_READ>(in_body, i + k * THREADS);
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
   }
-  for (; i < sn.v1; i += THREADS) process(load_vec<E, SAME_PHASE>(in_body, i), i);
+  for (; i < sn.v1; i += THREADS) process(load_vec<E, SAME_PHASE, LAST_READ>(in_body, i), i);
   return q_acc + (q2.x + q2.y);
 }
 
@@ -158,28 +166,32 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   // are loaded in the same round trip (they are only used when g != 0)
   const int64_t id64 = p.idx[r];
   const float lse = p.lse[r];
-  const float g = GRPO ? grpo_row_factor(p, r, b) : p.dlogp_up[r] / p.T;
+  bool kept = false;  // the GRPO forward read this row with evict_last
+  const float g = GRPO ? grpo_row_factor(p, r, b, kept) : p.dlogp_up[r] / p.T;
   S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
   const RowSplit sp = split_row<E>(out, V);
   const Span sn = whole_row(sp);
+  const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
 
   if (g == 0.f) {  // early-out: +0.0 over the row, nothing read
     fill_span<E, THREADS>(out, sp, sn, 0u);
+    if (kept) l2_demote<THREADS>(in, static_cast<int64_t>(V) * sizeof(S));
     return;
   }
   if (id64 < 0 || id64 >= V) {
     fill_span<E, THREADS>(out, sp, sn, E::kNaNPair);
+    if (kept) l2_demote<THREADS>(in, static_cast<int64_t>(V) * sizeof(S));
     if (tid == 0 && p.dev_err) atomicOr(p.dev_err, GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT);
     return;
   }
   const int idx = static_cast<int>(id64);
-  const S* in = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
   const float nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
   bool owner = false;
-  // d_j = -sign(g) |g| p_j: negated when g > 0
+  // d_j = -sign(g) |g| p_j: negated when g > 0.  After a GRPO forward this is the row's
+  // last read: evict_first.
   const float q_part =
-      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true>(in, out, sp, sn, idx, p.c, nK, owner)
-              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false>(in, out, sp, sn, idx, p.c, nK, owner);
+      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true, GRPO>(in, out, sp, sn, idx, p.c, nK, owner)
+              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false, GRPO>(in, out, sp, sn, idx, p.c, nK, owner);
 
   // g (1 - p_idx) = sign(g) * sum_{j != idx} |g| p_j; written by the thread that wrote
   // the idx element's provisional value, so its two stores stay in program order.
@@ -221,7 +233,7 @@ __device__ __forceinline__ void stream_span_entropy(const typename E::storage* i
       const float2 e = make_float2(ex2(t.x), ex2(t.y));
       d[q] = __fmul2_rn(e, __ffma2_rn(ln2, t, hs2));
     }
-    st_v4(ob + i, E::template pack_pairs<NEG>(d));
+    st_v4_evict_first(ob + i, E::template pack_pairs<NEG>(d));
   };
   int i = sn.v0 + tid;
   for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {

@@ -50,6 +50,73 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// The same accesses with an L2 eviction priority (createpolicy + .L2::cache_hint, the
+// policy made next to each access so that no 64-bit policy register stays live across
+// the streaming loops).  The priority steers which lines the L2 gives up first and
+// changes no result:
+//   evict_first - data touched for the last time in this pass: the logits of a row whose
+//                 gradient is known to be zero, a row's last read, every gradient store;
+//   evict_last  - logits that will be read again soon: a GRPO row in the forward (the
+//                 backward reads it next) and in the fused kernel's first sweep.  The
+//                 re-read lets them go (evict_first); a row that turns out to need no
+//                 re-read is put back to normal priority by l2_demote.
+__device__ __forceinline__ uint4 ld_nc_v4_evict_first(const void* p) {
+  uint4 r;
+  asm("{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_v4_evict_first(const void* p) {
+  uint4 r;
+  asm volatile("{\n\t.reg .b64 pol;\n\t"
+               "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+               "ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+__device__ __forceinline__ uint4 ld_nc_v4_evict_last(const void* p) {
+  uint4 r;
+  asm("{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_v4_evict_last(const void* p) {
+  uint4 r;
+  asm volatile("{\n\t.reg .b64 pol;\n\t"
+               "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+               "ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+__device__ __forceinline__ void st_v4_evict_first(void* p, uint4 v) {
+  asm volatile("{\n\t.reg .b64 pol;\n\t"
+               "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+               "st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, pol;\n\t}"
+               ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Put the L2 lines of [p, p + bytes) that are present back to normal priority, without
+// reading them.  The 128-byte line addresses are rounded down from p; they stay inside
+// the memory page that holds p, since pages are larger than and aligned to 128 bytes.
+template <int THREADS>
+__device__ __forceinline__ void l2_demote(const void* p, int64_t bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+  const uintptr_t end = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes);
+  for (uintptr_t a = a0 + 128u * threadIdx.x; a < end; a += 128u * THREADS)
+    asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(a) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // element traits
 // ---------------------------------------------------------------------------

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   const Span osn = whole_row(osp);
 
   const int64_t id64 = p.idx[r];  // loaded with the mask, before either is waited on
+  const float A_pre = p.beta == 0.f ? p.adv[b] : 1.f;
   if (p.mask != nullptr && p.mask[r] == 0) {  // masked token: zero outputs, zero gradient row
     if (tid == 0) masked_row_outputs(p, r);
     fill_span<E, THREADS>(out, osp, osn, 0u);
@@ -48,18 +49,26 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   if (tid < sp.head) run_scalar<kH>(rs, E::load_scalar(row + tid), c);
   if (tid < sp.tail) run_scalar<kH>(rs, E::load_scalar(row + sp.head + sp.nvec * VEC + tid), c);
   const uint4* vb = reinterpret_cast<const uint4*>(row + sp.head);
-  int i = tid;
-  for (; i + (UNROLL - 1) * THREADS < sp.nvec; i += UNROLL * THREADS) {
-    uint4 v[UNROLL];
+  // L2: a row whose gradient is zero in advance (A == 0 with beta == 0) is not read again;
+  // any other row is kept (evict_last) for the second sweep, which lets it go.
+  // Coherent loads: dlogits may alias the logits.
+  const bool kept = A_pre != 0.f;
+  auto sweep1 = [&](auto load) {
+    int i = tid;
+    for (; i + (UNROLL - 1) * THREADS < sp.nvec; i += UNROLL * THREADS) {
+      uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = ld_v4(vb + i + k * THREADS);  // coherent: dlogits may alias
-    run_vectors<E, kH>(rs, v, c);
-  }
-  for (; i < sp.nvec; i += THREADS) {
-    uint4 v[1];
-    v[0] = ld_v4(vb + i);
-    run_vectors<E, kH>(rs, v, c);
-  }
+      for (int k = 0; k < UNROLL; ++k) v[k] = load(vb + i + k * THREADS);
+      run_vectors<E, kH>(rs, v, c);
+    }
+    for (; i < sp.nvec; i += THREADS) {
+      uint4 v[1];
+      v[0] = load(vb + i);
+      run_vectors<E, kH>(rs, v, c);
+    }
+  };
+  if (kept) sweep1([](const uint4* q) { return ld_v4_evict_last(q); });
+  else sweep1([](const uint4* q) { return ld_v4_evict_first(q); });
   // the selected logit, loaded after the stream so that no dependent load delays it
   const float x_idx = tid == 0 ? E::load_scalar_coherent(row + idx) : 0.f;
   Stat mine;
@@ -83,11 +92,13 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   const float g = sh_g;
   if (g == 0.f) {  // early-out: +0.0 over the row
     fill_span<E, THREADS>(out, osp, osn, 0u);
+    if (kept) l2_demote<THREADS>(row, static_cast<int64_t>(V) * sizeof(S));
     return;
   }
   const int gidx = sh_idx;
   if (gidx < 0) {  // out-of-range idx (already reported by the forward outputs)
     fill_span<E, THREADS>(out, osp, osn, E::kNaNPair);
+    if (kept) l2_demote<THREADS>(row, static_cast<int64_t>(V) * sizeof(S));
     return;
   }
 
@@ -95,8 +106,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   bool owner = false;
   const float nK = sh_nK;
   const float q_part =
-      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true>(row, out, osp, osn, gidx, c, nK, owner)
-              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false>(row, out, osp, osn, gidx, c, nK, owner);
+      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true, true>(row, out, osp, osn, gidx, c, nK, owner)
+              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false, true>(row, out, osp, osn, gidx, c, nK, owner);
   const float q_total = block_sum_all<THREADS>(q_part);
   if (owner) E::store_scalar(out + gidx, g > 0.f ? q_total : -q_total);
 }

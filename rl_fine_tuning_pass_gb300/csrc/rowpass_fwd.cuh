@@ -73,6 +73,32 @@ __device__ __forceinline__ void run_vectors(Running& rs, uint4 (&v)[N], float c)
   }
 }
 
+// L2 priority of a row's logits in the forward.
+enum FwdL2 : int { kL2Default = 0, kL2First = 1, kL2Last = 2 };
+
+// The row body: 16-byte vectors [0, nvec), UNROLL in flight per thread, loaded with the
+// L2 priority POL.
+template <class E, int THREADS, int UNROLL, bool kH, int POL>
+__device__ __forceinline__ void stream_vectors(Running& rs, const uint4* vb, int nvec, float c) {
+  auto load = [](const uint4* q) {
+    if constexpr (POL == kL2First) return ld_nc_v4_evict_first(q);
+    else if constexpr (POL == kL2Last) return ld_nc_v4_evict_last(q);
+    else return ld_nc_v4(q);
+  };
+  int i = threadIdx.x;
+  for (; i + (UNROLL - 1) * THREADS < nvec; i += UNROLL * THREADS) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) v[k] = load(vb + i + k * THREADS);
+    run_vectors<E, kH>(rs, v, c);
+  }
+  for (; i < nvec; i += THREADS) {
+    uint4 v[1];
+    v[0] = load(vb + i);
+    run_vectors<E, kH>(rs, v, c);
+  }
+}
+
 // Outputs of one row from its merged statistic (thread 0); returns logp and lse through
 // the optional pointers.
 template <int MODE>
@@ -140,6 +166,10 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   const int64_t l = r - b * p.x.L;
   const int tid = threadIdx.x;
 
+  // with beta == 0, a zero advantage makes the row's gradient zero: the backward will not
+  // read this row again (loaded together with the mask: one round trip); every other GRPO
+  // row is kept in L2 for the backward
+  const float A_pre = (kGrpo && p.beta == 0.f) ? p.adv[b] : 1.f;
   if (kGrpo && p.mask != nullptr && p.mask[r] == 0) {
     // masked token: not part of the objective; every output is +0.0, no logits read
     if (tid == 0) masked_row_outputs(p, r);
@@ -161,19 +191,9 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   if (tid < sp.tail) run_scalar<kH>(rs, E::load_scalar(row + sp.head + sp.nvec * VEC + tid), c);
 
   const uint4* vb = reinterpret_cast<const uint4*>(row + sp.head);
-  const int v1 = sp.nvec;
-  int i = tid;
-  for (; i + (UNROLL - 1) * THREADS < v1; i += UNROLL * THREADS) {
-    uint4 v[UNROLL];
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = ld_nc_v4(vb + i + k * THREADS);
-    run_vectors<E, kH>(rs, v, c);
-  }
-  for (; i < v1; i += THREADS) {
-    uint4 v[1];
-    v[0] = ld_nc_v4(vb + i);
-    run_vectors<E, kH>(rs, v, c);
-  }
+  if (!kGrpo) stream_vectors<E, THREADS, UNROLL, kH, kL2Default>(rs, vb, sp.nvec, c);
+  else if (A_pre == 0.f) stream_vectors<E, THREADS, UNROLL, kH, kL2First>(rs, vb, sp.nvec, c);
+  else stream_vectors<E, THREADS, UNROLL, kH, kL2Last>(rs, vb, sp.nvec, c);
 
   bool bad_idx = false;
   float x_idx = 0.f;
