@@ -228,7 +228,7 @@ cudaError_t launch_dtype(int mode, const FwdParams& p, int64_t rows, int sms, cu
   switch (pick_threads_fwd(p.x.V, sizeof(typename E::storage), rows, sms)) {
     case 32: return launch_mode<E, 32, kUnrollSmall>(mode, p, rows, s);
     case 64: return launch_mode<E, 64, kUnroll>(mode, p, rows, s);
-    case 128: return launch_mode<E, 128, kUnroll>(mode, p, rows, s);
+    case 128: return launch_mode<E, 128, 2>(mode, p, rows, s);
     default: return launch_mode<E, 256, kUnroll>(mode, p, rows, s);
   }
 }
