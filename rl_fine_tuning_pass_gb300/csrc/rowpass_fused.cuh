@@ -131,6 +131,7 @@ cudaError_t launch_fused_dtype(const FusedParams& q, int64_t rows, bool same_pha
   switch (pick_threads_fused(q.f.x.V, sizeof(typename E::storage), rows, sms)) {
     case 64: return launch_fused_t<E, 64, kUnroll>(q, rows, same_phase, s);
     case 128: return launch_fused_t<E, 128, kUnroll>(q, rows, same_phase, s);
+    case 512: return launch_fused_t<E, 512, kUnroll>(q, rows, same_phase, s);
     default: return launch_fused_t<E, 256, kUnroll>(q, rows, same_phase, s);
   }
 }

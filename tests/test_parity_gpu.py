@@ -510,7 +510,7 @@ def test_fused_pages_workload_every_row_and_matches_separate():
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
-@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000])
+@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000, 151936])
 @pytest.mark.parametrize("offset,extra", [(0, 0), (3, 1)])
 def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
     B, L = 2, 5
