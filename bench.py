@@ -343,6 +343,104 @@ class FusedStep(GrpoStep):
         self.h_loss.copy_(f["loss"], non_blocking=True)
 
 
+def vocab_shard_starts(V, shards):
+    """Boundaries of `shards` near-equal column shards of a V-column vocabulary."""
+    return [V * k // shards for k in range(shards + 1)]
+
+
+class VocabShardStep(GrpoStep):
+    """The vocabulary-parallel GRPO step of `shards` ranks, run on one GPU shard after
+    shard: grpo_vocab_shard_stats on every shard (each writes its slot of the gathered
+    [shards, B*L, 4] buffer, where an all-gather would put it), grpo_vocab_combine, then
+    grpo_loss_bwd_vocab_shard on every shard into its columns of dlogits."""
+
+    def __init__(self, spec, seed, device, shards, inputs=None):
+        super().__init__(spec, seed, device, inputs)
+        lib = rp.load_library()
+        inp, o, R, V = self.inp, self.out, spec.rows, spec.V
+        self.shards = shards
+        self.starts = vocab_shard_starts(V, shards)
+        self.c_starts = (ctypes.c_int64 * (shards + 1))(*self.starts)
+        self.stats = torch.empty(shards, R, 4, dtype=torch.float32, device=device)
+        self.p_rest = torch.empty(R, dtype=torch.float32, device=device)
+        sl = lambda t, k: t[..., self.starts[k]:self.starts[k + 1]]
+        self.x_sh = [rp.rows_of(sl(inp.logits, k)) for k in range(shards)]
+        self.dx_sh = [rp.rows_of(sl(self.dlogits, k)) for k in range(shards)]
+        T, beta, el, eh = spec.T, spec.beta, spec.eps_low, spec.eps_high
+        self._st, self._cb, self._bw = lib.grpo_vocab_shard_stats, lib.grpo_vocab_combine, lib.grpo_loss_bwd_vocab_shard
+        self.st_args = [(ctypes.byref(self.x_sh[k]), self.starts[k], _p(inp.idx), _p(inp.mask), T,
+                         self.stats[k].data_ptr(), self.stream) for k in range(shards)]
+        self.cb_args = (shards, _p(self.stats), self.c_starts, spec.B, spec.L, _p(inp.idx), _p(self.old), _p(self.ref),
+                        _p(inp.adv), _p(inp.mask), T, beta, el, eh, _p(o["loss"]), _p(o["logp"]), _p(o["lse"]),
+                        _p(o["kl"]), _p(o["is_clipped"]), _p(o["entropy"]), _p(self.p_rest), None, self.stream)
+        self.bw_args = [(ctypes.byref(self.x_sh[k]), self.starts[k], V, _p(inp.idx), _p(self.old), _p(self.ref),
+                         _p(inp.adv), _p(inp.mask), _p(inp.dloss), _p(o["logp"]), _p(o["lse"]), _p(self.p_rest), T,
+                         beta, el, eh, ctypes.byref(self.dx_sh[k]), None, self.stream) for k in range(shards)]
+        self.kernels = [("grpo_vocab_shard_stats", self.stats_all_shards), ("grpo_vocab_combine", self.combine),
+                        ("grpo_loss_bwd_vocab_shard", self.bwd_all_shards)]
+        self.launches_per_step = 2 * shards + 1
+
+    @staticmethod
+    def _call(fn, args):
+        st = fn(*args)
+        if st:
+            raise rp.GrpoError(fn.__name__, st)
+
+    def stats_all_shards(self):
+        for a in self.st_args:
+            self._call(self._st, a)
+
+    def combine(self):
+        self._call(self._cb, self.cb_args)
+
+    def bwd_all_shards(self):
+        for a in self.bw_args:
+            self._call(self._bw, a)
+
+    def account(self):
+        """Minimal bytes.  Shard statistics: the logits of every unmasked row once over all
+        shards; every shard reads each row's mask byte and writes its 16-byte statistic,
+        and reads idx on unmasked rows.  Merge: every row's mask and outputs (21 B) and
+        p_rest; an unmasked row's S statistics, idx, old, ref.  Shard backward: the unsplit
+        backward's bytes (grpo_row_bytes), its per-row scalars read by every shard, and
+        p_rest read by every shard on rows with a non-zero factor."""
+        per = super().account()
+        spec, inp, S, R = self.spec, self.inp, self.shards, self.spec.rows
+        live = int(R - self.classes["masked"])
+        nonzero = int(R - self.classes["zero_grad_rows"])
+        m = 1 if inp.mask is not None else 0
+        o = 4 if self.old is not None else 0
+        r = 4 if self.ref is not None else 0
+        fwd_logits = live * spec.V * spec.elem_size
+        stats = fwd_logits + S * (R * (m + 16) + live * 8)
+        combine = R * (m + 21 + 4) + live * (S * 16 + 8 + o + r)
+        bwd = per["grpo_loss_bwd"] + (S - 1) * (R * m + live * (4 + o + r + 4) + nonzero * 12) + S * nonzero * 4
+        self.classes["vocab_shards"] = S
+        self.classes["vocab_starts"] = self.starts
+        return {"grpo_vocab_shard_stats": int(stats), "grpo_vocab_combine": int(combine),
+                "grpo_loss_bwd_vocab_shard": int(bwd)}
+
+    def e2e_step(self):
+        spec, dev = self.spec, self.d_logits.device
+        h = self.h
+        up = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        self.d_logits.copy_(h["logits"], non_blocking=True)
+        idx, adv, mask, dloss, old, ref = up(h["idx"]), up(h["adv"]), up(h["mask"]), up(h["dloss"]), up(h["old"]), up(h["ref"])
+        sl = lambda t, k: t[..., self.starts[k]:self.starts[k + 1]]
+        stats = torch.stack([rp.grpo_vocab_shard_stats(sl(self.d_logits, k), self.starts[k], T=spec.T, idx=idx,
+                                                       mask=mask) for k in range(self.shards)])
+        f = rp.grpo_vocab_combine(stats, self.starts, spec.B, spec.L, T=spec.T, idx=idx, adv=adv, grpo=True,
+                                  beta=spec.beta, eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=old,
+                                  ref_logp=ref, mask=mask)
+        for k in range(self.shards):
+            rp.grpo_loss_bwd_vocab_shard(sl(self.d_logits, k), self.starts[k], spec.V, idx, adv, dloss, f["logp"],
+                                         f["lse"], f["p_rest"], T=spec.T, beta=spec.beta, eps_low=spec.eps_low,
+                                         eps_high=spec.eps_high, old_logp=old, ref_logp=ref, mask=mask,
+                                         dlogits=sl(self.dlogits, k))
+        self.h_dl.copy_(self.dlogits, non_blocking=True)
+        self.h_loss.copy_(f["loss"], non_blocking=True)
+
+
 class EntropySlsmStep:
     """entropy_from_logits, selective_log_softmax_fwd, selective_log_softmax_bwd."""
 
@@ -414,9 +512,11 @@ def make_spec(args):
     return W.get(args.workload, **over)
 
 
-def make_step(spec, seed, device, fused=False):
+def make_step(spec, seed, device, fused=False, vocab_shards=0):
     if spec.name.startswith("entropy_slsm"):
         return EntropySlsmStep(spec, seed, device)
+    if vocab_shards:
+        return VocabShardStep(spec, seed, device, vocab_shards)
     return FusedStep(spec, seed, device) if fused else GrpoStep(spec, seed, device)
 
 
@@ -560,6 +660,8 @@ def parse_args(argv=None):
     ap.add_argument("--strided", action="store_true")
     ap.add_argument("--fused", action="store_true",
                     help="GRPO workloads: time grpo_loss_fused (one kernel) instead of grpo_loss_fwd + grpo_loss_bwd")
+    ap.add_argument("--vocab-shards", type=int, default=0,
+                    help="GRPO workloads: the vocabulary-parallel step of this many shards, run shard after shard")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -661,7 +763,7 @@ def main(argv=None):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     spec = make_spec(args)
-    step = make_step(spec, args.seed + rank, device, fused=args.fused)
+    step = make_step(spec, args.seed + rank, device, fused=args.fused, vocab_shards=args.vocab_shards)
     flush_buf = L2Flush(device)
 
     # one untimed step to classify rows, then calibrate the step count
@@ -720,7 +822,8 @@ def main(argv=None):
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": int(per_launch[dom])},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": len(step.kernels) * K,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": getattr(step, "launches_per_step", len(step.kernels)) * K,
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
             "timed_wall_s": round(wall, 3), "kernel_source": kernel_source_hash(),

@@ -261,6 +261,108 @@ grpo_status grpo_seq_terms(int64_t B, int64_t L, const float* logp, const float*
                            float beta, float eps_low, float eps_high, float* loss, float* kl, float* dlogp,
                            float* seq_ratio, uint8_t* seq_is_clipped, grpo_stream_t stream);
 
+/*
+ * Vocabulary-parallel form.  When the LM head is split over ranks by vocabulary (rank k
+ * holds the columns [vocab_start_k, vocab_start_{k+1}) of every row), the row pass runs
+ * per shard; the only exchange is one all-gather of a 4-float statistic per row:
+ *
+ *   1. grpo_vocab_shard_stats on each rank's shard         -> stats_k [B*L][4]
+ *   2. all-gather of stats_k over the ranks (the caller's collective, rank order)
+ *                                                          -> stats_all [world][B*L][4]
+ *   3. grpo_vocab_combine on every rank (same result on each): lse, logp, entropy and
+ *      the GRPO terms of the full rows, and p_rest for the backward
+ *   4. grpo_loss_bwd_vocab_shard (or selective_log_softmax_bwd_vocab_shard) on each
+ *      rank's shard -> that shard's columns of dlogits.  entropy_from_logits_bwd needs no
+ *      variant: given the full rows' lse and H it is already column-local.
+ *
+ * The definitions are those of the unsplit entry points above (the pages shard nothing;
+ * the split is exact algebra of the log-sum-exp).  A shard's statistic is, with
+ * c = log2(e) / T and its own offset a (its maximum logit times c, rounded to fp32):
+ *   a,  s = sum_j 2^(x_j c - a),  u = sum_j 2^(x_j c - a) (x_j c - a),
+ *   x_sel = the raw logit at idx if idx falls in the shard, else 0.
+ * Merged over the shards (largest offset A first): lse = ln2 A + ln S,
+ * H = ln S - ln2 U / S, logp = ln2 (x_sel c - A) - ln S, as in the unsplit forward.
+ */
+
+/*
+ * grpo_vocab_shard_stats -- the per-row statistic of one vocabulary shard.
+ *
+ *   logits_shard  [B, L, V_k] bf16 or fp32: columns [vocab_start, vocab_start + V_k)
+ *                 of the full rows, any row strides (a column slice of the full tensor
+ *                 is a valid view)
+ *   vocab_start   >= 0, the shard's first column in the full vocabulary
+ *   idx           [B*L] int64 sampled tokens (full-vocabulary indices), or NULL
+ *   mask          [B*L] uint8 or NULL; masked rows are not read and get (0, 0, 0, 0)
+ *   T             > 0 finite
+ *   stats         [B*L][4] fp32 output (a, s, u, x_sel), 16-byte aligned
+ */
+grpo_status grpo_vocab_shard_stats(const grpo_rows* logits_shard, int64_t vocab_start, const int64_t* idx,
+                                   const uint8_t* mask, float T, float* stats, grpo_stream_t stream);
+
+/*
+ * grpo_vocab_combine -- merge the gathered shard statistics into the full rows' forward
+ * outputs.
+ *
+ *   world         1 <= world <= GRPO_VOCAB_MAX_WORLD shards
+ *   stats_all     [world][B*L][4] fp32: shard k's grpo_vocab_shard_stats output at k
+ *   vocab_starts  HOST array of world + 1 increasing int64: shard k holds columns
+ *                 [vocab_starts[k], vocab_starts[k+1]); vocab_starts[0] = 0 and
+ *                 vocab_starts[world] = V, the full vocabulary
+ *   B, L          rows are r = b*L + l
+ *   idx           [B*L] int64 or NULL.  NULL: entropy / lse only (logp, loss, p_rest NULL)
+ *   lse           [B*L] fp32 output (required);  entropy: [B*L] fp32 output or NULL
+ *   logp          [B*L] fp32 output (required when idx is given)
+ *   p_rest        [B*L] fp32 output or NULL: the probability mass of the row outside the
+ *                 shard that holds idx; the backward of that shard needs it
+ *   loss          NULL: selective log-softmax only.  Otherwise the GRPO terms as in
+ *                 grpo_loss_fwd, with old_logp, ref_logp, adv, mask, beta, eps_low,
+ *                 eps_high, kl, is_clipped meaning what they mean there
+ *   dev_err       nullable device int32 error word
+ *
+ * Masked rows (mask given and 0) write +0.0 to every output.  An idx outside [0, V) on
+ * an unmasked row writes NaN to logp, loss, kl and p_rest and sets
+ * GRPO_DEVERR_IDX_OUT_OF_RANGE.  The result is the same on every rank for the same
+ * stats_all.
+ */
+#define GRPO_VOCAB_MAX_WORLD 64
+grpo_status grpo_vocab_combine(int32_t world, const float* stats_all, const int64_t* vocab_starts, int64_t B,
+                               int64_t L, const int64_t* idx, const float* old_logp, const float* ref_logp,
+                               const float* adv, const uint8_t* mask, float T, float beta, float eps_low,
+                               float eps_high, float* loss, float* logp, float* lse, float* kl,
+                               uint8_t* is_clipped, float* entropy, float* p_rest, int32_t* dev_err,
+                               grpo_stream_t stream);
+
+/*
+ * grpo_loss_bwd_vocab_shard -- grpo_loss_bwd on one vocabulary shard: the shard's
+ * columns of dlogits_rj = g_r (1[j == idx_r] - p_j), with the same row factor g_r and the
+ * same zero-row early-out.  The idx element, on the shard that holds it, is
+ * g_r (1 - p_idx) = sign(g_r) |g_r| (sum of the shard's other p_j + p_rest_r).
+ *
+ *   logits_shard, vocab_start   as in grpo_vocab_shard_stats
+ *   vocab_total                 V, the full vocabulary (idx must lie in [0, V))
+ *   idx, old_logp, ref_logp, adv, mask, dloss, T, beta, eps_low, eps_high: as in
+ *   grpo_loss_bwd;  logp, lse, p_rest [B*L] fp32 from grpo_vocab_combine
+ *   dlogits_shard               [B, L, V_k] output, same dtype and shape as logits_shard
+ *                               (may alias it exactly)
+ */
+grpo_status grpo_loss_bwd_vocab_shard(const grpo_rows* logits_shard, int64_t vocab_start, int64_t vocab_total,
+                                      const int64_t* idx, const float* old_logp, const float* ref_logp,
+                                      const float* adv, const uint8_t* mask, const float* dloss,
+                                      const float* logp, const float* lse, const float* p_rest, float T,
+                                      float beta, float eps_low, float eps_high, const grpo_rows* dlogits_shard,
+                                      int32_t* dev_err, grpo_stream_t stream);
+
+/*
+ * selective_log_softmax_bwd_vocab_shard -- selective_log_softmax_bwd on one vocabulary
+ * shard (g_r = dlogp_r / T), with lse and p_rest from grpo_vocab_combine; arguments as in
+ * grpo_loss_bwd_vocab_shard.
+ */
+grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard, int64_t vocab_start,
+                                                  int64_t vocab_total, const int64_t* idx, const float* dlogp,
+                                                  const float* lse, const float* p_rest, float T,
+                                                  const grpo_rows* dlogits_shard, int32_t* dev_err,
+                                                  grpo_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* grpo_status_string(grpo_status status);
 

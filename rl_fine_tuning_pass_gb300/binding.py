@@ -23,7 +23,9 @@ GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
 
 EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_logits",
             "entropy_from_logits_bwd", "selective_log_softmax_fwd", "selective_log_softmax_bwd",
-            "grpo_seq_terms", "grpo_status_string")
+            "grpo_seq_terms", "grpo_vocab_shard_stats", "grpo_vocab_combine", "grpo_loss_bwd_vocab_shard",
+            "selective_log_softmax_bwd_vocab_shard", "grpo_status_string")
+GRPO_VOCAB_MAX_WORLD = 64
 
 
 class GrpoRows(ctypes.Structure):
@@ -64,6 +66,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "grpo_seq_terms": [ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _F, _F, _F, _P, _P, _P, _P, _P, _P],
         "selective_log_softmax_fwd": [rows_p, _P, _F, _P, _P, _P, _P],
         "selective_log_softmax_bwd": [rows_p, _P, _P, _P, _F, rows_p, _P, _P],
+        "grpo_vocab_shard_stats": [rows_p, ctypes.c_int64, _P, _P, _F, _P, _P],
+        "grpo_vocab_combine": [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P,
+                               _F, _F, _F, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+        "grpo_loss_bwd_vocab_shard": [rows_p, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _F, _F, _F, _F, rows_p, _P, _P],
+        "selective_log_softmax_bwd_vocab_shard": [rows_p, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _F,
+                                                  rows_p, _P, _P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -276,3 +285,93 @@ def grpo_seq_terms(logp, adv, dloss, *, B, L, beta, eps_low, eps_high, old_logp=
         out["seq_ratio"].data_ptr(), out["seq_is_clipped"].data_ptr(), _stream(dev))
     _check("grpo_seq_terms", st)
     return out
+
+
+# ---------------------------------------------------------------------------
+# vocabulary-parallel form (each rank holds a column shard of every row)
+# ---------------------------------------------------------------------------
+
+def grpo_vocab_shard_stats(logits_shard, vocab_start, *, T=1.0, idx=None, mask=None):
+    """Per-row statistic (a, s, u, x_sel) of one vocabulary shard: [B*L, 4] fp32."""
+    B, L = _shape(logits_shard)
+    R = B * L
+    stats = torch.empty(R, 4, dtype=torch.float32, device=logits_shard.device)
+    x = rows_of(logits_shard)
+    st = load_library().grpo_vocab_shard_stats(
+        ctypes.byref(x), int(vocab_start), _ptr(idx, torch.int64, R, "idx"), _ptr(mask, torch.uint8, R, "mask"),
+        float(T), stats.data_ptr(), _stream(logits_shard.device))
+    _check("grpo_vocab_shard_stats", st)
+    return stats
+
+
+def grpo_vocab_combine(stats_all, vocab_starts, B, L, *, T=1.0, idx=None, adv=None, grpo=False, beta=0.0,
+                       eps_low=0.2, eps_high=0.2, old_logp=None, ref_logp=None, mask=None, with_entropy=True,
+                       with_p_rest=True, dev_err=None):
+    """Merge gathered shard statistics [world, B*L, 4] (rank order) into the full rows'
+    outputs: dict with lse (+ entropy), and with idx given logp and p_rest, and with
+    grpo=True the GRPO terms (loss, kl, is_clipped)."""
+    world = int(stats_all.shape[0])
+    R = B * L
+    dev = stats_all.device
+    if stats_all.dtype != torch.float32 or tuple(stats_all.shape) != (world, R, 4) or not stats_all.is_contiguous():
+        raise ValueError("stats_all must be a contiguous [world, B*L, 4] float32 tensor")
+    if not stats_all.is_cuda:
+        raise ValueError("stats_all must be a CUDA tensor")
+    starts = (ctypes.c_int64 * (world + 1))(*[int(v) for v in vocab_starts])
+    if len(vocab_starts) != world + 1:
+        raise ValueError("vocab_starts needs world + 1 entries")
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"lse": torch.empty(R, **f32), "entropy": torch.empty(R, **f32) if with_entropy else None,
+           "logp": None, "p_rest": None, "loss": None, "kl": None, "is_clipped": None}
+    if idx is not None:
+        out["logp"] = torch.empty(R, **f32)
+        out["p_rest"] = torch.empty(R, **f32) if with_p_rest else None
+    if grpo:
+        out["loss"], out["kl"] = torch.empty(R, **f32), torch.empty(R, **f32)
+        out["is_clipped"] = torch.empty(R, dtype=torch.uint8, device=dev)
+    p = lambda k, dt=torch.float32: _ptr(out[k], dt, R, k)
+    st = load_library().grpo_vocab_combine(
+        world, stats_all.data_ptr(), starts, B, L, _ptr(idx, torch.int64, R, "idx"),
+        _ptr(old_logp, torch.float32, R, "old_logp"), _ptr(ref_logp, torch.float32, R, "ref_logp"),
+        _ptr(adv, torch.float32, B, "adv"), _ptr(mask, torch.uint8, R, "mask"), float(T), float(beta),
+        float(eps_low), float(eps_high), p("loss"), p("logp"), p("lse"), p("kl"), p("is_clipped", torch.uint8),
+        p("entropy"), p("p_rest"), _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(dev))
+    _check("grpo_vocab_combine", st)
+    return {k: v for k, v in out.items() if v is not None}
+
+
+def grpo_loss_bwd_vocab_shard(logits_shard, vocab_start, vocab_total, idx, adv, dloss, logp, lse, p_rest, *, T,
+                              beta, eps_low, eps_high, old_logp=None, ref_logp=None, mask=None, dlogits=None,
+                              dev_err=None):
+    """This shard's columns of the GRPO dlogits (allocated like logits_shard unless given)."""
+    B, L = _shape(logits_shard)
+    R = B * L
+    if dlogits is None:
+        dlogits = torch.empty(logits_shard.shape, dtype=logits_shard.dtype, device=logits_shard.device)
+    x, dx = rows_of(logits_shard), rows_of(dlogits)
+    st = load_library().grpo_loss_bwd_vocab_shard(
+        ctypes.byref(x), int(vocab_start), int(vocab_total), _ptr(idx, torch.int64, R, "idx"),
+        _ptr(old_logp, torch.float32, R, "old_logp"), _ptr(ref_logp, torch.float32, R, "ref_logp"),
+        _ptr(adv, torch.float32, B, "adv"), _ptr(mask, torch.uint8, R, "mask"), _ptr(dloss, torch.float32, R, "dloss"),
+        _ptr(logp, torch.float32, R, "logp"), _ptr(lse, torch.float32, R, "lse"),
+        _ptr(p_rest, torch.float32, R, "p_rest"), float(T), float(beta), float(eps_low), float(eps_high),
+        ctypes.byref(dx), _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(logits_shard.device))
+    _check("grpo_loss_bwd_vocab_shard", st)
+    return dlogits
+
+
+def selective_log_softmax_bwd_vocab_shard(logits_shard, vocab_start, vocab_total, idx, dlogp, lse, p_rest, *,
+                                          T=1.0, dlogits=None, dev_err=None):
+    """This shard's columns of the selective-log-softmax dlogits."""
+    B, L = _shape(logits_shard)
+    R = B * L
+    if dlogits is None:
+        dlogits = torch.empty(logits_shard.shape, dtype=logits_shard.dtype, device=logits_shard.device)
+    x, dx = rows_of(logits_shard), rows_of(dlogits)
+    st = load_library().selective_log_softmax_bwd_vocab_shard(
+        ctypes.byref(x), int(vocab_start), int(vocab_total), _ptr(idx, torch.int64, R, "idx"),
+        _ptr(dlogp, torch.float32, R, "dlogp"), _ptr(lse, torch.float32, R, "lse"),
+        _ptr(p_rest, torch.float32, R, "p_rest"), float(T), ctypes.byref(dx),
+        _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(logits_shard.device))
+    _check("selective_log_softmax_bwd_vocab_shard", st)
+    return dlogits

@@ -28,7 +28,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["capi.cu", "rowpass_fwd_bf16.cu", "rowpass_fwd_f32.cu", "rowpass_bwd_bf16.cu", "rowpass_bwd_f32.cu",
-           "rowpass_fused_bf16.cu", "rowpass_fused_f32.cu", "rowpass_seq.cu"]
+           "rowpass_fused_bf16.cu", "rowpass_fused_f32.cu", "rowpass_seq.cu",
+           "rowpass_vocab.cu"]
 
 
 def nvcc() -> str:

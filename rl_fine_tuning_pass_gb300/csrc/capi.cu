@@ -372,6 +372,169 @@ grpo_status grpo_seq_terms(int64_t B, int64_t L, const float* logp, const float*
   return from_cuda(grpo::launch_seq(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+grpo_status grpo_vocab_shard_stats(const grpo_rows* logits_shard, int64_t vocab_start, const int64_t* idx,
+                                   const uint8_t* mask, float T, float* stats, grpo_stream_t stream) {
+  grpo_status st = check_rows(logits_shard);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T) || vocab_start < 0) return GRPO_ERR_INVALID_ARG;
+  const int64_t rows = rows_of(logits_shard);
+  if (rows == 0) return GRPO_OK;
+  if (stats == nullptr || !aligned(stats, 16) || (idx != nullptr && !aligned(idx, 8)))
+    return GRPO_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.x = view_of(logits_shard);
+  p.idx = idx;
+  p.mask = mask;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.vocab_start = vocab_start;
+  p.stats = stats;
+  return from_cuda(grpo::launch_fwd(grpo::kFwdShard, logits_shard->dtype, p, rows, device_sms(),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status grpo_vocab_combine(int32_t world, const float* stats_all, const int64_t* vocab_starts, int64_t B,
+                               int64_t L, const int64_t* idx, const float* old_logp, const float* ref_logp,
+                               const float* adv, const uint8_t* mask, float T, float beta, float eps_low,
+                               float eps_high, float* loss, float* logp, float* lse, float* kl,
+                               uint8_t* is_clipped, float* entropy, float* p_rest, int32_t* dev_err,
+                               grpo_stream_t stream) {
+  if (world < 1 || world > grpo::kVocabMaxWorld || vocab_starts == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (vocab_starts[0] != 0) return GRPO_ERR_INVALID_ARG;
+  for (int k = 0; k < world; ++k)
+    if (vocab_starts[k + 1] <= vocab_starts[k]) return GRPO_ERR_INVALID_ARG;
+  if (vocab_starts[world] > kMaxV) return GRPO_ERR_UNSUPPORTED;
+  if (B < 0 || L < 0) return GRPO_ERR_INVALID_ARG;
+  if (static_cast<long double>(B) * L > kMaxRows) return GRPO_ERR_UNSUPPORTED;
+  const bool grpo = loss != nullptr;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  if (grpo) {
+    grpo_status st = check_scalars_grpo(T, beta, eps_low, eps_high);
+    if (st != GRPO_OK) return st;
+  }
+  const int64_t rows = B * L;
+  if (rows == 0) return GRPO_OK;
+  if (stats_all == nullptr || !aligned(stats_all, 16) || !ok_f32(lse) || !ok_opt_f32(entropy) ||
+      !ok_opt_f32(p_rest) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if (idx == nullptr) {
+    if (logp != nullptr || loss != nullptr || p_rest != nullptr) return GRPO_ERR_INVALID_ARG;
+  } else if (!ok_i64(idx) || !ok_f32(logp)) {
+    return GRPO_ERR_INVALID_ARG;
+  }
+  if (grpo) {
+    if (!ok_f32(loss) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_opt_f32(kl)) return GRPO_ERR_INVALID_ARG;
+    if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+    if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  } else if (kl != nullptr || is_clipped != nullptr) {
+    return GRPO_ERR_INVALID_ARG;
+  }
+  grpo::VocabCombineParams q{};
+  q.world = world;
+  for (int k = 0; k <= world; ++k) q.starts[k] = vocab_starts[k];
+  q.stats = stats_all;
+  q.rows = rows;
+  q.p_rest = p_rest;
+  FwdParams& p = q.f;
+  p.x = grpo::RowsView{nullptr, L, 0, 0, static_cast<int>(vocab_starts[world])};
+  p.idx = idx;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.logp = logp;
+  p.lse = lse;
+  p.kl = kl;
+  p.is_clipped = is_clipped;
+  p.entropy = entropy;
+  p.dev_err = dev_err;
+  return from_cuda(grpo::launch_vocab_combine(q, grpo, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status grpo_loss_bwd_vocab_shard(const grpo_rows* logits_shard, int64_t vocab_start, int64_t vocab_total,
+                                      const int64_t* idx, const float* old_logp, const float* ref_logp,
+                                      const float* adv, const uint8_t* mask, const float* dloss,
+                                      const float* logp, const float* lse, const float* p_rest, float T,
+                                      float beta, float eps_low, float eps_high, const grpo_rows* dlogits_shard,
+                                      int32_t* dev_err, grpo_stream_t stream) {
+  grpo_status st = check_rows(logits_shard);
+  if (st != GRPO_OK) return st;
+  if ((st = check_scalars_grpo(T, beta, eps_low, eps_high)) != GRPO_OK) return st;
+  if (vocab_start < 0 || vocab_total < vocab_start + logits_shard->V || vocab_total > kMaxV)
+    return GRPO_ERR_INVALID_ARG;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits_shard, dlogits_shard, &same_phase)) != GRPO_OK) return st;
+  const int64_t rows = rows_of(logits_shard);
+  if (rows == 0) return GRPO_OK;
+  if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(logp) ||
+      !ok_f32(lse) || !ok_f32(p_rest) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  BwdParams p{};
+  p.x = view_of(logits_shard);
+  p.dx = grpo::OutView{dlogits_shard->ptr, dlogits_shard->L, dlogits_shard->stride_b, dlogits_shard->stride_l,
+                       static_cast<int>(dlogits_shard->V)};
+  p.idx = idx;
+  p.lse = lse;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.dloss = dloss;
+  p.logp = logp;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.T = T;
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.dev_err = dev_err;
+  p.vocab_start = vocab_start;
+  p.vocab_total = vocab_total;
+  p.p_rest = p_rest;
+  return from_cuda(grpo::launch_bwd_shard(true, logits_shard->dtype, same_phase, p, rows, device_sms(),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard, int64_t vocab_start,
+                                                  int64_t vocab_total, const int64_t* idx, const float* dlogp,
+                                                  const float* lse, const float* p_rest, float T,
+                                                  const grpo_rows* dlogits_shard, int32_t* dev_err,
+                                                  grpo_stream_t stream) {
+  grpo_status st = check_rows(logits_shard);
+  if (st != GRPO_OK) return st;
+  if (!finite_pos(T)) return GRPO_ERR_INVALID_ARG;
+  if (vocab_start < 0 || vocab_total < vocab_start + logits_shard->V || vocab_total > kMaxV)
+    return GRPO_ERR_INVALID_ARG;
+  bool same_phase = false;
+  if ((st = check_dlogits(logits_shard, dlogits_shard, &same_phase)) != GRPO_OK) return st;
+  const int64_t rows = rows_of(logits_shard);
+  if (rows == 0) return GRPO_OK;
+  if (!ok_i64(idx) || !ok_f32(dlogp) || !ok_f32(lse) || !ok_f32(p_rest) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  BwdParams p{};
+  p.x = view_of(logits_shard);
+  p.dx = grpo::OutView{dlogits_shard->ptr, dlogits_shard->L, dlogits_shard->stride_b, dlogits_shard->stride_l,
+                       static_cast<int>(dlogits_shard->V)};
+  p.idx = idx;
+  p.lse = lse;
+  p.dlogp_up = dlogp;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.T = T;
+  p.dev_err = dev_err;
+  p.vocab_start = vocab_start;
+  p.vocab_total = vocab_total;
+  p.p_rest = p_rest;
+  return from_cuda(grpo::launch_bwd_shard(false, logits_shard->dtype, same_phase, p, rows, device_sms(),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* grpo_status_string(grpo_status status) {
   switch (status) {
     case GRPO_OK: return "GRPO_OK";

@@ -153,7 +153,10 @@ __device__ __forceinline__ float stream_span(const typename E::storage* in, type
   return q_acc + (q2.x + q2.y);
 }
 
-template <class E, int THREADS, int UNROLL, bool GRPO, bool SAME_PHASE>
+// SHARD: the logits rows are one vocabulary shard (columns [vocab_start, vocab_start + V)
+// of rows of vocab_total columns).  The idx element is written only by the shard that
+// holds idx, as sign(g) (|g| sum of the shard's other p_j + |g| p_rest).
+template <class E, int THREADS, int UNROLL, bool GRPO, bool SAME_PHASE, bool SHARD>
 __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   using S = typename E::storage;
   const int64_t r = blockIdx.x;
@@ -166,6 +169,7 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   // are loaded in the same round trip (they are only used when g != 0)
   const int64_t id64 = p.idx[r];
   const float lse = p.lse[r];
+  const float prest = SHARD && p.p_rest != nullptr ? p.p_rest[r] : 0.f;
   bool kept = false;  // the GRPO forward read this row with evict_last
   const float g = GRPO ? grpo_row_factor(p, r, b, kept) : p.dlogp_up[r] / p.T;
   S* out = static_cast<S*>(p.dx.ptr) + b * p.dx.sb + l * p.dx.sl;
@@ -178,13 +182,17 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
     if (kept) l2_demote<THREADS>(in, static_cast<int64_t>(V) * sizeof(S));
     return;
   }
-  if (id64 < 0 || id64 >= V) {
+  if (id64 < 0 || id64 >= (SHARD ? p.vocab_total : static_cast<int64_t>(V))) {
     fill_span<E, THREADS>(out, sp, sn, E::kNaNPair);
     if (kept) l2_demote<THREADS>(in, static_cast<int64_t>(V) * sizeof(S));
     if (tid == 0 && p.dev_err) atomicOr(p.dev_err, GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT);
     return;
   }
-  const int idx = static_cast<int>(id64);
+  int idx = static_cast<int>(id64);
+  if constexpr (SHARD) {  // -1: idx is in another shard, no element of this one is excluded
+    const int64_t loc = id64 - p.vocab_start;
+    idx = loc >= 0 && loc < V ? static_cast<int>(loc) : -1;
+  }
   const float nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
   bool owner = false;
   // d_j = -sign(g) |g| p_j: negated when g > 0.  After a GRPO forward this is the row's
@@ -195,7 +203,8 @@ __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
 
   // g (1 - p_idx) = sign(g) * sum_{j != idx} |g| p_j; written by the thread that wrote
   // the idx element's provisional value, so its two stores stay in program order.
-  const float q_total = block_sum_all<THREADS>(q_part);
+  float q_total = block_sum_all<THREADS>(q_part);
+  if (SHARD) q_total += fabsf(g) * prest;
   if (owner) E::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
 
@@ -284,28 +293,26 @@ cudaError_t launch_entgrad_dtype(bool same_phase, const BwdParams& p, int64_t ro
   return cudaGetLastError();
 }
 
-template <class E, int THREADS, int U, bool GRPO, bool SAME_PHASE>
+template <class E, int THREADS, int U, bool GRPO, bool SAME_PHASE, bool SHARD>
 cudaError_t launch4(const BwdParams& p, int64_t rows, cudaStream_t s) {
-  rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE><<<dim3(static_cast<unsigned>(rows)), THREADS, 0, s>>>(p);
+  rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE, SHARD><<<dim3(static_cast<unsigned>(rows)), THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-template <class E, int THREADS, int U>
+template <class E, int THREADS, int U, bool SHARD>
 cudaError_t launch3(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, cudaStream_t s) {
-  if (grpo) return same_phase ? launch4<E, THREADS, U, true, true>(p, rows, s)
-                              : launch4<E, THREADS, U, true, false>(p, rows, s);
-  return same_phase ? launch4<E, THREADS, U, false, true>(p, rows, s)
-                    : launch4<E, THREADS, U, false, false>(p, rows, s);
+  if (grpo) return same_phase ? launch4<E, THREADS, U, true, true, SHARD>(p, rows, s)
+                              : launch4<E, THREADS, U, true, false, SHARD>(p, rows, s);
+  return same_phase ? launch4<E, THREADS, U, false, true, SHARD>(p, rows, s)
+                    : launch4<E, THREADS, U, false, false, SHARD>(p, rows, s);
 }
 
-template <class E>
+// pick_threads_bwd chooses 64 or 256 threads.
+template <class E, bool SHARD = false>
 cudaError_t launch2(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t s) {
-  switch (pick_threads_bwd(p.x.V, sizeof(typename E::storage), rows, sms)) {
-    case 32: return launch3<E, 32, kUnrollSmall>(grpo, same_phase, p, rows, s);
-    case 64: return launch3<E, 64, kUnroll>(grpo, same_phase, p, rows, s);
-    case 128: return launch3<E, 128, kUnroll>(grpo, same_phase, p, rows, s);
-    default: return launch3<E, 256, kUnroll>(grpo, same_phase, p, rows, s);
-  }
+  if (pick_threads_bwd(p.x.V, sizeof(typename E::storage), rows, sms) == 64)
+    return launch3<E, 64, kUnroll, SHARD>(grpo, same_phase, p, rows, s);
+  return launch3<E, 256, kUnroll, SHARD>(grpo, same_phase, p, rows, s);
 }
 
 }  // namespace

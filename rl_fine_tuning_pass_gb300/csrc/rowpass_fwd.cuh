@@ -155,8 +155,9 @@ __device__ __forceinline__ void masked_row_outputs(const FwdParams& p, int64_t r
 
 template <class E, int THREADS, int UNROLL, int MODE>
 __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
-  constexpr bool kIdx = MODE != kFwdEntropy;
-  constexpr bool kH = MODE == kFwdEntropy || MODE == kFwdGrpoH;
+  constexpr bool kShard = MODE == kFwdShard;
+  constexpr bool kIdx = MODE != kFwdEntropy;  // kFwdShard: only when p.idx is given
+  constexpr bool kH = MODE == kFwdEntropy || MODE == kFwdGrpoH || kShard;
   constexpr bool kGrpo = MODE == kFwdGrpo || MODE == kFwdGrpoH;
   constexpr int VEC = E::kVec;
   using S = typename E::storage;
@@ -170,9 +171,12 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   // read this row again (loaded together with the mask: one round trip); every other GRPO
   // row is kept in L2 for the backward
   const float A_pre = (kGrpo && p.beta == 0.f) ? p.adv[b] : 1.f;
-  if (kGrpo && p.mask != nullptr && p.mask[r] == 0) {
+  if ((kGrpo || kShard) && p.mask != nullptr && p.mask[r] == 0) {
     // masked token: not part of the objective; every output is +0.0, no logits read
-    if (tid == 0) masked_row_outputs(p, r);
+    if (tid == 0) {
+      if constexpr (kShard) reinterpret_cast<float4*>(p.stats)[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else masked_row_outputs(p, r);
+    }
     return;
   }
 
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   // idx is loaded now; the selected logit x[idx] only after the stream, so that no
   // dependent load delays the first logits loads of this warp
   int64_t id = 0;
-  if (kIdx && tid == 0) id = p.idx[r];
+  if (kIdx && tid == 0 && (!kShard || p.idx != nullptr)) id = p.idx[r];
 
   Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const RowSplit sp = split_row<E>(row, V);
@@ -198,8 +202,13 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   bool bad_idx = false;
   float x_idx = 0.f;
   if (kIdx && tid == 0) {
-    bad_idx = id < 0 || id >= V;
-    x_idx = E::load_scalar(row + (bad_idx ? 0 : static_cast<int>(id)));
+    if constexpr (kShard) {  // the selected logit, if idx falls in this shard
+      const int64_t loc = id - p.vocab_start;
+      if (p.idx != nullptr && loc >= 0 && loc < V) x_idx = E::load_scalar(row + static_cast<int>(loc));
+    } else {
+      bad_idx = id < 0 || id >= V;
+      x_idx = E::load_scalar(row + (bad_idx ? 0 : static_cast<int>(id)));
+    }
   }
   Stat mine;
   mine.a = rs.a;
@@ -207,7 +216,8 @@ __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
   mine.u = rs.u.x + rs.u.y;
   const Stat st = stat_block_reduce<THREADS>(mine);
   if (tid != 0) return;
-  row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx);
+  if constexpr (kShard) reinterpret_cast<float4*>(p.stats)[r] = make_float4(st.a, st.s, st.u, x_idx);
+  else row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx);
 }
 
 template <class E, int THREADS, int U>
@@ -218,6 +228,7 @@ cudaError_t launch_mode(int mode, const FwdParams& p, int64_t rows, cudaStream_t
     case kFwdEntropy: rowstats_kernel<E, THREADS, U, kFwdEntropy><<<grid, THREADS, 0, s>>>(p); break;
     case kFwdGrpo: rowstats_kernel<E, THREADS, U, kFwdGrpo><<<grid, THREADS, 0, s>>>(p); break;
     case kFwdGrpoH: rowstats_kernel<E, THREADS, U, kFwdGrpoH><<<grid, THREADS, 0, s>>>(p); break;
+    case kFwdShard: rowstats_kernel<E, THREADS, U, kFwdShard><<<grid, THREADS, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

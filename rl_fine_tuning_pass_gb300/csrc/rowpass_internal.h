@@ -70,6 +70,7 @@ enum FwdMode : int {
   kFwdEntropy = 1,  // entropy only
   kFwdGrpo = 2,     // GRPO loss, logp, lse (+ kl, is_clipped)
   kFwdGrpoH = 3,    // kFwdGrpo plus the entropy output
+  kFwdShard = 4,    // one vocabulary shard's statistic (a, s, u, x_sel) per row
 };
 
 struct FwdParams {
@@ -90,6 +91,9 @@ struct FwdParams {
   uint8_t* is_clipped;    // nullable
   float* entropy;         // nullable except in kFwdEntropy / kFwdGrpoH
   int32_t* dev_err;       // nullable
+  // kFwdShard: the shard's first column in the full vocabulary; output [rows][4]
+  int64_t vocab_start;
+  float* stats;
 };
 
 struct BwdParams {
@@ -114,6 +118,11 @@ struct BwdParams {
   float beta;
   float lo, hi;
   int32_t* dev_err;
+  // vocabulary shard (the *_vocab_shard entry points): columns [vocab_start,
+  // vocab_start + V) of rows of vocab_total columns; p_rest = mass outside the idx shard
+  int64_t vocab_start;
+  int64_t vocab_total;
+  const float* p_rest;
 };
 
 // Fused forward + backward: the forward's inputs and outputs, the gradient rows and the
@@ -143,6 +152,18 @@ struct SeqParams {
 };
 cudaError_t launch_seq(const SeqParams& p, cudaStream_t stream);
 
+// Merge of gathered vocabulary-shard statistics (one thread per row).
+constexpr int kVocabMaxWorld = 64;
+struct VocabCombineParams {
+  int world;
+  int64_t starts[kVocabMaxWorld + 1];  // shard k: columns [starts[k], starts[k+1])
+  const float* stats;                  // [world][rows][4]
+  int64_t rows;
+  FwdParams f;                         // x.L, idx, old/ref, adv, mask, c, beta, lo, hi, outputs
+  float* p_rest;                       // nullable
+};
+cudaError_t launch_vocab_combine(const VocabCombineParams& p, bool grpo, cudaStream_t stream);
+
 // Kernel launchers, one translation unit per element type (compiled in parallel).
 cudaError_t launch_fwd_bf16(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
 cudaError_t launch_fwd_f32(int mode, const FwdParams& p, int64_t rows, int sms, cudaStream_t stream);
@@ -150,6 +171,11 @@ cudaError_t launch_bwd_bf16(bool grpo, bool same_phase, const BwdParams& p, int6
                             cudaStream_t stream);
 cudaError_t launch_bwd_f32(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
                            cudaStream_t stream);
+// The same backward on one vocabulary shard (BwdParams::vocab_start / vocab_total / p_rest).
+cudaError_t launch_bwd_shard_bf16(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                                  cudaStream_t stream);
+cudaError_t launch_bwd_shard_f32(bool grpo, bool same_phase, const BwdParams& p, int64_t rows, int sms,
+                                 cudaStream_t stream);
 
 cudaError_t launch_entgrad_bf16(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t stream);
 cudaError_t launch_entgrad_f32(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t stream);
@@ -180,6 +206,11 @@ inline cudaError_t launch_bwd(bool grpo, int dtype, bool same_phase, const BwdPa
                               cudaStream_t stream) {
   return dtype == 1 ? launch_bwd_bf16(grpo, same_phase, p, rows, sms, stream)
                     : launch_bwd_f32(grpo, same_phase, p, rows, sms, stream);
+}
+inline cudaError_t launch_bwd_shard(bool grpo, int dtype, bool same_phase, const BwdParams& p, int64_t rows,
+                                    int sms, cudaStream_t stream) {
+  return dtype == 1 ? launch_bwd_shard_bf16(grpo, same_phase, p, rows, sms, stream)
+                    : launch_bwd_shard_f32(grpo, same_phase, p, rows, sms, stream);
 }
 
 }  // namespace grpo

@@ -153,6 +153,50 @@ def test_slsm_and_entropy_validation(lib):
                                          ctypes.byref(rows(ptr=FAKE + (1 << 20))), None, None) == INV
 
 
+def test_vocab_parallel_validation(lib):
+    """The vocabulary-shard entry points reject bad shards, starts and pointer sets on the
+    host, before any launch."""
+    x = rows()
+    def stats(T=1.0, start=0, out=FAKE, idx=None):
+        return lib.grpo_vocab_shard_stats(ctypes.byref(x), start, idx, None, T, out, None)
+    assert stats(T=0.0) == INV
+    assert stats(start=-1) == INV
+    assert stats(out=None) == INV
+    assert stats(out=FAKE + 8) == INV                  # stats need 16-byte alignment
+    assert stats(idx=FAKE + 4) == INV
+    assert lib.grpo_vocab_shard_stats(ctypes.byref(rows(B=0)), 0, None, None, 1.0, None, None) == binding.GRPO_OK
+
+    def comb(world=2, starts=(0, 10, 64), idx=FAKE, logp=FAKE + 64, lse=FAKE + 128, loss=None, adv=None,
+             st=FAKE, p_rest=None, beta=0.0, ref=None, kl=None):
+        arr = (ctypes.c_int64 * len(starts))(*starts)
+        return lib.grpo_vocab_combine(world, st, arr, 2, 8, idx, None, ref, adv, None, 1.0, beta, 0.2, 0.2,
+                                      loss, logp, lse, kl, None, None, p_rest, None, None)
+    assert comb(world=0, starts=(0,)) == INV
+    assert comb(world=65, starts=tuple(range(66))) == INV
+    assert comb(starts=(1, 10, 64)) == INV                       # must start at 0
+    assert comb(starts=(0, 10, 10)) == INV                       # empty shard
+    assert comb(starts=(0, 20, 10)) == INV                       # decreasing
+    assert comb(st=FAKE + 4) == INV                              # 16-byte stats
+    assert comb(idx=None) == INV                                 # logp without idx
+    assert comb(idx=None, logp=None, p_rest=FAKE) == INV         # p_rest without idx
+    assert comb(lse=None) == INV
+    assert comb(loss=FAKE + 192, adv=None) == INV                # GRPO terms need adv
+    assert comb(loss=FAKE + 192, adv=FAKE, beta=0.1) == INV      # and ref when beta > 0
+    assert comb(kl=FAKE) == INV                                  # kl only with the GRPO terms
+
+    far = rows(ptr=FAKE + (1 << 20))
+    def sbwd(start=0, total=64, dx=far, p_rest=FAKE, T=1.0):
+        return lib.grpo_loss_bwd_vocab_shard(ctypes.byref(x), start, total, FAKE, None, None, FAKE, None, FAKE,
+                                             FAKE, FAKE, p_rest, T, 0.0, 0.2, 0.2, ctypes.byref(dx), None, None)
+    assert sbwd(total=63) == INV                                 # shard past the vocabulary
+    assert sbwd(start=-1) == INV
+    assert sbwd(p_rest=None) == INV
+    assert sbwd(T=0.0) == INV
+    assert sbwd(dx=rows(ptr=FAKE + 64)) == INV                   # partial overlap
+    assert lib.selective_log_softmax_bwd_vocab_shard(ctypes.byref(x), 8, 60, FAKE, FAKE, FAKE, FAKE, 1.0,
+                                                     ctypes.byref(far), None, None) == INV
+
+
 def test_rows_of_strides():
     import torch
     base = torch.empty(4, 9, 16, dtype=torch.bfloat16)

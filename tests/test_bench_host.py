@@ -84,3 +84,11 @@ def test_reference_arm_line_shape():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "grpo_b4_l512_v32000"
+
+
+def test_vocab_shard_starts_cover_the_vocabulary():
+    for V, S in [(32000, 4), (151936, 8), (7, 3), (5, 5)]:
+        st = bench.vocab_shard_starts(V, S)
+        assert st[0] == 0 and st[-1] == V and len(st) == S + 1
+        w = np.diff(st)
+        assert (w >= 1).all() and w.max() - w.min() <= 1
