@@ -159,6 +159,7 @@ __device__ __forceinline__ float stream_span(const typename E::storage* in, type
 template <class E, int THREADS, int UNROLL, bool GRPO, bool SAME_PHASE, bool SHARD>
 __global__ void __launch_bounds__(THREADS) rowgrad_kernel(const BwdParams p) {
   using S = typename E::storage;
+  wait_for_previous_grids();
   const int64_t r = blockIdx.x;
   const int64_t b = r / p.x.L;
   const int64_t l = r - b * p.x.L;
@@ -258,6 +259,7 @@ __device__ __forceinline__ void stream_span_entropy(const typename E::storage* i
 template <class E, int THREADS, int UNROLL, bool SAME_PHASE>
 __global__ void __launch_bounds__(THREADS) entgrad_kernel(const BwdParams p) {
   using S = typename E::storage;
+  wait_for_previous_grids();
   const int64_t r = blockIdx.x;
   const int64_t b = r / p.x.L;
   const int64_t l = r - b * p.x.L;
@@ -284,19 +286,18 @@ template <class E>
 cudaError_t launch_entgrad_dtype(bool same_phase, const BwdParams& p, int64_t rows, int sms, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(rows));
   if (pick_threads_bwd(p.x.V, sizeof(typename E::storage), rows, sms) == 64) {
-    if (same_phase) entgrad_kernel<E, 64, kUnroll, true><<<grid, 64, 0, s>>>(p);
-    else entgrad_kernel<E, 64, kUnroll, false><<<grid, 64, 0, s>>>(p);
+    return same_phase ? launch_after_previous(entgrad_kernel<E, 64, kUnroll, true>, grid, dim3(64), s, p)
+                      : launch_after_previous(entgrad_kernel<E, 64, kUnroll, false>, grid, dim3(64), s, p);
   } else {
-    if (same_phase) entgrad_kernel<E, 256, kUnroll, true><<<grid, 256, 0, s>>>(p);
-    else entgrad_kernel<E, 256, kUnroll, false><<<grid, 256, 0, s>>>(p);
+    return same_phase ? launch_after_previous(entgrad_kernel<E, 256, kUnroll, true>, grid, dim3(256), s, p)
+                      : launch_after_previous(entgrad_kernel<E, 256, kUnroll, false>, grid, dim3(256), s, p);
   }
-  return cudaGetLastError();
 }
 
 template <class E, int THREADS, int U, bool GRPO, bool SAME_PHASE, bool SHARD>
 cudaError_t launch4(const BwdParams& p, int64_t rows, cudaStream_t s) {
-  rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE, SHARD><<<dim3(static_cast<unsigned>(rows)), THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_after_previous(rowgrad_kernel<E, THREADS, U, GRPO, SAME_PHASE, SHARD>,
+                               dim3(static_cast<unsigned>(rows)), dim3(THREADS), s, p);
 }
 
 template <class E, int THREADS, int U, bool SHARD>

@@ -18,6 +18,10 @@ namespace grpo {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
+// First statement of every kernel: wait until the grids launched before this one in the
+// stream have completed and their memory is visible (see launch_after_previous).
+__device__ __forceinline__ void wait_for_previous_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 2^x on the SFU (PTX ex2.approx.ftz.f32).  Results below 2^-126 flush to zero.
 __device__ __forceinline__ float ex2(float x) {
   float y;

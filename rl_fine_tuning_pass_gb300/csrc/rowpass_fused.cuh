@@ -16,6 +16,7 @@ namespace {
 
 template <class E, int THREADS, int UNROLL, bool kH, bool SAME_PHASE>
 __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
+  wait_for_previous_grids();
   constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
   constexpr int VEC = E::kVec;
   using S = typename E::storage;
@@ -115,9 +116,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
 template <class E, int THREADS, int U, bool kH>
 cudaError_t launch_fused_h(const FusedParams& q, int64_t rows, bool same_phase, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(rows));
-  if (same_phase) fused_kernel<E, THREADS, U, kH, true><<<grid, THREADS, 0, s>>>(q);
-  else fused_kernel<E, THREADS, U, kH, false><<<grid, THREADS, 0, s>>>(q);
-  return cudaGetLastError();
+  return same_phase ? launch_after_previous(fused_kernel<E, THREADS, U, kH, true>, grid, dim3(THREADS), s, q)
+                    : launch_after_previous(fused_kernel<E, THREADS, U, kH, false>, grid, dim3(THREADS), s, q);
 }
 
 template <class E, int THREADS, int U>

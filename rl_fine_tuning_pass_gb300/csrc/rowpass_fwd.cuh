@@ -155,6 +155,7 @@ __device__ __forceinline__ void masked_row_outputs(const FwdParams& p, int64_t r
 
 template <class E, int THREADS, int UNROLL, int MODE>
 __global__ void __launch_bounds__(THREADS) rowstats_kernel(const FwdParams p) {
+  wait_for_previous_grids();
   constexpr bool kShard = MODE == kFwdShard;
   constexpr bool kIdx = MODE != kFwdEntropy;  // kFwdShard: only when p.idx is given
   constexpr bool kH = MODE == kFwdEntropy || MODE == kFwdGrpoH || kShard;
@@ -224,14 +225,16 @@ template <class E, int THREADS, int U>
 cudaError_t launch_mode(int mode, const FwdParams& p, int64_t rows, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(rows));
   switch (mode) {
-    case kFwdSlsm: rowstats_kernel<E, THREADS, U, kFwdSlsm><<<grid, THREADS, 0, s>>>(p); break;
-    case kFwdEntropy: rowstats_kernel<E, THREADS, U, kFwdEntropy><<<grid, THREADS, 0, s>>>(p); break;
-    case kFwdGrpo: rowstats_kernel<E, THREADS, U, kFwdGrpo><<<grid, THREADS, 0, s>>>(p); break;
-    case kFwdGrpoH: rowstats_kernel<E, THREADS, U, kFwdGrpoH><<<grid, THREADS, 0, s>>>(p); break;
-    case kFwdShard: rowstats_kernel<E, THREADS, U, kFwdShard><<<grid, THREADS, 0, s>>>(p); break;
+    case kFwdSlsm: return launch_after_previous(rowstats_kernel<E, THREADS, U, kFwdSlsm>, grid, dim3(THREADS), s, p);
+    case kFwdEntropy:
+      return launch_after_previous(rowstats_kernel<E, THREADS, U, kFwdEntropy>, grid, dim3(THREADS), s, p);
+    case kFwdGrpo: return launch_after_previous(rowstats_kernel<E, THREADS, U, kFwdGrpo>, grid, dim3(THREADS), s, p);
+    case kFwdGrpoH:
+      return launch_after_previous(rowstats_kernel<E, THREADS, U, kFwdGrpoH>, grid, dim3(THREADS), s, p);
+    case kFwdShard:
+      return launch_after_previous(rowstats_kernel<E, THREADS, U, kFwdShard>, grid, dim3(THREADS), s, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 template <class E>

@@ -4,9 +4,30 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace grpo {
+
+// Every kernel of the library is launched with programmatic stream serialization, and
+// each one waits (griddepcontrol.wait) for the grids before it in the stream to complete
+// before it touches memory.  The launch and the CTAs' set-up then overlap the previous
+// kernel's drain instead of following it; the ordering the stream guarantees is kept.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Error bit OR-ed into the caller's device error word (GRPO_DEVERR_IDX_OUT_OF_RANGE).
 constexpr int GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT = 1;

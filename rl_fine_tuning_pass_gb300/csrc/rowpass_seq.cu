@@ -25,6 +25,7 @@ __device__ __forceinline__ float block_sum_f(float v) { return block_sum_all<THR
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) seq_kernel(const SeqParams p) {
+  wait_for_previous_grids();
   const int64_t b = blockIdx.x;
   const int64_t L = p.L;
   const int64_t base = b * L;
@@ -81,8 +82,7 @@ __global__ void __launch_bounds__(THREADS) seq_kernel(const SeqParams p) {
 }  // namespace
 
 cudaError_t launch_seq(const SeqParams& p, cudaStream_t stream) {
-  seq_kernel<256><<<dim3(static_cast<unsigned>(p.B)), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after_previous(seq_kernel<256>, dim3(static_cast<unsigned>(p.B)), dim3(256), stream, p);
 }
 
 }  // namespace grpo

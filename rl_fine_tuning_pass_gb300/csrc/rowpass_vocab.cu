@@ -15,6 +15,7 @@ namespace {
 
 template <int MODE>
 __global__ void __launch_bounds__(256) vocab_combine_kernel(const VocabCombineParams q) {
+  wait_for_previous_grids();
   const FwdParams& p = q.f;
   const float4* stats = reinterpret_cast<const float4*>(q.stats);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -73,14 +74,11 @@ cudaError_t launch_vocab_combine(const VocabCombineParams& q, bool grpo, cudaStr
   const int64_t blocks = (q.rows + 255) / 256;
   const dim3 grid(static_cast<unsigned>(blocks < 65535 ? blocks : 65535));
   if (grpo) {
-    if (q.f.entropy) vocab_combine_kernel<kFwdGrpoH><<<grid, 256, 0, s>>>(q);
-    else vocab_combine_kernel<kFwdGrpo><<<grid, 256, 0, s>>>(q);
-  } else if (q.f.idx) {
-    vocab_combine_kernel<kFwdSlsm><<<grid, 256, 0, s>>>(q);
-  } else {
-    vocab_combine_kernel<kFwdEntropy><<<grid, 256, 0, s>>>(q);
+    if (q.f.entropy) return launch_after_previous(vocab_combine_kernel<kFwdGrpoH>, grid, dim3(256), s, q);
+    return launch_after_previous(vocab_combine_kernel<kFwdGrpo>, grid, dim3(256), s, q);
   }
-  return cudaGetLastError();
+  if (q.f.idx) return launch_after_previous(vocab_combine_kernel<kFwdSlsm>, grid, dim3(256), s, q);
+  return launch_after_previous(vocab_combine_kernel<kFwdEntropy>, grid, dim3(256), s, q);
 }
 
 }  // namespace grpo
