@@ -16,7 +16,9 @@ Sources (the three web pages the method is described on):
   analysis".
 * [Liger-TRL]  "Liger GRPO meets TRL".  Sections used: "2. The core principle
   that sets GRPO apart from PPO" (group-relative, verifiable rewards),
-  "4. The chunked loss that computes gradients during the forward".
+  "3. The memory bottleneck of storing the full logits" (the logits are the LM head
+  applied to the hidden states), "4. The chunked loss that computes gradients during
+  the forward".
 * [axolotl]    "Axolotl: entropy and selective log-softmax with Triton kernels"
   (write-up of axolotl PR #3510).  Sections used: "1. benchmarks/bench_entropy.py"
   (the original eager entropy definition), "2. benchmarks/bench_selective_logsoftmax.py".
@@ -57,6 +59,7 @@ __all__ = [
     "entropy_from_logits_bwd",
     "grpo_seq_terms",
     "grpo_seq_loss_bwd",
+    "fused_linear_grpo",
     "per_row",
 ]
 
@@ -421,3 +424,28 @@ def grpo_seq_loss_bwd(x, idx, old_logp, ref_logp, adv_seq, mask, dloss, B, L, T,
     terms = grpo_seq_terms(logp, old_logp, ref_logp, adv_seq, mask, dloss, B, L, beta, eps_low, eps_high)
     g = terms["dlogp"] / np.float64(T)
     return softmax_gather_grad(x, idx, g, T), g, terms
+
+
+def fused_linear_grpo(h, W, idx, old_logp, ref_logp, adv_row, mask, dloss, T, beta, eps_low, eps_high):
+    """The GRPO loss on top of the LM head, with the gradients of the hidden states and
+    of the head weight (fp64).
+
+    [Liger-TRL], section 3: the logits are the LM head applied to the hidden states of
+    the rows, x = h W^T ([R, H] x [H, V]); section 4: the loss of each chunk of rows
+    computes, during its forward, the gradient of its input chunk and of the head
+    weight, and the weight gradient is accumulated over the chunks.  Splitting the rows
+    into chunks changes no value, so the definition is written on all rows at once:
+
+        x = h W^T,  loss / logp / ... = grpo_loss_fwd(x),  dx = grpo_loss_bwd(x)[0],
+        grad_h = dx W,  grad_W = dx^T h        (J = sum_r dloss_r loss_r)
+
+    Returns (fwd dict as grpo_loss_fwd, grad_h [R, H], grad_W [V, H], dx [R, V]).
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    x = h @ W.T
+    fwd = grpo_loss_fwd(x, idx, old_logp, ref_logp, adv_row, mask, T, beta, eps_low, eps_high)
+    dx, _ = grpo_loss_bwd(x, idx, old_logp, ref_logp, adv_row, mask, dloss, T, beta, eps_low, eps_high)
+    grad_h = dx @ W
+    grad_W = dx.T @ h
+    return fwd, grad_h, grad_W, dx

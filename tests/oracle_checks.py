@@ -499,6 +499,87 @@ def check_seq_terms_closed_forms(orc):
     assert np.all(t["dlogp"][4:] == 0.0) and np.all(t["loss"][8:] == 0.0)
 
 
+# ---------------------------------------------------------------------------
+# the GRPO loss on top of the LM head (hidden states and head weight)
+# ---------------------------------------------------------------------------
+
+def _linear_problem(seed=11, B=2, L=5, H=7, V=13):
+    rng = np.random.default_rng(seed)
+    R = B * L
+    h = rng.standard_normal((R, H))
+    W = rng.standard_normal((V, H)) * 0.7
+    idx = rng.integers(0, V, R)
+    A = rng.standard_normal(B)
+    return rng, h, W, idx, A
+
+
+def check_fused_linear_finite_differences(orc):
+    """grad_h and grad_W of J = sum_r dloss_r * loss_r(h W^T) against central differences
+    in every element of h and of W (beta > 0, T != 1, asymmetric eps, a mask)."""
+    rng, h, W, idx, A = _linear_problem()
+    R, H = h.shape
+    V = W.shape[0]
+    L = 5
+    T, beta, el, eh = 0.8, 0.07, 0.2, 0.28
+    adv = orc.per_row(A, L)
+    lp0, _ = orc.selective_log_softmax(h @ W.T, idx, T)
+    old = lp0 + rng.standard_normal(R) * 0.25
+    ref = lp0 + rng.standard_normal(R) * 0.15
+    mask = np.ones(R, np.uint8)
+    mask[[2, 7]] = 0
+    dloss = rng.uniform(0.1, 1.0, R)
+    r = np.exp(lp0 - old)
+    assert np.all((np.abs(r - (1 - el)) > 0.01) & (np.abs(r - (1 + eh)) > 0.01)), "a row sits on a clip boundary"
+    _, gh, gW, _ = orc.fused_linear_grpo(h, W, idx, old, ref, adv, mask, dloss, T, beta, el, eh)
+
+    def J(hh, WW):
+        f = orc.grpo_loss_fwd(hh @ WW.T, idx, old, ref, adv, mask, T, beta, el, eh)
+        return float(np.sum(f["loss"] * dloss))
+
+    eps = 1e-6
+    fd_h = np.zeros_like(h)
+    for i in range(R):
+        for k in range(H):
+            e = np.zeros_like(h)
+            e[i, k] = eps
+            fd_h[i, k] = (J(h + e, W) - J(h - e, W)) / (2 * eps)
+    fd_W = np.zeros_like(W)
+    for j in range(V):
+        for k in range(H):
+            e = np.zeros_like(W)
+            e[j, k] = eps
+            fd_W[j, k] = (J(h, W + e) - J(h, W - e)) / (2 * eps)
+    _close(gh, fd_h, 1e-6, 1e-9, "grad_h")
+    _close(gW, fd_W, 1e-6, 1e-9, "grad_W")
+    assert np.all(gh[[2, 7]] == 0.0), "masked rows get no hidden-state gradient"
+
+
+def check_fused_linear_identity_head_and_invariants(orc):
+    """A head W = s I (H = V) gives the row pass on x = s h: the same forward, grad_h =
+    s dx.  A head whose rows are all equal gives uniform p and grad_h = 0 (each row of dx
+    sums to 0); every column of grad_W sums to 0 over the vocabulary for any head."""
+    rng, h, _, idx, A = _linear_problem(seed=12, H=9, V=9)
+    R, H = h.shape
+    L = 5
+    T, beta, el, eh = 1.3, 0.0, 0.2, 0.2
+    adv = orc.per_row(A, L)
+    old = rng.standard_normal(R) * 0.1 - 2.0
+    dloss = rng.uniform(0.2, 1.0, R)
+    s = 1.7
+    f, gh, gW, dx = orc.fused_linear_grpo(h, s * np.eye(H), idx, old, None, adv, None, dloss, T, beta, el, eh)
+    f2 = orc.grpo_loss_fwd(s * h, idx, old, None, adv, None, T, beta, el, eh)
+    d2, _ = orc.grpo_loss_bwd(s * h, idx, old, None, adv, None, dloss, T, beta, el, eh)
+    for k in ("loss", "logp", "lse", "entropy"):
+        _close(f[k], f2[k], 1e-13, 1e-13, f"identity head {k}")
+    _close(gh, s * d2, 1e-12, 1e-14, "identity head grad_h")
+    w = rng.standard_normal(H)
+    _, gh_eq, gW_eq, _ = orc.fused_linear_grpo(h, np.tile(w, (11, 1)), idx % 11, old, None, adv, None, dloss, T,
+                                               beta, el, eh)
+    _close(gh_eq, np.zeros_like(gh_eq), 0, 1e-12, "equal head rows: grad_h = 0")
+    for g in (gW, gW_eq):
+        _close(g.sum(axis=0), np.zeros(H), 0, 1e-12, "grad_W columns sum to 0")
+
+
 ALL_CHECKS = [
     check_bf16_decode_all_patterns,
     check_bf16_rounding_vs_torch,
@@ -522,4 +603,6 @@ ALL_CHECKS = [
     check_entropy_bwd_closed_form_v2,
     check_seq_bwd_finite_differences,
     check_seq_terms_closed_forms,
+    check_fused_linear_finite_differences,
+    check_fused_linear_identity_head_and_invariants,
 ]

@@ -38,6 +38,9 @@ MUTATIONS = [
     ("entropy_zero_terms_not_skipped", "np.where(p == 0.0, 0.0, p * (lse[:, None] - z))", "p * (lse[:, None] - z)"),
     ("entropy_sign", "np.where(p == 0.0, 0.0, p * (lse[:, None] - z))", "np.where(p == 0.0, 0.0, p * (z - lse[:, None]))"),
     ("lse_drops_max", "lse = (m + np.log(s))[..., 0]", "lse = np.log(s)[..., 0]"),
+    ("linear_grad_h_scaled", "grad_h = dx @ W\n", "grad_h = dx @ W / T\n"),
+    ("linear_grad_W_sign", "grad_W = dx.T @ h\n", "grad_W = -(dx.T @ h)\n"),
+    ("linear_head_scaled", "x = h @ W.T\n", "x = h @ W.T * 1.01\n"),
     ("all_neginf_row_not_handled", "m = np.where(np.isneginf(m), 0.0, m)", "pass"),
     ("lse_no_shift", "s = np.sum(np.exp(z - m), axis=-1, keepdims=True)\n        lse = (m + np.log(s))[..., 0]",
      "s = np.sum(np.exp(z), axis=-1, keepdims=True)\n        lse = np.log(s)[..., 0]"),
