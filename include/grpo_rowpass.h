@@ -363,6 +363,41 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
                                                   const grpo_rows* dlogits_shard, int32_t* dev_err,
                                                   grpo_stream_t stream);
 
+/*
+ * grpo_fused_linear -- the GRPO loss on top of the LM head, with the gradients of the
+ * hidden states and of the head weight, in chunks of rows.
+ *
+ * Defined by [Liger-TRL] sections 3 and 4: the logits are the head applied to the hidden
+ * states, x = h W^T; the loss of each chunk of rows computes, during its forward, the
+ * gradient of its input chunk and of the head weight, the weight gradient accumulated over
+ * the chunks, so the logits of the whole batch never exist at once.  Per chunk:
+ *   x_c = h_c W^T (fp32, tensor-core GEMM)  ->  the row pass of grpo_loss_fused on x_c
+ *   (forward outputs, dlogits in bf16)  ->  grad_hidden_c = dlogits_c W,
+ *   grad_weight += dlogits_c^T h_c  (tensor-core GEMMs, fp32 accumulation).
+ * The GEMMs run through cuBLASLt; the row pass is this library's kernel.
+ *
+ *   hidden        [B*L, H] bf16, row-major, 16-byte aligned;  H a multiple of 8
+ *   weight        [V, H] bf16, row-major, 16-byte aligned
+ *   idx, old_logp, ref_logp, adv, mask, dloss, T, beta, eps_low, eps_high, loss, logp,
+ *   lse, kl, is_clipped, entropy, dev_err: as in grpo_loss_fused (per-row arrays [B*L])
+ *   chunk_rows    rows per chunk, >= 1 (the last chunk may be shorter)
+ *   workspace     device scratch of at least grpo_fused_linear_workspace_size() bytes,
+ *                 256-byte aligned; its contents are not kept between calls
+ *   grad_hidden   [B*L, H] fp32 output (overwritten), or NULL
+ *   grad_weight   [V, H] fp32, ACCUMULATED into (+=), or NULL; 16-byte aligned
+ *
+ * The logits are formed in fp32; dlogits are rounded to bf16 (the weight's type) for the
+ * two backward GEMMs.  Calls on the same stream run in order; the library keeps one
+ * cuBLASLt handle per device.
+ */
+grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes);
+grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H, int64_t V,
+                              const int64_t* idx, const float* old_logp, const float* ref_logp, const float* adv,
+                              const uint8_t* mask, const float* dloss, float T, float beta, float eps_low,
+                              float eps_high, int64_t chunk_rows, void* workspace, uint64_t workspace_bytes,
+                              float* loss, float* logp, float* lse, float* kl, uint8_t* is_clipped, float* entropy,
+                              float* grad_hidden, float* grad_weight, int32_t* dev_err, grpo_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* grpo_status_string(grpo_status status);
 

@@ -24,7 +24,8 @@ GRPO_DEVERR_IDX_OUT_OF_RANGE = 1
 EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_logits",
             "entropy_from_logits_bwd", "selective_log_softmax_fwd", "selective_log_softmax_bwd",
             "grpo_seq_terms", "grpo_vocab_shard_stats", "grpo_vocab_combine", "grpo_loss_bwd_vocab_shard",
-            "selective_log_softmax_bwd_vocab_shard", "grpo_status_string")
+            "selective_log_softmax_bwd_vocab_shard", "grpo_fused_linear_workspace_size", "grpo_fused_linear",
+            "grpo_status_string")
 GRPO_VOCAB_MAX_WORLD = 64
 
 
@@ -73,6 +74,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                       _P, _F, _F, _F, _F, rows_p, _P, _P],
         "selective_log_softmax_bwd_vocab_shard": [rows_p, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _F,
                                                   rows_p, _P, _P],
+        "grpo_fused_linear_workspace_size": [ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)],
+        "grpo_fused_linear": [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P,
+                              _P, _P, _F, _F, _F, _F, ctypes.c_int64, _P, ctypes.c_uint64, _P, _P, _P, _P, _P, _P,
+                              _P, _P, _P, _P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -375,3 +380,54 @@ def selective_log_softmax_bwd_vocab_shard(logits_shard, vocab_start, vocab_total
         _ptr(dev_err, torch.int32, 1, "dev_err"), _stream(logits_shard.device))
     _check("selective_log_softmax_bwd_vocab_shard", st)
     return dlogits
+
+
+# ---------------------------------------------------------------------------
+# the GRPO loss on top of the LM head (hidden states and head weight)
+# ---------------------------------------------------------------------------
+
+def grpo_fused_linear_workspace_size(V, chunk_rows):
+    out = ctypes.c_uint64(0)
+    _check("grpo_fused_linear_workspace_size",
+           load_library().grpo_fused_linear_workspace_size(int(V), int(chunk_rows), ctypes.byref(out)))
+    return int(out.value)
+
+
+def grpo_fused_linear(hidden, weight, idx, adv, dloss, *, B, L, T, beta, eps_low, eps_high, old_logp=None,
+                      ref_logp=None, mask=None, chunk_rows=1024, with_grad_hidden=True, grad_weight=None,
+                      with_grad_weight=True, with_entropy=True, workspace=None, dev_err=None):
+    """GRPO loss on top of the LM head, in chunks of rows: dict with the forward outputs
+    (loss, logp, lse, kl, is_clipped, entropy), grad_hidden [B*L, H] fp32 and grad_weight
+    [V, H] fp32 (accumulated into the given tensor, else into zeros)."""
+    R, H = hidden.shape
+    V = weight.shape[0]
+    if R != B * L:
+        raise ValueError("hidden must be [B*L, H]")
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape[-1] != H:
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor with H columns")
+    dev = hidden.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"loss": torch.empty(R, **f32), "logp": torch.empty(R, **f32), "lse": torch.empty(R, **f32),
+           "kl": torch.empty(R, **f32), "is_clipped": torch.empty(R, dtype=torch.uint8, device=dev),
+           "entropy": torch.empty(R, **f32) if with_entropy else None,
+           "grad_hidden": torch.empty(R, H, **f32) if with_grad_hidden else None}
+    if with_grad_weight and grad_weight is None:
+        grad_weight = torch.zeros(V, H, **f32)
+    out["grad_weight"] = grad_weight if with_grad_weight else None
+    chunk = max(1, min(int(chunk_rows), R)) if R else 1
+    need = grpo_fused_linear_workspace_size(V, chunk)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = load_library().grpo_fused_linear(
+        hidden.data_ptr(), weight.data_ptr(), B, L, H, V, _ptr(idx, torch.int64, R, "idx"),
+        _ptr(old_logp, torch.float32, R, "old_logp"), _ptr(ref_logp, torch.float32, R, "ref_logp"),
+        _ptr(adv, torch.float32, B, "adv"), _ptr(mask, torch.uint8, R, "mask"), _ptr(dloss, torch.float32, R, "dloss"),
+        float(T), float(beta), float(eps_low), float(eps_high), chunk, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), out["loss"].data_ptr(), out["logp"].data_ptr(),
+        out["lse"].data_ptr(), out["kl"].data_ptr(), out["is_clipped"].data_ptr(),
+        _ptr(out["entropy"], torch.float32, R, "entropy"), _ptr(out["grad_hidden"], torch.float32, R * H, "grad_hidden"),
+        _ptr(out["grad_weight"], torch.float32, V * H, "grad_weight"), _ptr(dev_err, torch.int32, 1, "dev_err"),
+        _stream(dev))
+    _check("grpo_fused_linear", st)
+    return {k: v for k, v in out.items() if v is not None}

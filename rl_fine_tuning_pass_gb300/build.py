@@ -2,7 +2,8 @@
 ``rl_fine_tuning_pass_gb300/libgrpo_rowpass.so`` for sm_103a (GB300).
 
 Each translation unit is compiled in parallel with one ``-gencode`` (a minute or less),
-then linked with the static CUDA runtime.  Nothing is installed outside this directory.
+then linked with the static CUDA runtime and the toolkit's cuBLASLt (the LM-head GEMMs of
+grpo_fused_linear).  Nothing is installed outside this directory.
 
     python -m rl_fine_tuning_pass_gb300.build          # build if sources changed
     python -m rl_fine_tuning_pass_gb300.build --force  # rebuild
@@ -29,7 +30,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--ex
               "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["capi.cu", "rowpass_fwd_bf16.cu", "rowpass_fwd_f32.cu", "rowpass_bwd_bf16.cu", "rowpass_bwd_f32.cu",
            "rowpass_fused_bf16.cu", "rowpass_fused_f32.cu", "rowpass_seq.cu",
-           "rowpass_vocab.cu"]
+           "rowpass_vocab.cu", "rowpass_linear.cu"]
 
 
 def nvcc() -> str:
@@ -37,6 +38,11 @@ def nvcc() -> str:
         if cand and os.path.exists(cand):
             return cand
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the row-pass library")
+
+
+def cuda_lib_dir() -> str:
+    """The toolkit's library directory (next to nvcc), for cuBLASLt."""
+    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
 
 
 def _deps():
@@ -70,7 +76,9 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    lib_dir = cuda_lib_dir()
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-L", lib_dir, "-lcublasLt",
+           "-Xlinker", f"-rpath,{lib_dir}"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")

@@ -535,6 +535,92 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+constexpr uint64_t kLinearGemmWs = uint64_t(32) << 20;  // the GEMMs' workspace
+uint64_t round256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+int64_t linear_ld(int64_t V) { return (V + 7) / 8 * 8; }
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes) {
+  if (bytes == nullptr || V < 1 || V > kMaxV || chunk_rows < 1 || chunk_rows > kMaxRows) return GRPO_ERR_INVALID_ARG;
+  const uint64_t ld = static_cast<uint64_t>(linear_ld(V));
+  *bytes = round256(ld * chunk_rows * 4) + round256(ld * chunk_rows * 2) + kLinearGemmWs;
+  return GRPO_OK;
+}
+
+grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H, int64_t V,
+                              const int64_t* idx, const float* old_logp, const float* ref_logp, const float* adv,
+                              const uint8_t* mask, const float* dloss, float T, float beta, float eps_low,
+                              float eps_high, int64_t chunk_rows, void* workspace, uint64_t workspace_bytes,
+                              float* loss, float* logp, float* lse, float* kl, uint8_t* is_clipped, float* entropy,
+                              float* grad_hidden, float* grad_weight, int32_t* dev_err, grpo_stream_t stream) {
+  grpo_status st = check_scalars_grpo(T, beta, eps_low, eps_high);
+  if (st != GRPO_OK) return st;
+  if (B < 0 || L < 0 || H < 8 || H % 8 != 0 || V < 1 || chunk_rows < 1) return GRPO_ERR_INVALID_ARG;
+  if (V > kMaxV || static_cast<long double>(B) * L > kMaxRows || H > (int64_t(1) << 24)) return GRPO_ERR_UNSUPPORTED;
+  const int64_t rows = B * L;
+  if (rows == 0) return GRPO_OK;
+  uint64_t need = 0;
+  const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
+  grpo_fused_linear_workspace_size(V, chunk, &need);
+  if (hidden == nullptr || !aligned(hidden, 16) || weight == nullptr || !aligned(weight, 16) ||
+      workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
+    return GRPO_ERR_INVALID_ARG;
+  if (!ok_i64(idx) || !ok_opt_f32(old_logp) || !ok_f32(adv) || !ok_f32(dloss) || !ok_f32(loss) || !ok_f32(logp) ||
+      !ok_f32(lse) || !ok_opt_f32(kl) || !ok_opt_f32(entropy) || !ok_opt_i32(dev_err))
+    return GRPO_ERR_INVALID_ARG;
+  if ((grad_hidden != nullptr && !aligned(grad_hidden, 16)) || (grad_weight != nullptr && !aligned(grad_weight, 16)))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
+  if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
+  const int64_t ld = linear_ld(V);
+  grpo::FusedLinearParams q{};
+  q.hidden = static_cast<const uint16_t*>(hidden);
+  q.weight = static_cast<const uint16_t*>(weight);
+  q.rows = rows;
+  q.H = H;
+  q.V = V;
+  q.chunk = chunk;
+  q.ld = ld;
+  char* w = static_cast<char*>(workspace);
+  q.logits = reinterpret_cast<float*>(w);
+  q.dlogits = reinterpret_cast<uint16_t*>(w + round256(static_cast<uint64_t>(ld) * chunk * 4));
+  q.ws = w + round256(static_cast<uint64_t>(ld) * chunk * 4) + round256(static_cast<uint64_t>(ld) * chunk * 2);
+  q.ws_bytes = kLinearGemmWs;
+  q.grad_hidden = grad_hidden;
+  q.grad_weight = grad_weight;
+  grpo::LinearChunkParams& cp = q.chunk_params;
+  FwdParams& p = cp.f;
+  p.x = grpo::RowsView{nullptr, L, 0, 0, static_cast<int>(V)};
+  p.idx = idx;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.c = static_cast<float>(kLog2eD / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.logp = logp;
+  p.lse = lse;
+  p.kl = kl;
+  p.is_clipped = is_clipped;
+  p.entropy = entropy;
+  p.dev_err = dev_err;
+  cp.logits = q.logits;
+  cp.dlogits = q.dlogits;
+  cp.ld = ld;
+  cp.dloss = dloss;
+  cp.T = T;
+  return from_cuda(grpo::launch_fused_linear(q, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* grpo_status_string(grpo_status status) {
   switch (status) {
     case GRPO_OK: return "GRPO_OK";

@@ -173,6 +173,33 @@ struct SeqParams {
 };
 cudaError_t launch_seq(const SeqParams& p, cudaStream_t stream);
 
+// The GRPO loss on top of the LM head, in chunks of rows (rowpass_linear.cu).
+struct LinearChunkParams {
+  FwdParams f;            // per-row inputs and outputs of the whole batch; f.x.L = tokens per
+                          // sequence, f.x.V = vocabulary
+  const float* logits;    // the chunk's logits [rows][ld] fp32
+  uint16_t* dlogits;      // the chunk's dlogits [rows][ld] bf16
+  int64_t ld;             // elements between rows, a multiple of 8
+  int64_t row0;           // the chunk's first row in the batch
+  const float* dloss;     // [batch rows]
+  float T;
+};
+struct FusedLinearParams {
+  const uint16_t* hidden;  // [rows][H] bf16
+  const uint16_t* weight;  // [V][H] bf16
+  int64_t rows, H, V;
+  int64_t chunk;           // rows per chunk
+  int64_t ld;              // row stride of the chunk buffers (V rounded up to 8)
+  float* logits;           // workspace: [chunk][ld] fp32
+  uint16_t* dlogits;       // workspace: [chunk][ld] bf16
+  void* ws;                // workspace for the GEMMs
+  size_t ws_bytes;
+  float* grad_hidden;      // [rows][H] fp32, or null
+  float* grad_weight;      // [V][H] fp32, accumulated into, or null
+  LinearChunkParams chunk_params;
+};
+cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream);
+
 // Merge of gathered vocabulary-shard statistics (one thread per row).
 constexpr int kVocabMaxWorld = 64;
 struct VocabCombineParams {

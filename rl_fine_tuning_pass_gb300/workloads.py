@@ -23,6 +23,12 @@ Workloads (the shapes and distributions of the pages' benchmarks):
                            V=151936 (a Qwen3-0.6B-shaped LM head, no weights).
 * ``sweep_b16_l4096_v151936``       B=16, L=4096, V=151936 (~20 GB bf16 logits),
                            beta and the zero-advantage fraction swept.
+* ``linear_qwen3_b16_l1024_h1024_v151936``  the Qwen3-shaped GRPO batch above given as
+                           hidden states [B*L, H=1024] and an LM-head weight [V, H]
+                           (Qwen3-0.6B's hidden size), bf16, for the loss on top of the
+                           head (``generate_linear``).  h ~ N(0, 1), W ~ N(0, w_sigma^2)
+                           with w_sigma = sigma / sqrt(H), so the logits have the same
+                           N(0, sigma^2) spread as the logits workloads.
 
 The public GRPO runs the pages cite use datasets (gsm8k, TLDR) and trained
 weights that are not available here; these synthetic tensors stand in for the
@@ -37,7 +43,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-__all__ = ["WorkloadSpec", "WORKLOADS", "get", "Inputs", "generate", "sample_rows"]
+__all__ = ["WorkloadSpec", "WORKLOADS", "get", "Inputs", "generate", "LinearInputs", "generate_linear",
+           "sample_rows"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -61,6 +68,7 @@ class WorkloadSpec:
     group_size: int = 1        # completions per prompt (for group-normalised advantages)
     zero_adv_seqs: int = 0     # for adv == "sweep": number of sequences with A == 0
     strided: bool = False      # logits as logits[:, :-1, :] of a [B, L+1, V] tensor
+    H: int = 0                 # hidden size of the LM-head workloads (logits = h W^T)
 
     @property
     def rows(self) -> int:
@@ -91,6 +99,10 @@ WORKLOADS = {
         "grpo_qwen3_b16_l1024_v151936", B=16, L=1024, V=151936, dtype="bf16", sigma=2.0, T=1.0,
         beta=0.04, eps_low=0.2, eps_high=0.28, adv="group_bernoulli", mask="uniform_len",
         old_sigma=0.15, ref_sigma=0.05, group_size=4),
+    "linear_qwen3_b16_l1024_h1024_v151936": WorkloadSpec(
+        "linear_qwen3_b16_l1024_h1024_v151936", B=16, L=1024, V=151936, dtype="bf16", sigma=2.0, T=1.0,
+        beta=0.04, eps_low=0.2, eps_high=0.28, adv="group_bernoulli", mask="uniform_len",
+        old_sigma=0.15, ref_sigma=0.05, group_size=4, H=1024),
     "sweep_b16_l4096_v151936": WorkloadSpec(
         "sweep_b16_l4096_v151936", B=16, L=4096, V=151936, dtype="bf16", sigma=2.0, T=0.7,
         beta=0.0, eps_low=0.2, eps_high=0.2, adv="sweep", mask="none",
@@ -105,7 +117,7 @@ def get(name: str, **overrides) -> WorkloadSpec:
 
 # Independent streams per component so that changing how one tensor is drawn
 # never shifts another.
-_STREAM = {"logits": 1, "idx": 2, "old": 3, "ref": 4, "adv": 5, "mask": 6, "peak": 7}
+_STREAM = {"logits": 1, "idx": 2, "old": 3, "ref": 4, "adv": 5, "mask": 6, "peak": 7, "hidden": 8, "head": 9}
 
 
 def _gen(seed: int, what: str, device="cpu", chunk: int = 0) -> torch.Generator:
@@ -210,6 +222,26 @@ def _lengths(spec: WorkloadSpec, seed: int) -> torch.Tensor:
     raise ValueError(spec.mask)
 
 
+def _row_inputs(spec: WorkloadSpec, seed: int):
+    """Advantages, mask, per-token loss weights, old/ref offsets, upstream gradient and
+    completion lengths (host tensors)."""
+    B, L, R = spec.B, spec.L, spec.rows
+    adv = _advantages(spec, seed)
+    lengths = _lengths(spec, seed)
+    pos = torch.arange(L, dtype=torch.int64)[None, :]
+    mask_bl = (pos < lengths[:, None]).to(torch.uint8)
+    mask = None if spec.mask == "none" else mask_bl.reshape(R)
+    # per-token loss weight: mean over each completion, then mean over the batch
+    dloss = (mask_bl.double() / (B * lengths[:, None].double())).float().reshape(R)
+    old_offset = ref_offset = None
+    if spec.old_sigma is not None:
+        old_offset = (torch.randn(R, generator=_gen(seed, "old"), dtype=torch.float64) * spec.old_sigma).float()
+    if spec.ref_sigma is not None:
+        ref_offset = (torch.randn(R, generator=_gen(seed, "ref"), dtype=torch.float64) * spec.ref_sigma).float()
+    upstream = torch.full((R,), 1.0 / R, dtype=torch.float32)
+    return adv, mask, dloss, old_offset, ref_offset, upstream, lengths
+
+
 def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", rows_per_chunk: int = 4096) -> Inputs:
     """All inputs of one workload, seeded.  Large logits should be generated with
     ``device='cuda'`` (drawn on the GPU in row chunks); the small per-row arrays are
@@ -240,21 +272,7 @@ def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", rows_per_chunk: in
                 vals = logits[b, l, cd].float() + spec.peak_height
                 logits[b, l, cd] = vals.to(logits.dtype)
 
-    adv = _advantages(spec, seed)
-    lengths = _lengths(spec, seed)
-    pos = torch.arange(L, dtype=torch.int64)[None, :]
-    mask_bl = (pos < lengths[:, None]).to(torch.uint8)
-    mask = None if spec.mask == "none" else mask_bl.reshape(R)
-    # per-token loss weight: mean over each completion, then mean over the batch
-    dloss = (mask_bl.double() / (B * lengths[:, None].double())).float().reshape(R)
-
-    old_offset = ref_offset = None
-    if spec.old_sigma is not None:
-        old_offset = (torch.randn(R, generator=_gen(seed, "old"), dtype=torch.float64) * spec.old_sigma).float()
-    if spec.ref_sigma is not None:
-        ref_offset = (torch.randn(R, generator=_gen(seed, "ref"), dtype=torch.float64) * spec.ref_sigma).float()
-    upstream = torch.full((R,), 1.0 / R, dtype=torch.float32)
-
+    adv, mask, dloss, old_offset, ref_offset, upstream, lengths = _row_inputs(spec, seed)
     mv = lambda t: None if t is None else t.to(device)
     return Inputs(spec, logits, mv(idx), mv(adv), mv(mask), mv(dloss), mv(old_offset), mv(ref_offset),
                   mv(upstream), lengths)
@@ -268,3 +286,34 @@ def sample_rows(R: int, k: int, seed: int = 0) -> np.ndarray:
     rng = np.random.default_rng(seed + 12345)
     inner = rng.choice(np.arange(1, R - 1), size=max(k - 2, 0), replace=False)
     return np.unique(np.concatenate([[0, R - 1], inner]).astype(np.int64))
+
+
+@dataclasses.dataclass
+class LinearInputs:
+    spec: WorkloadSpec
+    hidden: torch.Tensor               # [B*L, H] bf16 hidden states entering the LM head
+    weight: torch.Tensor               # [V, H] bf16 LM-head weight
+    idx: torch.Tensor                  # [B*L] int64
+    adv: torch.Tensor                  # [B] fp32
+    mask: Optional[torch.Tensor]       # [B*L] uint8 or None
+    dloss: torch.Tensor                # [B*L] fp32
+    old_offset: Optional[torch.Tensor]
+    ref_offset: Optional[torch.Tensor]
+    lengths: torch.Tensor
+
+
+def generate_linear(spec: WorkloadSpec, seed: int = 0, device="cpu") -> LinearInputs:
+    """Inputs of the GRPO loss on top of the LM head: hidden states h ~ N(0, 1) and a head
+    weight W ~ N(0, (sigma / sqrt(H))^2), both bf16, drawn in fp32 with their own seeded
+    streams; the per-row inputs as in ``generate``."""
+    B, L, V, H, R = spec.B, spec.L, spec.V, spec.H, spec.rows
+    assert H > 0, "not an LM-head workload"
+    dev_type = torch.device(device).type
+    h = torch.randn((R, H), generator=_gen(seed, "hidden", dev_type), device=device, dtype=torch.float32)
+    W = torch.randn((V, H), generator=_gen(seed, "head", dev_type), device=device, dtype=torch.float32)
+    W.mul_(spec.sigma / float(np.sqrt(H)))
+    idx = torch.randint(0, V, (R,), generator=_gen(seed, "idx"), dtype=torch.int64)
+    adv, mask, dloss, old_offset, ref_offset, _, lengths = _row_inputs(spec, seed)
+    mv = lambda t: None if t is None else t.to(device)
+    return LinearInputs(spec, h.to(torch.bfloat16), W.to(torch.bfloat16), mv(idx), mv(adv), mv(mask), mv(dloss),
+                        mv(old_offset), mv(ref_offset), lengths)

@@ -197,6 +197,32 @@ def test_vocab_parallel_validation(lib):
                                                      ctypes.byref(far), None, None) == INV
 
 
+def test_fused_linear_validation(lib):
+    """Shapes, alignment and the workspace size are checked on the host before any launch."""
+    need = ctypes.c_uint64(0)
+    assert lib.grpo_fused_linear_workspace_size(1000, 16, ctypes.byref(need)) == binding.GRPO_OK
+    assert need.value >= 1000 * 16 * 6
+    assert lib.grpo_fused_linear_workspace_size(0, 16, ctypes.byref(need)) == INV
+    assert lib.grpo_fused_linear_workspace_size(1000, 0, ctypes.byref(need)) == INV
+    big = need.value
+
+    def call(H=64, V=1000, hidden=FAKE, weight=FAKE, ws=FAKE, ws_bytes=big, chunk=16, T=1.0, beta=0.0, ref=None,
+             idx=FAKE, gh=None, B=2, L=8):
+        return lib.grpo_fused_linear(hidden, weight, B, L, H, V, idx, None, ref, FAKE, None, FAKE, T, beta, 0.2, 0.2,
+                                     chunk, ws, ws_bytes, FAKE, FAKE, FAKE, None, None, None, gh, None, None, None)
+    assert call(H=60) == INV                       # H must be a multiple of 8
+    assert call(hidden=FAKE + 8) == INV             # 16-byte operands
+    assert call(weight=None) == INV
+    assert call(ws=FAKE + 128) == INV               # 256-byte workspace
+    assert call(ws_bytes=big - 1) == INV            # too small for V, chunk
+    assert call(chunk=0) == INV
+    assert call(T=0.0) == INV
+    assert call(beta=0.1) == INV                    # ref_logp required when beta > 0
+    assert call(idx=None) == INV
+    assert call(gh=FAKE + 4) == INV
+    assert call(B=0) == binding.GRPO_OK             # no rows: nothing launched
+
+
 def test_rows_of_strides():
     import torch
     base = torch.empty(4, 9, 16, dtype=torch.bfloat16)
