@@ -67,6 +67,8 @@ class L2Flush:
         self.w.fill_(i & 0x7F)
         torch.sum(self.r, dim=0, out=self.sink)
 GRPO_WORKLOADS = ("grpo_b4_l512_v32000", "grpo_qwen3_b16_l1024_v151936", "sweep_b16_l4096_v151936")
+LINEAR_WORKLOAD = "linear_qwen3_b16_l1024_h1024_v151936"
+LINEAR_METRIC = "GRPO loss on the LM head (fused linear) rows/s"
 
 
 # ---------------------------------------------------------------------------
@@ -78,6 +80,19 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def load_bf16_peak(sustained=True):
+    """The measured dense bf16 tensor peak (TFLOP/s): the sustained figure for work timed
+    inside a long loop, else the burst figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        k = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        return float(p[k]), f"measured (MEASURED_PEAKS.json {k}, cuBLAS bf16 GEMM)"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback (no MEASURED_PEAKS.json)"
 
 
 def load_peaks():
@@ -341,6 +356,144 @@ class FusedStep(GrpoStep):
                                dlogits=self.dlogits)
         self.h_dl.copy_(f["dlogits"], non_blocking=True)
         self.h_loss.copy_(f["loss"], non_blocking=True)
+
+
+class LinearStep:
+    """grpo_fused_linear over the LM-head workload: per chunk of rows, the logits GEMM,
+    the row pass, the hidden-state gradient GEMM and the head-weight gradient GEMM."""
+
+    def __init__(self, spec, seed, device, chunk_rows):
+        self.spec = spec
+        li = W.generate_linear(spec, seed, device=device)
+        self.li = li
+        self.chunk = min(chunk_rows, spec.rows)
+        R, V, H = spec.rows, spec.V, spec.H
+        f32 = dict(dtype=torch.float32, device=device)
+        self.grad_w = torch.zeros(V, H, **f32)
+        self.ws = torch.empty(rp.grpo_fused_linear_workspace_size(V, self.chunk), dtype=torch.uint8, device=device)
+        # old / ref placed near the current logp with a first pass of the same call (setup)
+        f0 = rp.grpo_fused_linear(li.hidden, li.weight, li.idx, li.adv, li.dloss, B=spec.B, L=spec.L, T=spec.T,
+                                  beta=0.0, eps_low=spec.eps_low, eps_high=spec.eps_high, mask=li.mask,
+                                  chunk_rows=self.chunk, with_grad_hidden=False, with_grad_weight=False,
+                                  workspace=self.ws)
+        self.old = (f0["logp"] + li.old_offset).contiguous()
+        self.ref = (f0["logp"] + li.ref_offset).contiguous()
+        del f0
+        self.kernels = [("grpo_fused_linear", self.call)]
+        self.launches_per_step = 4 * ((R + self.chunk - 1) // self.chunk)
+        self.flops_per_step = 6 * R * V * H
+
+    def call(self, hidden=None, idx=None, adv=None, dloss=None, mask=None, old=None, ref=None):
+        spec, li = self.spec, self.li
+        pick = lambda a, b: b if a is None else a
+        return rp.grpo_fused_linear(pick(hidden, li.hidden), li.weight, pick(idx, li.idx), pick(adv, li.adv),
+                                    pick(dloss, li.dloss), B=spec.B, L=spec.L, T=spec.T, beta=spec.beta,
+                                    eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=pick(old, self.old),
+                                    ref_logp=pick(ref, self.ref), mask=pick(mask, li.mask), chunk_rows=self.chunk,
+                                    grad_weight=self.grad_w, workspace=self.ws)
+
+    def e2e_setup(self):
+        li = self.li
+        pin = lambda t: None if t is None else t.detach().cpu().pin_memory()
+        self.h = {"hidden": pin(li.hidden), "idx": pin(li.idx), "adv": pin(li.adv), "mask": pin(li.mask),
+                  "dloss": pin(li.dloss), "old": pin(self.old), "ref": pin(self.ref)}
+        R, H = self.spec.rows, self.spec.H
+        self.h_gh = torch.empty(R, H, dtype=torch.float32).pin_memory()
+        self.h_loss = torch.empty(R, dtype=torch.float32).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h.values() if t is not None)
+        self.d2h = self.h_gh.numel() * 4 + self.h_loss.numel() * 4
+
+    def e2e_step(self):
+        dev = self.li.hidden.device
+        up = {k: None if t is None else t.to(dev, non_blocking=True) for k, t in self.h.items()}
+        out = self.call(**up)
+        self.h_gh.copy_(out["grad_hidden"], non_blocking=True)
+        self.h_loss.copy_(out["loss"], non_blocking=True)
+
+
+def run_linear(args):
+    """Bench line of the LM-head workload: rows/s and the tensor-core roofline of the step
+    (6 R V H flops: the logits GEMM and the two gradient GEMMs)."""
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    spec = W.get(LINEAR_WORKLOAD)
+    step = LinearStep(spec, args.seed + rank, device, args.chunk_rows)
+    flush_buf = L2Flush(device)
+    step.call()
+    torch.cuda.synchronize()
+    K = args.steps if args.steps is not None else 20
+    Wm = max(3, args.warmup)
+    clocks = ClockSampler(local)
+    clocks.start()
+    steps, wall = timed_run(step, K, Wm, flush_buf, world, per_kernel=False)
+    clk = clocks.stop()
+    step_ms = statistics.mean(steps["step"])
+    total_ms = aggregate_max_ms(sum(steps["step"]), world, device)
+    rows_per_s = spec.rows * K * world / (total_ms * 1e-3)
+    peak, peak_src = load_bf16_peak(sustained=True)
+    tflops = step.flops_per_step / (step_ms * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        ms = e2e_run(step, min(K, 10), 2)
+        e2e = {"value": round(spec.rows * world / (ms * 1e-3), 1), "unit": "rows/s", "h2d_bytes_per_step": int(step.h2d),
+               "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4),
+               "path": "public Python API, pinned host hidden states and per-row inputs, loss and grad_hidden "
+                       "copied back; the head weight and its gradient stay on the device"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = linear_cpu_baseline(step)
+    if rank == 0:
+        full_logits = spec.rows * spec.V * 2
+        line = {"metric": LINEAR_METRIC, "unit": "rows/s", "n_gpus": world, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+                "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "H": spec.H, "V": spec.V, "T": spec.T,
+                           "beta": spec.beta, "eps_low": spec.eps_low, "eps_high": spec.eps_high,
+                           "chunk_rows": step.chunk, "operands": "bf16 hidden and head weight; fp32 logits per chunk",
+                           "l2": "flushed before every timed step (256 MB write + 256 MB read, not timed)",
+                           "parallelism": f"{world} independent batch(es), one per GPU"},
+                "value": round(rows_per_s, 1), "steps": K, "warmup": Wm, "ms_per_step": round(step_ms, 4),
+                "dtype": "bf16", "rows_per_s": round(rows_per_s, 1),
+                "roofline": {"bound": "tensor", "kernel": "grpo_fused_linear (3 GEMMs + row pass per chunk)",
+                             "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tflops / peak, 4), "traffic": None, "peak_source": peak_src,
+                             "flops_per_step": int(step.flops_per_step)},
+                "memory": {"workspace_bytes": int(step.ws.numel()), "full_batch_logits_bytes_bf16": int(full_logits),
+                           "full_batch_logits_and_dlogits_bytes_bf16": int(2 * full_logits)},
+                "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": step.launches_per_step * K,
+                "gpu_launches_note": "per chunk: 3 cuBLASLt GEMMs (library kernels) and 1 row-pass kernel",
+                "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                           "samples": clk["samples"]},
+                "timed_wall_s": round(wall, 3), "kernel_source": kernel_source_hash()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def linear_cpu_baseline(step, budget_s=12.0):
+    """The oracle's fused_linear_grpo on a bounded sample of rows (the whole head weight)."""
+    import oracle
+    spec, li = step.spec, step.li
+    Wf = oracle.bf16_bits_to_fp64(li.weight.cpu().view(torch.int16).numpy().view(np.uint16))
+    def run(n):
+        rows = W.sample_rows(spec.rows, n, 13)
+        r = torch.as_tensor(rows, device=li.hidden.device)
+        hf = oracle.bf16_bits_to_fp64(li.hidden[r].cpu().view(torch.int16).numpy().view(np.uint16))
+        g = lambda t: None if t is None else t[r].double().cpu().numpy()
+        adv = oracle.per_row(li.adv.cpu().numpy(), spec.L)[rows]
+        t0 = time.perf_counter()
+        oracle.fused_linear_grpo(hf, Wf, li.idx[r].cpu().numpy(), g(step.old), g(step.ref), adv, g(li.mask),
+                                 g(li.dloss), spec.T, spec.beta, spec.eps_low, spec.eps_high)
+        return len(rows), time.perf_counter() - t0
+    n, dt = run(4)
+    n = int(max(4, min(512, budget_s / max(dt / n, 1e-9))))
+    n, dt = run(n)
+    return {"value": round(n / dt, 3), "unit": "rows/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{n} of {spec.rows} rows of {spec.name} (fp64 numpy, the full head weight), {dt:.1f} s"}
 
 
 def vocab_shard_starts(V, shards):
@@ -662,7 +815,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="grpo_b4_l512_v32000",
-                    choices=list(GRPO_WORKLOADS) + ["entropy_slsm_b16_l4096_v32000"])
+                    choices=list(GRPO_WORKLOADS) + ["entropy_slsm_b16_l4096_v32000", LINEAR_WORKLOAD])
+    ap.add_argument("--chunk-rows", type=int, default=1024,
+                    help="rows per chunk of the LM-head workload (grpo_fused_linear)")
     ap.add_argument("--beta", type=float, default=None)
     ap.add_argument("--zero-seqs", type=int, default=None)
     ap.add_argument("--strided", action="store_true")
@@ -694,6 +849,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle  # the one other place bench.py runs the oracle
+    if args.workload == LINEAR_WORKLOAD:
+        return run_reference_linear(args, oracle)
     spec = make_spec(args)
     inp = W.generate(spec, args.seed, device="cpu")
     R, L = spec.rows, spec.L
@@ -759,10 +916,54 @@ def run_reference(args):
     return 0
 
 
+def run_reference_linear(args, oracle):
+    """The oracle's fused_linear_grpo as the reference arm of the LM-head workload: each
+    step a bounded sample of rows against the whole head weight, on the host."""
+    spec = W.get(LINEAR_WORKLOAD)
+    li = W.generate_linear(spec, args.seed, device="cpu")
+    Wf = oracle.bf16_bits_to_fp64(li.weight.view(torch.int16).numpy().view(np.uint16))
+    adv_rows = oracle.per_row(li.adv.numpy(), spec.L)
+
+    def step(rows):
+        hf = oracle.bf16_bits_to_fp64(li.hidden[rows].view(torch.int16).numpy().view(np.uint16))
+        lp, _ = oracle.selective_log_softmax(hf @ Wf.T, li.idx.numpy()[rows], spec.T)
+        old = oracle.round_to_fp32(lp + li.old_offset.numpy()[rows]).astype(np.float64)
+        ref = oracle.round_to_fp32(lp + li.ref_offset.numpy()[rows]).astype(np.float64)
+        mask = None if li.mask is None else li.mask.numpy()[rows]
+        t = time.perf_counter()
+        oracle.fused_linear_grpo(hf, Wf, li.idx.numpy()[rows], old, ref, adv_rows[rows], mask,
+                                 li.dloss.numpy().astype(np.float64)[rows], spec.T, spec.beta, spec.eps_low,
+                                 spec.eps_high)
+        return time.perf_counter() - t
+
+    K = args.steps if args.steps is not None else 10
+    Wm = args.warmup
+    per_row = step(W.sample_rows(spec.rows, 4, 3)) / 4
+    n = int(max(1, min(spec.rows, 150.0 / max(1, K + Wm) / max(per_row, 1e-9))))
+    times = [step(W.sample_rows(spec.rows, n, 100 + i)) for i in range(Wm + K)][Wm:]
+    total = sum(times)
+    value = n * K / total
+    line = {"metric": LINEAR_METRIC, "unit": "rows/s", "n_gpus": 1, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "data": "synthetic", "impl": "reference",
+            "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "H": spec.H, "V": spec.V},
+            "value": round(value, 4), "steps": K, "warmup": Wm, "ms_per_step": round(1e3 * total / K, 3),
+            "dtype": "f64", "rows_per_s": round(value, 4)}
+    line["cpu_baseline"] = {"value": line["value"], "unit": "rows/s", "cores": torch.get_num_threads(),
+                            "kind": "oracle",
+                            "sample": f"{n} of {spec.rows} rows per step (fp64 numpy, the full head weight)"}
+    line["e2e"] = {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == LINEAR_WORKLOAD:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU: the row pass has no CPU path")
+        return run_linear(args)
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU: the row pass has no CPU path")
