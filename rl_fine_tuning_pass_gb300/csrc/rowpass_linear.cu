@@ -35,7 +35,7 @@ __device__ __forceinline__ float linear_sweep2(const float* row, uint16_t* out, 
   float2 q2 = make_float2(0.f, 0.f);
   const int groups = V / 8;  // 8 logits (two 16-byte fp32 vectors) -> one 16-byte bf16 vector
   for (int i = tid; i < groups; i += THREADS) {
-    const uint4 a = ld_v4(vb + 2 * i), b = ld_v4(vb + 2 * i + 1);
+    const uint4 a = ld_v4_evict_first(vb + 2 * i), b = ld_v4_evict_first(vb + 2 * i + 1);
     float2 e[4];
     const float2 x[4] = {make_float2(__uint_as_float(a.x), __uint_as_float(a.y)),
                          make_float2(__uint_as_float(a.z), __uint_as_float(a.w)),
@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
 
-  // sweep 1: the online statistic of the fp32 row (16-byte aligned: ld % 8 == 0)
+  // sweep 1: the online statistic of the fp32 row (16-byte aligned: ld % 8 == 0).  The row
+  // is kept in L2 (evict_last) for sweep 2, which lets it go (evict_first); one CTA of 1024
+  // threads per SM keeps some 150 rows in flight, few enough for L2 to hold them.
   Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const uint4* vb = reinterpret_cast<const uint4*>(row);
   const int nvec = V / 4;
@@ -110,12 +112,12 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   for (; i + (UNROLL - 1) * THREADS < nvec; i += UNROLL * THREADS) {
     uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = ld_v4(vb + i + k * THREADS);
+    for (int k = 0; k < UNROLL; ++k) v[k] = ld_v4_evict_last(vb + i + k * THREADS);
     run_vectors<F32, kH>(rs, v, c);
   }
   for (; i < nvec; i += THREADS) {
     uint4 v[1];
-    v[0] = ld_v4(vb + i);
+    v[0] = ld_v4_evict_last(vb + i);
     run_vectors<F32, kH>(rs, v, c);
   }
   const float x_idx = tid == 0 ? row[idx] : 0.f;
@@ -137,10 +139,12 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   const float g = sh_g;
   if (g == 0.f) {  // early-out: +0.0 over the row
     fill_bf16_row(out, V, 0u, THREADS);
+    l2_demote<THREADS>(row, static_cast<int64_t>(V) * 4);
     return;
   }
   if (bad_idx) {
     fill_bf16_row(out, V, BF16::kNaNPair, THREADS);
+    l2_demote<THREADS>(row, static_cast<int64_t>(V) * 4);
     return;
   }
   // sweep 2: d_j = -sign(g) |g| p_j in bf16, and g (1 - p_idx) at idx
@@ -260,8 +264,8 @@ cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream)
     LinearChunkParams lp = q.chunk_params;
     lp.row0 = r0;
     const dim3 grid(static_cast<unsigned>(c));
-    e = lp.f.entropy ? launch_after_previous(linear_chunk_kernel<256, kUnroll, true>, grid, dim3(256), stream, lp)
-                     : launch_after_previous(linear_chunk_kernel<256, kUnroll, false>, grid, dim3(256), stream, lp);
+    e = lp.f.entropy ? launch_after_previous(linear_chunk_kernel<1024, kUnroll, true>, grid, dim3(1024), stream, lp)
+                     : launch_after_previous(linear_chunk_kernel<1024, kUnroll, false>, grid, dim3(1024), stream, lp);
     if (e != cudaSuccess) return e;
     if (q.grad_hidden != nullptr) {
       // grad_h^T [H, c] = W^T-as-[H, V] x dlogits^T [V, c]
