@@ -398,6 +398,36 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
                               float* loss, float* logp, float* lse, float* kl, uint8_t* is_clipped, float* entropy,
                               float* grad_hidden, float* grad_weight, int32_t* dev_err, grpo_stream_t stream);
 
+/*
+ * grpo_fused_linear_noalloc -- grpo_fused_linear without a workspace argument: it allocates
+ * no device memory, for callers that cannot call cudaMalloc at the point where the loss
+ * runs (a runtime without a device allocator, a process whose device memory is all
+ * handed to a pool it does not control, or a step that must not stall on an allocation).
+ * The pages have no counterpart; this is a convenience of this library.
+ *
+ * Its scratch (one chunk's fp32 logits and bf16 dlogits, and a 4 MiB workspace for the
+ * GEMMs) is a fixed 32 MiB device array inside the library, which every device context that
+ * loads the library holds until the process exits.  Limit: chunk_rows * 6 * V8 bytes, each
+ * of the two chunk buffers rounded up to 256 bytes, plus 4 MiB must fit in 32 MiB
+ * (V8 = V rounded up to a multiple of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before
+ * any launch.  For V = 151936 that is at most 32 rows per chunk.
+ *
+ * The first call on a device does the set-up: it looks up the array's device address and,
+ * like every GEMM path of this library, creates the library's cuBLASLt handle for that
+ * device.  Make that first call before any stream capture.  Every call uses the whole
+ * array, so calls that overlap on the GPU race on it: run them on one stream, or one after
+ * the other.  The array keeps the last call's contents; nothing in it has to start at zero.
+ *
+ * Arguments: those of grpo_fused_linear without workspace / workspace_bytes; the results
+ * equal grpo_fused_linear's to within the GEMMs' fp32 summation order.
+ */
+grpo_status grpo_fused_linear_noalloc(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H,
+                                      int64_t V, const int64_t* idx, const float* old_logp, const float* ref_logp,
+                                      const float* adv, const uint8_t* mask, const float* dloss, float T, float beta,
+                                      float eps_low, float eps_high, int64_t chunk_rows, float* loss, float* logp,
+                                      float* lse, float* kl, uint8_t* is_clipped, float* entropy, float* grad_hidden,
+                                      float* grad_weight, int32_t* dev_err, grpo_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* grpo_status_string(grpo_status status);
 

@@ -25,7 +25,7 @@ EXPORTED = ("grpo_loss_fwd", "grpo_loss_bwd", "grpo_loss_fused", "entropy_from_l
             "entropy_from_logits_bwd", "selective_log_softmax_fwd", "selective_log_softmax_bwd",
             "grpo_seq_terms", "grpo_vocab_shard_stats", "grpo_vocab_combine", "grpo_loss_bwd_vocab_shard",
             "selective_log_softmax_bwd_vocab_shard", "grpo_fused_linear_workspace_size", "grpo_fused_linear",
-            "grpo_status_string")
+            "grpo_fused_linear_noalloc", "grpo_status_string")
 GRPO_VOCAB_MAX_WORLD = 64
 
 
@@ -78,6 +78,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "grpo_fused_linear": [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P,
                               _P, _P, _F, _F, _F, _F, ctypes.c_int64, _P, ctypes.c_uint64, _P, _P, _P, _P, _P, _P,
                               _P, _P, _P, _P],
+        "grpo_fused_linear_noalloc": [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P,
+                                      _P, _P, _P, _P, _F, _F, _F, _F, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

@@ -12,11 +12,13 @@
 // is g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
 #include <cublasLt.h>
 
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
 
+#include "grpo_rowpass.h"
 #include "rowpass_bwd.cuh"
 #include "rowpass_fwd.cuh"
 
@@ -284,3 +286,222 @@ cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream)
 }
 
 }  // namespace grpo
+
+// ---------------------------------------------------------------------------
+// grpo_fused_linear_noalloc: the same computation with its scratch in a fixed device array
+// ---------------------------------------------------------------------------
+//
+// For callers that must not allocate device memory at call time (an allocator-free
+// runtime, a host process that has handed all device memory to a pool it does not own, a
+// code path that must not synchronise on an allocation).  The scratch grpo_fused_linear
+// takes from the caller (one chunk's fp32 logits and bf16 dlogits, and the GEMMs'
+// workspace) lives here in one array of kNoallocScratchBytes, reserved in every device
+// context that loads this library and held until the process exits.  Every call uses the
+// whole array: calls that run at the same time on the GPU (different streams, threads or
+// host processes sharing the context) race on it.  Nothing in it has to start at zero: each
+// call writes every part before reading it.
+
+namespace grpo {
+namespace {
+
+constexpr uint64_t kNoallocScratchBytes = uint64_t(32) << 20;  // 32 MiB per device
+constexpr uint64_t kNoallocGemmWs = uint64_t(4) << 20;         // of which the GEMMs' workspace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// The array's device address, looked up once per device with that device current.
+void* noalloc_scratch_address() {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+// lt_gemm with its descriptors in caller-provided (stack) storage and the chosen
+// algorithms in a fixed table, so that a call allocates nothing, on the host either.
+cudaError_t lt_gemm_noalloc(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
+                            const void* B, int64_t ldb, void* D, int64_t ldd, float beta, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  cublasLtHandle_t h = lt_handle();
+  if (h == nullptr) return cudaErrorNotSupported;
+  cublasLtMatmulDescOpaque_t op_s;
+  cublasLtMatrixLayoutOpaque_t la_s, lb_s, ld_s;
+  cublasLtMatmulDesc_t op = &op_s;
+  cublasLtMatrixLayout_t la = &la_s, lb = &lb_s, ldl = &ld_s;
+  const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
+  if (cublasLtMatmulDescInit(op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatrixLayoutInit(la, CUDA_R_16BF, ta ? k : m, ta ? m : k, lda) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatrixLayoutInit(lb, CUDA_R_16BF, tb ? n : k, tb ? k : n, ldb) != CUBLAS_STATUS_SUCCESS ||
+      cublasLtMatrixLayoutInit(ldl, CUDA_R_32F, m, n, ldd) != CUBLAS_STATUS_SUCCESS)
+    return cudaErrorNotSupported;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const GemmKey key{dev, ta, tb, static_cast<int>(CUDA_R_32F), m, n, k, lda, ldb, ldd, ws_bytes};
+  struct Entry {
+    GemmKey key;
+    cublasLtMatmulAlgo_t algo;
+    bool used;
+  };
+  static Entry table[64];
+  static int next = 0;
+  static std::mutex mu;
+  cublasLtMatmulAlgo_t algo;
+  bool have = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : table)
+      if (e.used && !(e.key < key) && !(key < e.key)) {
+        algo = e.algo;
+        have = true;
+        break;
+      }
+  }
+  if (!have) {
+    cublasLtMatmulPreferenceOpaque_t pref_s;
+    cublasLtMatmulPreference_t pref = &pref_s;
+    if (cublasLtMatmulPreferenceInit(pref) != CUBLAS_STATUS_SUCCESS) return cudaErrorNotSupported;
+    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
+                                         sizeof(ws_bytes));
+    cublasLtMatmulHeuristicResult_t res;
+    int found = 0;
+    if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ldl, ldl, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS ||
+        found < 1)
+      return cudaErrorNotSupported;
+    algo = res.algo;
+    std::lock_guard<std::mutex> lock(mu);
+    table[next] = Entry{key, algo, true};  // a fixed table: the oldest entry makes room
+    next = (next + 1) % 64;
+  }
+  const float alpha = 1.f;
+  return cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, D, ldl, D, ldl, &algo, ws, ws_bytes, stream) ==
+                 CUBLAS_STATUS_SUCCESS
+             ? cudaSuccess
+             : cudaErrorLaunchFailure;
+}
+
+cudaError_t launch_fused_linear_noalloc(const FusedLinearParams& q, cudaStream_t stream) {
+  const int64_t R = q.rows, H = q.H, V = q.V, ld = q.ld;
+  for (int64_t r0 = 0; r0 < R; r0 += q.chunk) {
+    const int64_t c = R - r0 < q.chunk ? R - r0 : q.chunk;
+    const uint16_t* h = q.hidden + r0 * H;
+    cudaError_t e = lt_gemm_noalloc(true, false, V, c, H, q.weight, H, h, H, q.logits, ld, 0.f, q.ws, q.ws_bytes,
+                                    stream);
+    if (e != cudaSuccess) return e;
+    LinearChunkParams lp = q.chunk_params;
+    lp.row0 = r0;
+    const dim3 grid(static_cast<unsigned>(c));
+    e = lp.f.entropy ? launch_after_previous(linear_chunk_kernel<1024, kUnroll, true>, grid, dim3(1024), stream, lp)
+                     : launch_after_previous(linear_chunk_kernel<1024, kUnroll, false>, grid, dim3(1024), stream, lp);
+    if (e != cudaSuccess) return e;
+    if (q.grad_hidden != nullptr) {
+      e = lt_gemm_noalloc(false, false, H, c, V, q.weight, H, q.dlogits, ld, q.grad_hidden + r0 * H, H, 0.f, q.ws,
+                          q.ws_bytes, stream);
+      if (e != cudaSuccess) return e;
+    }
+    if (q.grad_weight != nullptr) {
+      e = lt_gemm_noalloc(false, true, H, V, c, h, H, q.dlogits, ld, q.grad_weight, H, 1.f, q.ws, q.ws_bytes,
+                          stream);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+bool noalloc_f32(const void* p, bool required) {
+  return p == nullptr ? !required : (reinterpret_cast<uintptr_t>(p) % 4) == 0;
+}
+
+}  // namespace
+}  // namespace grpo
+
+extern "C" grpo_status grpo_fused_linear_noalloc(
+    const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H, int64_t V, const int64_t* idx,
+    const float* old_logp, const float* ref_logp, const float* adv, const uint8_t* mask, const float* dloss, float T,
+    float beta, float eps_low, float eps_high, int64_t chunk_rows, float* loss, float* logp, float* lse, float* kl,
+    uint8_t* is_clipped, float* entropy, float* grad_hidden, float* grad_weight, int32_t* dev_err,
+    grpo_stream_t stream) {
+  using grpo::noalloc_f32;
+  // the arguments, checked as grpo_fused_linear checks them, before any CUDA call
+  if (!(std::isfinite(T) && T > 0.f) || !std::isfinite(beta) || beta < 0.f || !std::isfinite(eps_low) ||
+      eps_low < 0.f || eps_low > 1.f || !std::isfinite(eps_high) || eps_high < 0.f)
+    return GRPO_ERR_INVALID_ARG;
+  if (B < 0 || L < 0 || H < 8 || H % 8 != 0 || V < 1 || chunk_rows < 1) return GRPO_ERR_INVALID_ARG;
+  if (V > (int64_t(1) << 30) || static_cast<long double>(B) * L > ((int64_t(1) << 31) - 1) || H > (int64_t(1) << 24))
+    return GRPO_ERR_UNSUPPORTED;
+  const int64_t rows = B * L;
+  if (rows == 0) return GRPO_OK;
+  const int64_t ld = (V + 7) / 8 * 8;
+  const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
+  const uint64_t logits_bytes = (static_cast<uint64_t>(ld) * chunk * 4 + 255) & ~uint64_t(255);
+  const uint64_t dlogits_bytes = (static_cast<uint64_t>(ld) * chunk * 2 + 255) & ~uint64_t(255);
+  // the fixed array's limit: chunk * 6 * ld bytes (rounded to 256) + the GEMMs' 4 MiB <= 32 MiB
+  if (logits_bytes + dlogits_bytes + grpo::kNoallocGemmWs > grpo::kNoallocScratchBytes) return GRPO_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
+  if (!a16(hidden) || !a16(weight)) return GRPO_ERR_INVALID_ARG;
+  if (idx == nullptr || (reinterpret_cast<uintptr_t>(idx) % 8) != 0 || !noalloc_f32(old_logp, false) ||
+      !noalloc_f32(adv, true) || !noalloc_f32(dloss, true) || !noalloc_f32(loss, true) || !noalloc_f32(logp, true) ||
+      !noalloc_f32(lse, true) || !noalloc_f32(kl, false) || !noalloc_f32(entropy, false) ||
+      !noalloc_f32(dev_err, false))
+    return GRPO_ERR_INVALID_ARG;
+  if ((grad_hidden != nullptr && !a16(grad_hidden)) || (grad_weight != nullptr && !a16(grad_weight)))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && !noalloc_f32(ref_logp, true)) return GRPO_ERR_INVALID_ARG;
+  if (!noalloc_f32(ref_logp, false)) return GRPO_ERR_INVALID_ARG;
+
+  // set-up on this device's first call: the array's address (and the library's cuBLASLt
+  // handle for the device, created on first use by every GEMM path of this library)
+  char* scratch = static_cast<char*>(grpo::noalloc_scratch_address());
+  if (scratch == nullptr) return GRPO_ERR_CUDA;
+
+  grpo::FusedLinearParams q{};
+  q.hidden = static_cast<const uint16_t*>(hidden);
+  q.weight = static_cast<const uint16_t*>(weight);
+  q.rows = rows;
+  q.H = H;
+  q.V = V;
+  q.chunk = chunk;
+  q.ld = ld;
+  q.logits = reinterpret_cast<float*>(scratch);
+  q.dlogits = reinterpret_cast<uint16_t*>(scratch + logits_bytes);
+  q.ws = scratch + logits_bytes + dlogits_bytes;
+  q.ws_bytes = grpo::kNoallocGemmWs;
+  q.grad_hidden = grad_hidden;
+  q.grad_weight = grad_weight;
+  grpo::LinearChunkParams& cp = q.chunk_params;
+  grpo::FwdParams& p = cp.f;
+  p.x = grpo::RowsView{nullptr, L, 0, 0, static_cast<int>(V)};
+  p.idx = idx;
+  p.old_logp = old_logp;
+  p.ref_logp = ref_logp;
+  p.adv = adv;
+  p.mask = mask;
+  p.c = static_cast<float>(1.4426950408889634074 / static_cast<double>(T));
+  p.invT = static_cast<float>(1.0 / static_cast<double>(T));
+  p.beta = beta;
+  p.lo = static_cast<float>(1.0 - static_cast<double>(eps_low));
+  p.hi = static_cast<float>(1.0 + static_cast<double>(eps_high));
+  p.loss = loss;
+  p.logp = logp;
+  p.lse = lse;
+  p.kl = kl;
+  p.is_clipped = is_clipped;
+  p.entropy = entropy;
+  p.dev_err = dev_err;
+  cp.logits = q.logits;
+  cp.dlogits = q.dlogits;
+  cp.ld = ld;
+  cp.dloss = dloss;
+  cp.T = T;
+  return grpo::launch_fused_linear_noalloc(q, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GRPO_OK
+             : GRPO_ERR_CUDA;
+}
