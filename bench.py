@@ -663,6 +663,8 @@ def make_spec(args):
         over["zero_adv_seqs"] = args.zero_seqs
     if args.strided:
         over["strided"] = True
+    if args.batch is not None:
+        over["B"] = args.batch
     return W.get(args.workload, **over)
 
 
@@ -822,6 +824,8 @@ def parse_args(argv=None):
     ap.add_argument("--beta", type=float, default=None)
     ap.add_argument("--zero-seqs", type=int, default=None)
     ap.add_argument("--strided", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences B instead of the workload's own (a smaller case of the same rows, e.g. for ncu)")
     ap.add_argument("--fused", action="store_true",
                     help="GRPO workloads: time grpo_loss_fused (one kernel) instead of grpo_loss_fwd + grpo_loss_bwd")
     ap.add_argument("--vocab-shards", type=int, default=0,
