@@ -6,9 +6,15 @@ One step = one pass of the whole hot path over one batch of synthetic logits:
 * GRPO workloads (default ``grpo_b4_l512_v32000``, the GRPO backward workload of the
   Liger-Kernel GRPO Loss Backward write-up: (B, L, V, zero-grad%) = (4, 512, 32000, 50%)):
   ``grpo_loss_fwd`` (loss, logp, lse, kl, is_clipped, entropy) then ``grpo_loss_bwd``;
-  with ``--fused``, the single kernel ``grpo_loss_fused`` (dloss known in advance).
+  with ``--fused``, the single kernel ``grpo_loss_fused`` (dloss known in advance); with
+  ``--seq-level``, the sequence-level form (``selective_log_softmax_fwd``,
+  ``grpo_seq_terms``, ``selective_log_softmax_bwd``); with ``--vocab-shards S``, the
+  vocabulary-parallel form with its S shards run one after another.
 * ``entropy_slsm_b16_l4096_v32000``: ``entropy_from_logits``, ``selective_log_softmax_fwd``
-  and ``selective_log_softmax_bwd``.
+  and ``selective_log_softmax_bwd``; with ``--entropy-bwd``, ``entropy_from_logits`` (with
+  lse) and ``entropy_from_logits_bwd``.
+* ``linear_qwen3_b16_l1024_h1024_v151936``: ``grpo_fused_linear`` on hidden states and a
+  Qwen3-0.6B-shaped LM head (rows/s and tensor TFLOP/s).
 
 The metric is algorithmic HBM bytes per second (the minimal bytes of the step: each
 unmasked row's logits read once by the forward; each backward row with a non-zero
@@ -227,6 +233,8 @@ SLSM_ROW_BYTES = {"entropy_from_logits": lambda V, s: V * s + 4,
 
 class GrpoStep:
     """grpo_loss_fwd (+entropy, kl, is_clipped) then grpo_loss_bwd over one batch."""
+
+    oracle_kind = "grpo"
 
     def __init__(self, spec, seed, device, inputs=None):
         self.spec = spec
@@ -598,6 +606,8 @@ class VocabShardStep(GrpoStep):
 class EntropySlsmStep:
     """entropy_from_logits, selective_log_softmax_fwd, selective_log_softmax_bwd."""
 
+    oracle_kind = "slsm"
+
     def __init__(self, spec, seed, device):
         self.spec = spec
         lib = rp.load_library()
@@ -655,6 +665,121 @@ class EntropySlsmStep:
         self.h_out[2 * R:].copy_(lse, non_blocking=True)
 
 
+
+class SeqStep(GrpoStep):
+    """Sequence-level GRPO: selective_log_softmax_fwd (logp, lse), grpo_seq_terms (the
+    per-sequence ratio, clip and KL terms and the per-token dlogp), then
+    selective_log_softmax_bwd (dlogits; rows whose dlogp is 0 are written without a read)."""
+
+    oracle_kind = "seq"
+
+    def __init__(self, spec, seed, device, inputs=None):
+        super().__init__(spec, seed, device, inputs)
+        lib = rp.load_library()
+        inp, o, R, B = self.inp, self.out, spec.rows, spec.B
+        f32 = dict(dtype=torch.float32, device=device)
+        self.dlogp = torch.empty(R, **f32)
+        self.seq_ratio = torch.empty(B, **f32)
+        self.seq_clip = torch.empty(B, dtype=torch.uint8, device=device)
+        T = spec.T
+        self._sf, self._sq, self._sb = (lib.selective_log_softmax_fwd, lib.grpo_seq_terms,
+                                        lib.selective_log_softmax_bwd)
+        self.sf_args = (ctypes.byref(self.x_desc), _p(inp.idx), T, _p(o["logp"]), _p(o["lse"]), None, self.stream)
+        self.sq_args = (B, spec.L, _p(o["logp"]), _p(self.old), _p(self.ref), _p(inp.adv), _p(inp.mask),
+                        _p(inp.dloss), spec.beta, spec.eps_low, spec.eps_high, _p(o["loss"]), _p(o["kl"]),
+                        _p(self.dlogp), _p(self.seq_ratio), _p(self.seq_clip), self.stream)
+        self.sb_args = (ctypes.byref(self.x_desc), _p(inp.idx), _p(self.dlogp), _p(o["lse"]), T,
+                        ctypes.byref(self.dx_desc), None, self.stream)
+        self.kernels = [("selective_log_softmax_fwd", lambda: self._call(self._sf, self.sf_args)),
+                        ("grpo_seq_terms", lambda: self._call(self._sq, self.sq_args)),
+                        ("selective_log_softmax_bwd", lambda: self._call(self._sb, self.sb_args))]
+
+    @staticmethod
+    def _call(fn, args):
+        st = fn(*args)
+        if st:
+            raise rp.GrpoError(fn.__name__, st)
+
+    def account(self):
+        """Minimal bytes.  Forward: every row reads its V logits and idx, writes logp and
+        lse.  Sequence terms: every row reads its mask byte and writes loss, kl, dlogp; an
+        unmasked row reads logp, old, ref, dloss; every sequence reads A and writes its
+        ratio and clip flag.  Backward: every row reads dlogp and writes V dlogits; a row
+        whose dlogp is non-zero also reads idx, lse and its V logits."""
+        spec, inp = self.spec, self.inp
+        R, V, s = spec.rows, spec.V, spec.elem_size
+        live = np.ones(R, bool) if inp.mask is None else inp.mask.bool().cpu().numpy()
+        zero = (self.dlogp == 0).cpu().numpy()
+        m = 1 if inp.mask is not None else 0
+        o = 4 if self.old is not None else 0
+        r = 4 if self.ref is not None else 0
+        n_live, n_zero = int(live.sum()), int(zero.sum())
+        self.classes = {"rows": R, "masked": R - n_live, "zero_grad_rows": n_zero,
+                        "zero_grad_frac": round(n_zero / R, 4), "seq_level": True,
+                        "seq_clipped": int(self.seq_clip.sum())}
+        return {"selective_log_softmax_fwd": R * (V * s + 16),
+                "grpo_seq_terms": R * (m + 12) + n_live * (8 + o + r) + spec.B * 9,
+                "selective_log_softmax_bwd": R * (4 + V * s) + (R - n_zero) * (12 + V * s)}
+
+    def e2e_step(self):
+        spec, dev = self.spec, self.d_logits.device
+        h = self.h
+        up = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        self.d_logits.copy_(h["logits"], non_blocking=True)
+        idx, adv, mask, dloss, old, ref = up(h["idx"]), up(h["adv"]), up(h["mask"]), up(h["dloss"]), up(h["old"]), up(h["ref"])
+        lp, lse = rp.selective_log_softmax_fwd(self.d_logits, idx, T=spec.T)
+        t = rp.grpo_seq_terms(lp, adv, dloss, B=spec.B, L=spec.L, beta=spec.beta, eps_low=spec.eps_low,
+                              eps_high=spec.eps_high, old_logp=old, ref_logp=ref, mask=mask)
+        dl = rp.selective_log_softmax_bwd(self.d_logits, idx, t["dlogp"], lse, T=spec.T, dlogits=self.dlogits)
+        self.h_dl.copy_(dl, non_blocking=True)
+        self.h_loss.copy_(t["loss"], non_blocking=True)
+
+
+class EntropyBwdStep(EntropySlsmStep):
+    """entropy_from_logits (entropy and lse) then entropy_from_logits_bwd, the gradient of
+    sum_r u_r H_r with the workload's upstream gradient u."""
+
+    oracle_kind = "entropy_bwd"
+
+    def __init__(self, spec, seed, device):
+        super().__init__(spec, seed, device)
+        lib = rp.load_library()
+        inp, T = self.inp, spec.T
+        self._eb = lib.entropy_from_logits_bwd
+        self.e_args = (ctypes.byref(self.x_desc), T, _p(self.H), _p(self.lse), self.stream)
+        self.eb_args = (ctypes.byref(self.x_desc), _p(inp.upstream), _p(self.lse), _p(self.H), T,
+                        ctypes.byref(self.dx_desc), self.stream)
+        self.kernels = [("entropy_from_logits", lambda: self._call(self._e, self.e_args)),
+                        ("entropy_from_logits_bwd", lambda: self._call(self._eb, self.eb_args))]
+
+    def account(self):
+        """Minimal bytes.  Forward: every row reads its V logits, writes entropy and lse.
+        Backward: every row reads u and writes V dlogits; a row with u != 0 also reads
+        lse, entropy and its V logits."""
+        spec, inp = self.spec, self.inp
+        R, V, s = spec.rows, spec.V, spec.elem_size
+        n_zero = int((inp.upstream == 0).sum())
+        self.classes = {"rows": R, "zero_grad_rows": n_zero, "strided": spec.strided, "entropy_bwd": True}
+        return {"entropy_from_logits": R * (V * s + 8),
+                "entropy_from_logits_bwd": R * (4 + V * s) + (R - n_zero) * (8 + V * s)}
+
+    def e2e_setup(self):
+        super().e2e_setup()
+        self.h.pop("idx")
+        self.h_out = torch.empty(self.spec.rows, dtype=torch.float32).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h.values())
+        self.d2h = self.h_dl.numel() * self.h_dl.element_size() + self.h_out.numel() * 4
+
+    def e2e_step(self):
+        dev, T = self.d_logits.device, self.spec.T
+        self.d_logits.copy_(self.h["logits"], non_blocking=True)
+        up = self.h["up"].to(dev, non_blocking=True)
+        H, lse = rp.entropy_from_logits(self.d_logits, T=T, return_lse=True)
+        dl = rp.entropy_from_logits_bwd(self.d_logits, up, lse, H, T=T, dlogits=self.dlogits)
+        self.h_dl.copy_(dl, non_blocking=True)
+        self.h_out.copy_(H, non_blocking=True)
+
+
 def make_spec(args):
     over = {}
     if args.beta is not None:
@@ -668,11 +793,20 @@ def make_spec(args):
     return W.get(args.workload, **over)
 
 
-def make_step(spec, seed, device, fused=False, vocab_shards=0):
+def step_kind(args, spec):
+    """Which pass a bench run times: "grpo", "slsm", "seq" or "entropy_bwd"."""
     if spec.name.startswith("entropy_slsm"):
-        return EntropySlsmStep(spec, seed, device)
+        return "entropy_bwd" if args.entropy_bwd else "slsm"
+    return "seq" if args.seq_level else "grpo"
+
+
+def make_step(spec, seed, device, fused=False, vocab_shards=0, seq_level=False, entropy_bwd=False):
+    if spec.name.startswith("entropy_slsm"):
+        return EntropyBwdStep(spec, seed, device) if entropy_bwd else EntropySlsmStep(spec, seed, device)
     if vocab_shards:
         return VocabShardStep(spec, seed, device, vocab_shards)
+    if seq_level:
+        return SeqStep(spec, seed, device)
     return FusedStep(spec, seed, device) if fused else GrpoStep(spec, seed, device)
 
 
@@ -768,15 +902,33 @@ def oracle_sample(step, rows):
         smp.update(old=g(step.old), ref=g(step.ref), dloss=g(inp.dloss))
     else:
         smp.update(up=g(inp.upstream))
+    if step.oracle_kind == "seq":
+        smp["adv_seq"] = inp.adv.cpu().double().numpy()[np.asarray(rows)[::spec.L] // spec.L]
     return smp
 
 
-def oracle_step(spec, smp):
+def sample_units(spec, kind, n, seed):
+    """Rows of a bounded oracle sample: n rows, or for the sequence-level step whole
+    sequences (its ratio is a sum over a sequence) of about n rows in total."""
+    if kind != "seq":
+        return W.sample_rows(spec.rows, n, seed)
+    seqs = W.sample_rows(spec.B, max(1, -(-n // spec.L)), seed)
+    return (seqs[:, None] * spec.L + np.arange(spec.L)[None, :]).reshape(-1)
+
+
+def oracle_step(spec, smp, kind):
     import oracle
-    if spec.name.startswith("entropy_slsm"):
+    if kind == "slsm":
         oracle.entropy_from_logits(smp["x"], spec.T)
         oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
         d, _ = oracle.selective_log_softmax_bwd(smp["x"], smp["idx"], smp["up"], spec.T)
+    elif kind == "entropy_bwd":
+        oracle.entropy_from_logits(smp["x"], spec.T)
+        d, _ = oracle.entropy_from_logits_bwd(smp["x"], smp["up"], spec.T)
+    elif kind == "seq":
+        n_seq = len(smp["adv_seq"])
+        d, _, _ = oracle.grpo_seq_loss_bwd(smp["x"], smp["idx"], smp["old"], smp["ref"], smp["adv_seq"], smp["mask"],
+                                           smp["dloss"], n_seq, spec.L, spec.T, spec.beta, spec.eps_low, spec.eps_high)
     else:
         oracle.grpo_loss_fwd(smp["x"], smp["idx"], smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.T,
                              spec.beta, spec.eps_low, spec.eps_high)
@@ -790,21 +942,22 @@ def oracle_step(spec, smp):
 
 def cpu_baseline(step, bytes_per_row, budget_s=12.0):
     """Time the oracle, as it stands, on a bounded sample of rows of this workload."""
-    spec = step.spec
-    probe = W.sample_rows(spec.rows, 16, 7)
+    spec, kind = step.spec, step.oracle_kind
+    probe = sample_units(spec, kind, 16, 7)
     smp = oracle_sample(step, probe)
     t = time.perf_counter()
-    oracle_step(spec, smp)
+    oracle_step(spec, smp, kind)
     per_row = (time.perf_counter() - t) / len(probe)
     n = int(max(16, min(spec.rows, budget_s / max(per_row, 1e-9))))
-    rows = W.sample_rows(spec.rows, n, 11)
+    rows = sample_units(spec, kind, n, 11)
     smp = oracle_sample(step, rows)
     t = time.perf_counter()
-    oracle_step(spec, smp)
+    oracle_step(spec, smp, kind)
     dt = time.perf_counter() - t
     return {"value": round(bytes_per_row * len(rows) / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
             "kind": "oracle", "rows_per_s": round(len(rows) / dt, 2),
-            "sample": f"{len(rows)} of {spec.rows} rows of {spec.name} (fwd+bwd, fp64 numpy, one thread), {dt:.1f} s"}
+            "sample": f"{len(rows)} of {spec.rows} rows of {spec.name} ({kind} fwd+bwd, fp64 numpy, one thread), "
+                      f"{dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -830,6 +983,11 @@ def parse_args(argv=None):
                     help="GRPO workloads: time grpo_loss_fused (one kernel) instead of grpo_loss_fwd + grpo_loss_bwd")
     ap.add_argument("--vocab-shards", type=int, default=0,
                     help="GRPO workloads: the vocabulary-parallel step of this many shards, run shard after shard")
+    ap.add_argument("--seq-level", action="store_true",
+                    help="GRPO workloads: the sequence-level step (selective_log_softmax_fwd, grpo_seq_terms, "
+                         "selective_log_softmax_bwd)")
+    ap.add_argument("--entropy-bwd", action="store_true",
+                    help="entropy_slsm workload: entropy_from_logits (with lse) then entropy_from_logits_bwd")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -839,7 +997,8 @@ def parse_args(argv=None):
 def base_line(args, spec, world):
     return {"metric": METRIC, "unit": "GB/s", "n_gpus": world, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic",
-            "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "V": spec.V, "T": spec.T,
+            "config": {"workload": spec.name, "pass": step_kind(args, spec), "B": spec.B, "L": spec.L, "V": spec.V,
+                       "T": spec.T,
                        "beta": spec.beta, "eps_low": spec.eps_low, "eps_high": spec.eps_high,
                        "logits_dtype": spec.dtype, "strided": spec.strided,
                        "l2": "flushed before every timed step (256 MB write + 256 MB read, not timed)",
@@ -860,6 +1019,7 @@ def run_reference(args):
     inp = W.generate(spec, args.seed, device="cpu")
     R, L = spec.rows, spec.L
     grpo = not spec.name.startswith("entropy_slsm")
+    kind = step_kind(args, spec)
     adv_rows = oracle.per_row(inp.adv.numpy(), L)
 
     def sample(rows):
@@ -877,12 +1037,26 @@ def run_reference(args):
             smp["dloss"] = inp.dloss.numpy().astype(np.float64)[rows]
         else:
             smp["up"] = inp.upstream.numpy().astype(np.float64)[rows]
+        if kind == "seq":
+            smp["adv_seq"] = inp.adv.numpy().astype(np.float64)[rows[::L] // L]
         return smp
 
     def sample_bytes(smp):
         n = len(smp["idx"])
+        V, s = spec.V, spec.elem_size
+        if kind == "entropy_bwd":
+            return n * (V * s + 8) + n * (4 + V * s) + int((smp["up"] != 0).sum()) * (8 + V * s)
         if not grpo:
-            return n * sum(f(spec.V, spec.elem_size) for f in SLSM_ROW_BYTES.values())
+            return n * sum(f(V, s) for f in SLSM_ROW_BYTES.values())
+        if kind == "seq":
+            live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
+            lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
+            t = oracle.grpo_seq_terms(lp, smp["old"], smp["ref"], smp["adv_seq"], smp["mask"], smp["dloss"],
+                                      n // L, L, spec.beta, spec.eps_low, spec.eps_high)
+            m, o, r = (smp["mask"] is not None), 4 * (smp["old"] is not None), 4 * (smp["ref"] is not None)
+            nz = int((t["dlogp"] != 0).sum())
+            return (n * (V * s + 16) + n * (m + 12) + int(live.sum()) * (8 + o + r) + (n // L) * 9
+                    + n * (4 + V * s) + nz * (12 + V * s))
         live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
         lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
         g = oracle.grpo_dlogp(lp, smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.beta, spec.eps_low,
@@ -893,16 +1067,17 @@ def run_reference(args):
 
     K = args.steps if args.steps is not None else 10
     Wm = args.warmup
-    probe = sample(W.sample_rows(R, 8, 3))
+    probe_rows = sample_units(spec, kind, 8, 3)
+    probe = sample(probe_rows)
     t = time.perf_counter()
-    oracle_step(spec, probe)
-    per_row = (time.perf_counter() - t) / 8
+    oracle_step(spec, probe, kind)
+    per_row = (time.perf_counter() - t) / len(probe_rows)
     rows_per_step = int(max(1, min(R, 150.0 / max(1, K + Wm) / max(per_row, 1e-9))))
     times, nbytes = [], 0
     for i in range(Wm + K):
-        smp = sample(W.sample_rows(R, rows_per_step, 100 + i))
+        smp = sample(sample_units(spec, kind, rows_per_step, 100 + i))
         t = time.perf_counter()
-        oracle_step(spec, smp)
+        oracle_step(spec, smp, kind)
         dt = time.perf_counter() - t
         if i >= Wm:
             times.append(dt)
@@ -913,7 +1088,7 @@ def run_reference(args):
     line.update({"impl": "reference", "value": round(value, 6), "steps": K, "warmup": Wm,
                  "ms_per_step": round(1e3 * total / K, 3), "dtype": "f64",
                  "rows_per_s": round(rows_per_step * K / total, 2)})
-    sample_txt = f"{rows_per_step} of {R} rows of {spec.name} per step (fwd+bwd, fp64 numpy, one thread)"
+    sample_txt = f"{rows_per_step} of {R} rows of {spec.name} per step ({kind} fwd+bwd, fp64 numpy, one thread)"
     line["cpu_baseline"] = {"value": line["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
                             "sample": sample_txt}
     line["e2e"] = {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -977,7 +1152,8 @@ def main(argv=None):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     spec = make_spec(args)
-    step = make_step(spec, args.seed + rank, device, fused=args.fused, vocab_shards=args.vocab_shards)
+    step = make_step(spec, args.seed + rank, device, fused=args.fused, vocab_shards=args.vocab_shards,
+                     seq_level=args.seq_level, entropy_bwd=args.entropy_bwd)
     flush_buf = L2Flush(device)
 
     # one untimed step to classify rows, then calibrate the step count

@@ -92,3 +92,20 @@ def test_vocab_shard_starts_cover_the_vocabulary():
         assert st[0] == 0 and st[-1] == V and len(st) == S + 1
         w = np.diff(st)
         assert (w >= 1).all() and w.max() - w.min() <= 1
+
+
+def test_step_kind_and_sequence_samples():
+    """The sequence-level pass is sampled in whole sequences (its ratio sums over one);
+    the other passes sample single rows."""
+    spec = W.get("grpo_b4_l512_v32000")
+    args = bench.parse_args(["--seq-level"])
+    assert bench.step_kind(args, spec) == "seq"
+    assert bench.step_kind(bench.parse_args([]), spec) == "grpo"
+    ent = W.get("entropy_slsm_b16_l4096_v32000")
+    assert bench.step_kind(bench.parse_args(["--entropy-bwd"]), ent) == "entropy_bwd"
+    assert bench.step_kind(bench.parse_args([]), ent) == "slsm"
+    rows = bench.sample_units(spec, "seq", 700, 5)
+    assert len(rows) == 2 * spec.L
+    seqs = rows.reshape(-1, spec.L)
+    assert (np.diff(seqs, axis=1) == 1).all() and (seqs[:, 0] % spec.L == 0).all()
+    assert len(bench.sample_units(spec, "grpo", 700, 5)) == 700
