@@ -109,3 +109,27 @@ def test_step_kind_and_sequence_samples():
     seqs = rows.reshape(-1, spec.L)
     assert (np.diff(seqs, axis=1) == 1).all() and (seqs[:, 0] % spec.L == 0).all()
     assert len(bench.sample_units(spec, "grpo", 700, 5)) == 700
+
+
+def test_oracle_pool_splits_whole_units_and_runs():
+    """The all-cores oracle baseline: parts are disjoint, cover the sample, and keep whole
+    sequences for the sequence-level pass; two spawned workers run the oracle on them."""
+    import oracle
+    spec = W.get("grpo_b4_l512_v32000", B=3, L=8, V=64)
+    inp = W.generate(spec, 0, device="cpu")
+    x = oracle.bf16_bits_to_fp64(inp.logits.reshape(-1, spec.V).view(torch.int16).numpy().view(np.uint16))
+    smp = {"x": x, "idx": inp.idx.numpy(), "adv": oracle.per_row(inp.adv.numpy(), spec.L), "mask": inp.mask.numpy(),
+           "old": None, "ref": None, "dloss": inp.dloss.double().numpy(), "adv_seq": inp.adv.double().numpy()}
+    for kind, unit in (("grpo", 1), ("seq", spec.L)):
+        pool = bench.OraclePool(2, spec, kind)
+        try:
+            parts = pool.split(smp)
+            assert len(parts) == 2
+            assert np.array_equal(np.concatenate([p["x"] for p in parts]), x)
+            assert all(len(p["idx"]) % unit == 0 for p in parts)
+            if kind == "seq":
+                assert np.array_equal(np.concatenate([p["adv_seq"] for p in parts]), smp["adv_seq"])
+            dt, used = pool.run(smp)
+            assert used == 2 and dt > 0
+        finally:
+            pool.close()
