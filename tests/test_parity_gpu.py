@@ -41,14 +41,15 @@ def select_rows(logits: torch.Tensor, rows: np.ndarray) -> torch.Tensor:
     return logits[r // L, r % L]
 
 
-def oracle_logp(logits, idx_np, T, chunk=256):
+def oracle_logp(logits, idx_np, T, chunk=256, rows=None):
+    """The oracle's logp of `rows` (default: every row), in chunks of rows."""
     B, L, V = logits.shape
-    R = B * L
-    out = np.empty(R)
-    for r0 in range(0, R, chunk):
-        rows = np.arange(r0, min(R, r0 + chunk))
-        lp, _ = oracle.selective_log_softmax(rows_f64(select_rows(logits, rows)), idx_np[rows], T)
-        out[rows] = lp
+    rows = np.arange(B * L) if rows is None else np.asarray(rows)
+    out = np.empty(len(rows))
+    for k0 in range(0, len(rows), chunk):
+        part = rows[k0:k0 + chunk]
+        lp, _ = oracle.selective_log_softmax(rows_f64(select_rows(logits, part)), idx_np[part], T)
+        out[k0:k0 + len(part)] = lp
     return out
 
 
@@ -599,7 +600,8 @@ def test_entropy_bwd_tiny_every_row(seed):
 
 
 def test_entropy_bwd_v32000_sampled_rows_with_peaks():
-    spec = W.get("entropy_slsm_b16_l4096_v32000", L=256)
+    """(16, 4096, 32000) bf16 at full size, as the benchmark's entropy-backward step runs it."""
+    spec = W.get("entropy_slsm_b16_l4096_v32000")
     inp = W.generate(spec, 2, device=DEV)
     T = 1.0
     H, lse = rp.entropy_from_logits(inp.logits, T=T, return_lse=True)
@@ -661,52 +663,58 @@ def run_seq_pipeline(inp, old, ref, T, beta, el, eh):
     return logp, lse, st, dl
 
 
-def compare_seq(inp, old, ref, T, beta, el, eh, logp, lse, st, dl, tag, rows=None):
-    """Every sequence's terms and the dlogits of `rows` (default: every row) against the oracle.
-    The per-sequence ratio depends on the forward's fp32 logp of all the sequence's tokens,
-    so the budget of each term includes |A| s max|dlogp| (and the KL's own dependence)."""
+def compare_seq(inp, old, ref, T, beta, el, eh, logp, lse, st, dl, tag, rows=None, seqs=None):
+    """The terms of the sequences `seqs` (default: every sequence) and the dlogits of `rows`
+    (default: every row of those sequences) against the oracle.  The per-sequence ratio
+    depends on the forward's fp32 logp of all the sequence's tokens, so the budget of each
+    term includes |A| s max|dlogp| (and the KL's own dependence)."""
     spec = inp.spec
     B, L = spec.B, spec.L
-    R = B * L
-    x_all = None
-    idx = inp.idx.cpu().numpy()
-    mask = None if inp.mask is None else inp.mask.cpu().numpy()
-    dloss = inp.dloss.cpu().numpy().astype(np.float64)
-    A = inp.adv.cpu().numpy().astype(np.float64)
-    o_old = None if old is None else np.asarray(old, dtype=np.float64)
-    o_ref = None if ref is None else np.asarray(ref, dtype=np.float64)
-    lp_o = oracle_logp(inp.logits, idx, T)
-    terms = oracle.grpo_seq_terms(lp_o, o_old, o_ref, A, mask, dloss, B, L, beta, el, eh)
-    dlp = np.abs(logp.double().cpu().numpy() - lp_o)
-    m = np.ones((B, L), bool) if mask is None else mask.reshape(B, L) != 0
-    dmax = np.where(m, dlp.reshape(B, L), 0.0).max(axis=1)                       # per sequence
+    seqs = np.arange(B) if seqs is None else np.sort(np.asarray(seqs))
+    Bs = len(seqs)
+    srows = (seqs[:, None] * L + np.arange(L)[None, :]).reshape(-1)     # rows of the checked sequences
+    idx_all = inp.idx.cpu().numpy()
+    idx = idx_all[srows]
+    mask = None if inp.mask is None else inp.mask.cpu().numpy()[srows]
+    dloss = inp.dloss.cpu().numpy().astype(np.float64)[srows]
+    A = inp.adv.cpu().numpy().astype(np.float64)[seqs]
+    o_old = None if old is None else np.asarray(old, dtype=np.float64)[srows]
+    o_ref = None if ref is None else np.asarray(ref, dtype=np.float64)[srows]
+    lp_o = oracle_logp(inp.logits, idx_all, T, rows=srows)
+    terms = oracle.grpo_seq_terms(lp_o, o_old, o_ref, A, mask, dloss, Bs, L, beta, el, eh)
+    dlp = np.abs(logp.double().cpu().numpy()[srows] - lp_o)
+    m = np.ones((Bs, L), bool) if mask is None else mask.reshape(Bs, L) != 0
+    dmax = np.where(m, dlp.reshape(Bs, L), 0.0).max(axis=1)                      # per sequence
     s = terms["seq_ratio"]
-    assert_scalar_close(st["seq_ratio"], s, f"{tag} seq ratio", atol=0.0,
+    assert_scalar_close(st["seq_ratio"].cpu()[seqs], s, f"{tag} seq ratio", atol=0.0,
                         rtol=1e-5 + float(np.max(dmax) * 1.01))
     lo, hi = 1 - el, 1 + eh
     amb_seq = (A != 0) & ((np.abs(s - lo) <= 1e-5 * lo) | (np.abs(s - hi) <= 1e-5 * hi))
-    assert np.array_equal(st["seq_is_clipped"].cpu().numpy().astype(bool)[~amb_seq], terms["seq_is_clipped"][~amb_seq])
-    W = np.where(m, dloss.reshape(B, L), 0.0).sum(axis=1)
+    assert np.array_equal(st["seq_is_clipped"].cpu().numpy().astype(bool)[seqs][~amb_seq],
+                          terms["seq_is_clipped"][~amb_seq])
+    W = np.where(m, dloss.reshape(Bs, L), 0.0).sum(axis=1)
     n = np.maximum(m.sum(axis=1), 1)
     pg_sens = (np.abs(A) * s)[:, None] * dmax[:, None]                             # |d pg| bound
-    kl_sens = (beta * np.exp(np.asarray(o_ref).reshape(B, L) - lp_o.reshape(B, L)) * dlp.reshape(B, L)
-               if (beta != 0 and o_ref is not None) else np.zeros((B, L)))
+    kl_sens = (beta * np.exp(np.asarray(o_ref).reshape(Bs, L) - lp_o.reshape(Bs, L)) * dlp.reshape(Bs, L)
+               if (beta != 0 and o_ref is not None) else np.zeros((Bs, L)))
     loss_budget = (pg_sens + kl_sens).reshape(-1) * 1.01
-    assert_scalar_close(st["loss"], terms["loss"], f"{tag} loss", atol=1e-5 + float(loss_budget.max()))
-    dlogp_budget = ((W * np.abs(A) * s / n * 2 * dmax)[:, None] + kl_sens * np.abs(dloss.reshape(B, L))).reshape(-1)
-    got = st["dlogp"].double().cpu().numpy()
+    assert_scalar_close(st["loss"].cpu()[srows], terms["loss"], f"{tag} loss", atol=1e-5 + float(loss_budget.max()))
+    dlogp_budget = ((W * np.abs(A) * s / n * 2 * dmax)[:, None] + kl_sens * np.abs(dloss.reshape(Bs, L))).reshape(-1)
+    got = st["dlogp"].double().cpu().numpy()[srows]
     err = np.abs(got - terms["dlogp"])
     assert np.all(err <= 1e-5 * np.abs(terms["dlogp"]) + 1e-7 * np.abs(W).max() + dlogp_budget * 1.01), \
         f"{tag} dlogp: worst {err.max():.3g}"
     # dlogits: the row factor is dlogp / T with the GPU's own dlogp; its deviation is the budget
-    rows = np.arange(R) if rows is None else rows
+    rows = srows if rows is None else np.asarray(rows)
+    pos = np.searchsorted(srows, rows)
+    assert np.array_equal(srows[pos], rows), "rows outside the checked sequences"
     x = rows_f64(select_rows(inp.logits, rows))
-    odl = oracle.softmax_gather_grad(x, idx[rows], terms["dlogp"][rows] / T, T)
-    g = terms["dlogp"][rows] / T
+    odl = oracle.softmax_gather_grad(x, idx[pos], terms["dlogp"][pos] / T, T)
+    g = terms["dlogp"][pos] / T
     with np.errstate(divide="ignore", invalid="ignore"):
-        rho = np.where(g != 0, err[rows] / np.abs(terms["dlogp"][rows]), 0.0)
-    rho = rho + np.abs(lse.double().cpu().numpy()[rows] - oracle.selective_log_softmax(x, idx[rows], T)[1]) + 1e-6
-    amb = (rho > 2.0 ** -10) | np.repeat(amb_seq, L)[rows]
+        rho = np.where(g != 0, err[pos] / np.abs(terms["dlogp"][pos]), 0.0)
+    rho = rho + np.abs(lse.double().cpu().numpy()[rows] - oracle.selective_log_softmax(x, idx[pos], T)[1]) + 1e-6
+    amb = (rho > 2.0 ** -10) | np.repeat(amb_seq, L)[pos]
     assert amb.sum() <= max(2, 0.01 * len(rows)), f"{tag}: {amb.sum()} ambiguous rows"
     assert_grad_rows(select_rows(dl, rows), odl, g, amb, f"{tag} dlogits", rho=rho)
 
@@ -750,3 +758,29 @@ def test_seq_level_beta_and_all_masked_sequence():
     compare_seq(inp, old, ref, T, beta, el, eh, *out, "seq beta")
     assert float(out[2]["seq_ratio"][2]) == 1.0
     assert_plus_zero(out[3][2], "all-masked sequence")
+
+
+def test_seq_level_qwen3_full_size_sampled():
+    """(16, 1024, 151936) bf16, beta = 0.04, in the launch configuration the benchmark's
+    sequence-level step times.  Three whole sequences go through the oracle (their ratio
+    sums over all their tokens) with 48 of their rows checked element by element; every
+    row is checked for masked rows being +0.0 and for a row sum of ~0."""
+    spec = W.get("grpo_qwen3_b16_l1024_v151936")
+    inp = W.generate(spec, 1, device=DEV)
+    T, beta, el, eh = f32(spec.T), f32(spec.beta), f32(spec.eps_low), f32(spec.eps_high)
+    seqs = np.array([0, 7, 15])
+    srows = (seqs[:, None] * spec.L + np.arange(spec.L)[None, :]).reshape(-1)
+    lp_all = torch_logp(inp.logits, inp.idx, T).double().cpu().numpy()
+    lp_all[srows] = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T, rows=srows)
+    old, ref = near_logp_inputs(inp, lp_all)
+    logp, lse, st, dl = run_seq_pipeline(inp, old, ref, T, beta, el, eh)
+    live = inp.mask.cpu().numpy()[srows] != 0
+    rows = np.unique(np.concatenate([srows[live][W.sample_rows(int(live.sum()), 40, 6)],
+                                     srows[~live][:8]]))
+    compare_seq(inp, old, ref, T, beta, el, eh, logp, lse, st, dl, "seq qwen3", rows=rows, seqs=seqs)
+    masked = inp.mask == 0
+    assert bool(masked.any())
+    assert_plus_zero(dl.reshape(-1, spec.V)[masked], "masked dlogits rows")
+    g = st["dlogp"].abs() / T
+    rs = dl.float().sum(dim=-1).reshape(-1).abs()
+    assert bool(torch.all(rs <= g * (1e-3 + spec.V * 2.0 ** -8)))
