@@ -111,18 +111,58 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
-def kernel_source_hash() -> str:
-    h = hashlib.sha256()
+# Translation units behind each entry point; with the files they include (closure of the
+# quoted #include lines) they fix that entry point's kernels and launch shapes.
+_FWD = ("rowpass_fwd_bf16.cu", "rowpass_fwd_f32.cu")
+_BWD = ("rowpass_bwd_bf16.cu", "rowpass_bwd_f32.cu")
+KERNEL_UNITS = {
+    "grpo_loss_fwd": _FWD, "entropy_from_logits": _FWD, "selective_log_softmax_fwd": _FWD,
+    "grpo_vocab_shard_stats": _FWD,
+    "grpo_loss_bwd": _BWD, "selective_log_softmax_bwd": _BWD, "entropy_from_logits_bwd": _BWD,
+    "grpo_loss_bwd_vocab_shard": _BWD,
+    "grpo_loss_fused": ("rowpass_fused_bf16.cu", "rowpass_fused_f32.cu"),
+    "grpo_seq_terms": ("rowpass_seq.cu",),
+    "grpo_vocab_combine": ("rowpass_vocab.cu",),
+    "grpo_fused_linear": ("rowpass_linear.cu",),
+}
+
+
+def _source_closure(units):
     csrc = os.path.join(ROOT, "rl_fine_tuning_pass_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+    search = (csrc, os.path.join(ROOT, "include"))
+    seen, todo = {}, list(units)
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in search if os.path.isfile(os.path.join(d, name))), None)
+        if path is None:
+            continue
+        with open(path, "rb") as f:
+            seen[name] = f.read()
+        for line in seen[name].decode(errors="replace").splitlines():
+            line = line.strip()
+            if line.startswith("#include \""):
+                todo.append(line.split('"')[1])
+    return seen
+
+
+def kernel_source_hash(kernel: str = None) -> str:
+    """Hash of the kernel sources: all of them, or those behind one entry point."""
+    if kernel is None:
+        csrc = os.path.join(ROOT, "rl_fine_tuning_pass_gb300", "csrc")
+        files = {n: open(os.path.join(csrc, n), "rb").read() for n in os.listdir(csrc)}
+    else:
+        files = _source_closure(KERNEL_UNITS[kernel])
+    h = hashlib.sha256()
+    for name in sorted(files):
+        h.update(name.encode() + b"\0" + files[name])
     return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources; else None."""
+    current sources of that kernel (kernel_source_hash(kernel)); else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -130,7 +170,7 @@ def measured_traffic(kernel: str, workload: str):
     except Exception:
         return None
     ent = rec.get(workload, {}).get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or kernel not in KERNEL_UNITS or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -1369,6 +1409,7 @@ def main(argv=None):
                             "GB_per_s": round(per_launch[n] / (kern_ms[n] * 1e-3) / 1e9, 1)} for n in kern_ms},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "source_hash": kernel_source_hash(dom) if dom in KERNEL_UNITS else None,
                          "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": int(per_launch[dom])},
             "cpu_baseline": cpu, "e2e": e2e,

@@ -133,3 +133,15 @@ def test_oracle_pool_splits_whole_units_and_runs():
             assert used == 2 and dt > 0
         finally:
             pool.close()
+
+
+def test_kernel_source_hash_per_entry_point():
+    """Each entry point's hash covers its translation units and what they include, and no more."""
+    seq = bench._source_closure(bench.KERNEL_UNITS["grpo_seq_terms"])
+    assert "rowpass_seq.cu" in seq and "rowpass_common.cuh" in seq and "rowpass_fwd.cuh" not in seq
+    fused = bench._source_closure(bench.KERNEL_UNITS["grpo_loss_fused"])
+    assert {"rowpass_fused.cuh", "rowpass_fwd.cuh", "rowpass_bwd.cuh", "rowpass_internal.h"} <= set(fused)
+    hashes = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_UNITS}
+    assert hashes["grpo_loss_fwd"] == hashes["entropy_from_logits"] != hashes["grpo_loss_bwd"]
+    assert all(len(h) == 16 for h in hashes.values())
+    assert bench.measured_traffic("not_an_entry_point", "grpo_b4_l512_v32000") is None
