@@ -784,3 +784,43 @@ def test_seq_level_qwen3_full_size_sampled():
     g = st["dlogp"].abs() / T
     rs = dl.float().sum(dim=-1).reshape(-1).abs()
     assert bool(torch.all(rs <= g * (1e-3 + spec.V * 2.0 ** -8)))
+
+
+@pytest.mark.parametrize("L", [1, 31, 256, 257, 700, 1024, 1025, 3000])
+def test_seq_terms_every_length_against_oracle(L):
+    """grpo_seq_terms alone on fp32 inputs, across the register-resident kernels (L <= 256,
+    512, 1024) and the two-pass one (L > 1024): a masked tail, a fully masked sequence, one
+    with A = 0, and beta on."""
+    B = 5
+    g = torch.Generator().manual_seed(L)
+    logp = -torch.rand(B * L, generator=g).float() * 4
+    old = (logp + torch.randn(B * L, generator=g) * 0.05).float()
+    ref = (logp + torch.randn(B * L, generator=g) * 0.05).float()
+    mask = (torch.rand(B * L, generator=g) > 0.15).to(torch.uint8)
+    mask.view(B, L)[1] = 0
+    dloss = (torch.rand(B * L, generator=g) / L).float() * mask.float()
+    adv = torch.randn(B, generator=g).float()
+    adv[2] = 0.0
+    beta, el, eh = 0.04, 0.2, 0.28
+    st = rp.grpo_seq_terms(logp.to(DEV), adv.to(DEV), dloss.to(DEV), B=B, L=L, beta=beta, eps_low=el, eps_high=eh,
+                           old_logp=old.to(DEV), ref_logp=ref.to(DEV), mask=mask.to(DEV))
+    torch.cuda.synchronize()
+    t = oracle.grpo_seq_terms(logp.double().numpy(), old.double().numpy(), ref.double().numpy(),
+                              adv.double().numpy(), mask.numpy(), dloss.double().numpy(), B, L, beta, el, eh)
+    assert_scalar_close(st["seq_ratio"], t["seq_ratio"], f"L={L} seq ratio")
+    lo, hi = 1 - el, 1 + eh
+    s = t["seq_ratio"]
+    amb = (np.abs(s - lo) <= 1e-5 * lo) | (np.abs(s - hi) <= 1e-5 * hi)
+    assert np.array_equal(st["seq_is_clipped"].cpu().numpy().astype(bool)[~amb], t["seq_is_clipped"][~amb])
+    assert_scalar_close(st["loss"], t["loss"], f"L={L} loss")
+    assert_scalar_close(st["kl"], t["kl"], f"L={L} kl")
+    W = np.abs(dloss.double().numpy()).reshape(B, L).sum(axis=1)
+    got = st["dlogp"].double().cpu().numpy()
+    err = np.abs(got - t["dlogp"])
+    assert np.all(err <= 1e-5 * np.abs(t["dlogp"]) + 1e-6 * np.repeat(W * np.abs(adv.numpy()) + beta, L)), \
+        f"L={L} dlogp: worst {err.max():.3g}"
+    masked = mask.numpy() == 0
+    for k in ("loss", "kl", "dlogp"):
+        v = st[k].cpu().numpy()[masked]
+        assert np.all(v == 0.0) and not np.any(np.signbit(v)), f"L={L} masked {k} must be +0.0"
+    assert float(st["seq_ratio"][1]) == 1.0
