@@ -824,3 +824,49 @@ def test_seq_terms_every_length_against_oracle(L):
         v = st[k].cpu().numpy()[masked]
         assert np.all(v == 0.0) and not np.any(np.signbit(v)), f"L={L} masked {k} must be +0.0"
     assert float(st["seq_ratio"][1]) == 1.0
+
+
+# ---------------------------------------------------------------------------
+# size limits: a million-entry vocabulary row, sixteen million rows
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_vocabulary_of_a_million_every_element(dtype):
+    """V = 2^20 + 3 (a scalar tail after the last 16-byte vector): four rows with idx at the
+    first column, the last column and two inside, every output and every dlogits element
+    against the oracle.  Each thread's partial sums cover ~4096 terms here, 15 times more
+    than at V = 151936; the scalar tolerances are unchanged."""
+    spec = W.get("tiny_fp32", B=1, L=4, V=(1 << 20) + 3, dtype=dtype, adv="plus_minus_one")
+    inp = W.generate(spec, 5, device=DEV)
+    inp.idx[0] = 0
+    inp.idx[1] = spec.V - 1
+    T, beta, el, eh = f32(0.8), f32(0.04), f32(spec.eps_low), f32(spec.eps_high)
+    lp = oracle_logp(inp.logits, inp.idx.cpu().numpy(), T)
+    old, ref = near_logp_inputs(inp, lp)
+    f, dl, err = run_gpu_grpo(inp, old, ref, T, beta, el, eh)
+    assert err == 0
+    compare_grpo_rows(inp, f, dl, np.arange(spec.rows), old, ref, T, beta, el, eh, f"V=2^20+3 {dtype}")
+
+
+def test_sixteen_million_rows_sampled():
+    """B = L = 4096 (16,777,216 rows, one CTA each) with V = 8: 4096 sampled rows against the
+    oracle, and over every row: masked rows and zero-advantage sequences (beta = 0) give
+    +0.0 gradient rows, the others sum to ~0."""
+    spec = W.get("grpo_b4_l512_v32000", B=4096, L=4096, V=8)
+    inp = W.generate(spec, 7, device=DEV, rows_per_chunk=1 << 20)
+    T, beta, el, eh = f32(spec.T), 0.0, f32(spec.eps_low), f32(spec.eps_high)
+    rows = W.sample_rows(spec.rows, 4096, 9)
+    lp_all = torch_logp(inp.logits, inp.idx, T, chunk=1 << 20).double().cpu().numpy()
+    lp_all[rows] = oracle.selective_log_softmax(rows_f64(select_rows(inp.logits, rows)),
+                                                inp.idx.cpu().numpy()[rows], T)[0]
+    old, ref = near_logp_inputs(inp, lp_all)
+    f, dl, err = run_gpu_grpo(inp, old, ref, T, beta, el, eh)
+    assert err == 0
+    compare_grpo_rows(inp, f, dl, rows, old, ref, T, beta, el, eh, "16M rows")
+    flat = dl.reshape(-1, spec.V)
+    zero_rows = (inp.mask == 0) | (inp.adv.repeat_interleave(spec.L) == 0)
+    assert bool(zero_rows.any()) and bool((~zero_rows).any())
+    assert_plus_zero(flat[zero_rows], "masked and zero-advantage rows")
+    rs = flat.float().sum(dim=-1).abs()
+    bound = flat.float().abs().sum(dim=-1) * 2.0 ** -8 + 1e-30
+    assert bool(torch.all(rs <= bound)), "row sums"
