@@ -397,11 +397,14 @@ def grpo_fused_linear_workspace_size(V, chunk_rows):
 
 
 def grpo_fused_linear(hidden, weight, idx, adv, dloss, *, B, L, T, beta, eps_low, eps_high, old_logp=None,
-                      ref_logp=None, mask=None, chunk_rows=1024, with_grad_hidden=True, grad_weight=None,
+                      ref_logp=None, mask=None, chunk_rows=2048, with_grad_hidden=True, grad_weight=None,
                       with_grad_weight=True, with_entropy=True, workspace=None, dev_err=None):
     """GRPO loss on top of the LM head, in chunks of rows: dict with the forward outputs
     (loss, logp, lse, kl, is_clipped, entropy), grad_hidden [B*L, H] fp32 and grad_weight
-    [V, H] fp32 (accumulated into the given tensor, else into zeros)."""
+    [V, H] fp32 (accumulated into the given tensor, else into zeros).  chunk_rows trades
+    workspace (one chunk's fp32 logits and bf16 dlogits, ~6 V bytes a row) for speed: with
+    V = 151936 and H = 1024, 1024 / 2048 / 4096 rows took 13.2 / 11.7 / 10.9 ms for 16384
+    rows on GB300."""
     R, H = hidden.shape
     V = weight.shape[0]
     if R != B * L:
