@@ -272,15 +272,21 @@ SLSM_ROW_BYTES = {"entropy_from_logits": lambda V, s: V * s + 4,
 
 
 class PipelinedE2E:
-    """End-to-end through the public API with host buffers.  The batch is cut into parts
-    of whole sequences; a part's inputs go host -> device on one stream, its calls run on a
-    second stream once they have landed, and its outputs go device -> host on a third, so
-    the two copy directions and the kernels of neighbouring parts overlap.  A subclass
-    names its inputs (e2e_inputs: tensor and layout, "b" = leading batch dimension, "r" =
-    one value per row), its outputs (e2e_outputs: shape, dtype, layout) and makes the
-    public calls of one part (e2e_part)."""
+    """End-to-end through the public API with host buffers.  The batch is cut into parts: a
+    part is a group of whole sequences, or, for the token-level passes when there are
+    fewer sequences than parts, a range of one sequence's tokens (the public calls take it
+    as a batch of one sequence of that many tokens).  The per-row and per-sequence inputs
+    go host -> device once at the start of the step; then each part's logits go host ->
+    device on one stream, its calls run on a second once they have landed, and its outputs
+    go device -> host on a third, so the two copy directions and the kernels of
+    neighbouring parts overlap.  A subclass names its inputs (e2e_inputs: tensor and
+    layout: "bl" = [B, L, ...], "s" = one value per sequence, "r" = one value per row), its
+    outputs (e2e_outputs: shape, dtype, layout) and makes the public calls of one part
+    (e2e_part)."""
 
-    E2E_PARTS = 8
+    E2E_PARTS = 16               # at most; parts of at least E2E_PART_BYTES of logits
+    E2E_PART_BYTES = 32 << 20    # below this the calls' host-side cost outweighs a part's copy time
+    E2E_WHOLE_SEQUENCES = False  # True where a part must hold whole sequences
 
     def e2e_setup(self):
         dev = self.inp.logits.device
@@ -293,14 +299,19 @@ class PipelinedE2E:
         self.lay_out = {k: lay for k, (_, _, lay) in outs.items()}
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
         self.d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
-        B = self.spec.B
-        P = max(1, min(B, self.E2E_PARTS))
-        self.e2e_bounds = [(B * k // P, B * (k + 1) // P) for k in range(P)]
+        logit_bytes = self.h_in["logits"].numel() * self.h_in["logits"].element_size()
+        n = int(max(1, min(self.E2E_PARTS, (logit_bytes + self.E2E_PART_BYTES // 2) // self.E2E_PART_BYTES)))
+        self.e2e_bounds = e2e_parts(self.spec.B, self.spec.L, n, self.E2E_WHOLE_SEQUENCES)
         self.e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
 
-    def _cut(self, t, lay, b0, b1):
+    def _cut(self, t, lay, part):
+        b0, b1, l0, l1 = part
+        if lay == "bl":
+            return t[b0:b1, l0:l1]
+        if lay == "s":
+            return t[b0:b1]
         L = self.spec.L
-        return t[b0:b1] if lay == "b" else t[b0 * L:b1 * L]
+        return t[b0 * L + l0:(b1 - 1) * L + l1]
 
     def e2e_step(self):
         s_in, s_run, s_out = self.e2e_streams
@@ -308,32 +319,46 @@ class PipelinedE2E:
         s_in.wait_stream(main)  # the previous step is over (main waited for its last copy out)
         landed = []
         with torch.cuda.stream(s_in):
-            for b0, b1 in self.e2e_bounds:
+            for k, h in self.h_in.items():  # per-row and per-sequence inputs: once per step
+                if self.lay_in[k] != "bl":
+                    self.d_in[k].copy_(h, non_blocking=True)
+            for part in self.e2e_bounds:
                 for k, h in self.h_in.items():
-                    lay = self.lay_in[k]
-                    self._cut(self.d_in[k], lay, b0, b1).copy_(self._cut(h, lay, b0, b1), non_blocking=True)
+                    if self.lay_in[k] == "bl":
+                        self._cut(self.d_in[k], "bl", part).copy_(self._cut(h, "bl", part), non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(s_in)
                 landed.append(ev)
         done = []
         with torch.cuda.stream(s_run):
-            for (b0, b1), ev in zip(self.e2e_bounds, landed):
+            for part, ev in zip(self.e2e_bounds, landed):
                 s_run.wait_event(ev)
-                d = {k: self._cut(t, self.lay_in[k], b0, b1) for k, t in self.d_in.items()}
-                out = self.e2e_part(d, b0, b1)
+                d = {k: self._cut(t, self.lay_in[k], part) for k, t in self.d_in.items()}
+                out = self.e2e_part(d, part)
                 ev2 = torch.cuda.Event()
                 ev2.record(s_run)
                 done.append((ev2, out))
         with torch.cuda.stream(s_out):
-            for (b0, b1), (ev, out) in zip(self.e2e_bounds, done):
+            for part, (ev, out) in zip(self.e2e_bounds, done):
                 s_out.wait_event(ev)
                 for k, t in out.items():
                     t.record_stream(s_out)  # allocated on s_run, read here
-                    self._cut(self.h_out[k], self.lay_out[k], b0, b1).copy_(t, non_blocking=True)
+                    self._cut(self.h_out[k], self.lay_out[k], part).copy_(t, non_blocking=True)
         main.wait_stream(s_out)
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         raise NotImplementedError
+
+
+def e2e_parts(B, L, P, whole_sequences):
+    """Parts (b0, b1, l0, l1) of a batch of B sequences of L tokens: P groups of whole
+    sequences when B >= P (or when whole sequences are required), else every sequence cut
+    into ceil(P / B) token ranges."""
+    if whole_sequences or B >= P:
+        n = max(1, min(B, P))
+        return [(B * k // n, B * (k + 1) // n, 0, L) for k in range(n)]
+    per = min(L, -(-P // B))
+    return [(b, b + 1, L * k // per, L * (k + 1) // per) for b in range(B) for k in range(per)]
 
 
 class GrpoStep(PipelinedE2E):
@@ -402,21 +427,22 @@ class GrpoStep(PipelinedE2E):
     # -- end-to-end through the public API with host buffers (PipelinedE2E) ------
     def e2e_inputs(self):
         inp = self.inp
-        return {"logits": (inp.logits, "b"), "idx": (inp.idx, "r"), "adv": (inp.adv, "b"), "mask": (inp.mask, "r"),
+        return {"logits": (inp.logits, "bl"), "idx": (inp.idx, "r"), "adv": (inp.adv, "s"), "mask": (inp.mask, "r"),
                 "dloss": (inp.dloss, "r"), "old": (self.old, "r"), "ref": (self.ref, "r")}
 
     def e2e_outputs(self):
-        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "b"),
+        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "bl"),
                 "loss": ((self.spec.rows,), torch.float32, "r")}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         spec = self.spec
         f = rp.grpo_loss_fwd(d["logits"], d["idx"], d["adv"], T=spec.T, beta=spec.beta, eps_low=spec.eps_low,
                              eps_high=spec.eps_high, old_logp=d.get("old"), ref_logp=d.get("ref"), mask=d.get("mask"),
                              with_entropy=True)
         dl = rp.grpo_loss_bwd(d["logits"], d["idx"], d["adv"], d["dloss"], f["logp"], f["lse"], T=spec.T,
                               beta=spec.beta, eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=d.get("old"),
-                              ref_logp=d.get("ref"), mask=d.get("mask"), dlogits=self.dlogits[b0:b1])
+                              ref_logp=d.get("ref"), mask=d.get("mask"),
+                              dlogits=self._cut(self.dlogits, "bl", part))
         return {"dlogits": dl, "loss": f["loss"]}
 
 
@@ -452,12 +478,12 @@ class FusedStep(GrpoStep):
                         "zero_grad_frac": round(n_zero / R, 4), "fused": True}
         return {"grpo_loss_fused": int(b.sum())}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         spec = self.spec
         f = rp.grpo_loss_fused(d["logits"], d["idx"], d["adv"], d["dloss"], T=spec.T, beta=spec.beta,
                                eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=d.get("old"),
                                ref_logp=d.get("ref"), mask=d.get("mask"), with_entropy=True,
-                               dlogits=self.dlogits[b0:b1])
+                               dlogits=self._cut(self.dlogits, "bl", part))
         return {"dlogits": f["dlogits"], "loss": f["loss"]}
 
 
@@ -677,14 +703,14 @@ class VocabShardStep(GrpoStep):
         return {"grpo_vocab_shard_stats": int(stats), "grpo_vocab_combine": int(combine),
                 "grpo_loss_bwd_vocab_shard": int(bwd)}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         spec = self.spec
-        x, dlog = d["logits"], self.dlogits[b0:b1]
+        x, dlog = d["logits"], self._cut(self.dlogits, "bl", part)
         idx, adv, mask, dloss, old, ref = d["idx"], d["adv"], d.get("mask"), d["dloss"], d.get("old"), d.get("ref")
         sl = lambda t, k: t[..., self.starts[k]:self.starts[k + 1]]
         stats = torch.stack([rp.grpo_vocab_shard_stats(sl(x, k), self.starts[k], T=spec.T, idx=idx, mask=mask)
                              for k in range(self.shards)])
-        f = rp.grpo_vocab_combine(stats, self.starts, b1 - b0, spec.L, T=spec.T, idx=idx, adv=adv, grpo=True,
+        f = rp.grpo_vocab_combine(stats, self.starts, x.shape[0], x.shape[1], T=spec.T, idx=idx, adv=adv, grpo=True,
                                   beta=spec.beta, eps_low=spec.eps_low, eps_high=spec.eps_high, old_logp=old,
                                   ref_logp=ref, mask=mask)
         for k in range(self.shards):
@@ -735,19 +761,20 @@ class EntropySlsmStep(PipelinedE2E):
 
     def e2e_inputs(self):
         inp = self.inp
-        return {"logits": (inp.logits, "b"), "idx": (inp.idx, "r"), "up": (inp.upstream, "r")}
+        return {"logits": (inp.logits, "bl"), "idx": (inp.idx, "r"), "up": (inp.upstream, "r")}
 
     def e2e_outputs(self):
         R = self.spec.rows
         f32 = lambda: ((R,), torch.float32, "r")
-        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "b"), "entropy": f32(), "logp": f32(),
+        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "bl"), "entropy": f32(), "logp": f32(),
                 "lse": f32()}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         T = self.spec.T
         H = rp.entropy_from_logits(d["logits"], T=T)
         lp, lse = rp.selective_log_softmax_fwd(d["logits"], d["idx"], T=T)
-        dl = rp.selective_log_softmax_bwd(d["logits"], d["idx"], d["up"], lse, T=T, dlogits=self.dlogits[b0:b1])
+        dl = rp.selective_log_softmax_bwd(d["logits"], d["idx"], d["up"], lse, T=T,
+                                          dlogits=self._cut(self.dlogits, "bl", part))
         return {"dlogits": dl, "entropy": H, "logp": lp, "lse": lse}
 
 
@@ -757,6 +784,7 @@ class SeqStep(GrpoStep):
     selective_log_softmax_bwd (dlogits; rows whose dlogp is 0 are written without a read)."""
 
     oracle_kind = "seq"
+    E2E_WHOLE_SEQUENCES = True
 
     def __init__(self, spec, seed, device, inputs=None):
         super().__init__(spec, seed, device, inputs)
@@ -806,13 +834,15 @@ class SeqStep(GrpoStep):
                 "grpo_seq_terms": R * (m + 12) + n_live * (8 + o + r) + spec.B * 9,
                 "selective_log_softmax_bwd": R * (4 + V * s) + (R - n_zero) * (12 + V * s)}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         spec = self.spec
+        b0, b1, l0, l1 = part
+        assert (l0, l1) == (0, spec.L), "the sequence-level terms need whole sequences"
         lp, lse = rp.selective_log_softmax_fwd(d["logits"], d["idx"], T=spec.T)
         t = rp.grpo_seq_terms(lp, d["adv"], d["dloss"], B=b1 - b0, L=spec.L, beta=spec.beta, eps_low=spec.eps_low,
                               eps_high=spec.eps_high, old_logp=d.get("old"), ref_logp=d.get("ref"), mask=d.get("mask"))
         dl = rp.selective_log_softmax_bwd(d["logits"], d["idx"], t["dlogp"], lse, T=spec.T,
-                                          dlogits=self.dlogits[b0:b1])
+                                          dlogits=self._cut(self.dlogits, "bl", part))
         return {"dlogits": dl, "loss": t["loss"]}
 
 
@@ -845,16 +875,17 @@ class EntropyBwdStep(EntropySlsmStep):
                 "entropy_from_logits_bwd": R * (4 + V * s) + (R - n_zero) * (8 + V * s)}
 
     def e2e_inputs(self):
-        return {"logits": (self.inp.logits, "b"), "up": (self.inp.upstream, "r")}
+        return {"logits": (self.inp.logits, "bl"), "up": (self.inp.upstream, "r")}
 
     def e2e_outputs(self):
-        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "b"),
+        return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "bl"),
                 "entropy": ((self.spec.rows,), torch.float32, "r")}
 
-    def e2e_part(self, d, b0, b1):
+    def e2e_part(self, d, part):
         T = self.spec.T
         H, lse = rp.entropy_from_logits(d["logits"], T=T, return_lse=True)
-        dl = rp.entropy_from_logits_bwd(d["logits"], d["up"], lse, H, T=T, dlogits=self.dlogits[b0:b1])
+        dl = rp.entropy_from_logits_bwd(d["logits"], d["up"], lse, H, T=T,
+                                        dlogits=self._cut(self.dlogits, "bl", part))
         return {"dlogits": dl, "entropy": H}
 
 
@@ -1390,8 +1421,9 @@ def main(argv=None):
         e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4), "steps": Ke,
                "parts": len(step.e2e_bounds),
-               "path": "public Python API, pinned host inputs, outputs copied back; the batch in parts of whole "
-                       "sequences, host->device copies, kernels and device->host copies on three streams"}
+               "path": "public Python API, pinned host inputs, outputs copied back; the batch in parts (whole "
+                       "sequences, or token ranges of one sequence for the token-level passes), the logits copied "
+                       "in, the kernels and the outputs copied out per part on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

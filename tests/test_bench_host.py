@@ -145,3 +145,20 @@ def test_kernel_source_hash_per_entry_point():
     assert hashes["grpo_loss_fwd"] == hashes["entropy_from_logits"] != hashes["grpo_loss_bwd"]
     assert all(len(h) == 16 for h in hashes.values())
     assert bench.measured_traffic("not_an_entry_point", "grpo_b4_l512_v32000") is None
+
+
+def test_e2e_parts_cover_every_row_once():
+    """Parts of the end-to-end path: whole sequences where required or when there are
+    enough sequences, else token ranges of one sequence; together every row exactly once."""
+    for B, L, P, whole in [(4, 512, 16, False), (4, 512, 16, True), (16, 1024, 16, False), (3, 5, 16, False),
+                           (1, 7, 4, False), (20, 3, 16, False)]:
+        parts = bench.e2e_parts(B, L, P, whole)
+        seen = np.zeros(B * L, int)
+        for b0, b1, l0, l1 in parts:
+            assert 0 <= b0 < b1 <= B and 0 <= l0 < l1 <= L
+            assert b1 - b0 == 1 or (l0, l1) == (0, L)      # a token range stays in one sequence
+            if whole:
+                assert (l0, l1) == (0, L)
+            for b in range(b0, b1):
+                seen[b * L + l0:b * L + l1] += 1
+        assert np.all(seen == 1), (B, L, P, whole)
