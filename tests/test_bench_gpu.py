@@ -41,7 +41,7 @@ def _device_outputs(step):
     return out
 
 
-@pytest.mark.parametrize("case", ["grpo", "fused", "seq", "vocab2", "slsm", "entropy_bwd"])
+@pytest.mark.parametrize("case", ["grpo", "grpo_token_ranges", "fused", "seq", "vocab2", "slsm", "entropy_bwd"])
 def test_pipelined_e2e_matches_device_step(case):
     if case in ("slsm", "entropy_bwd"):
         spec = W.get("entropy_slsm_b16_l4096_v32000", L=128)
@@ -50,7 +50,11 @@ def test_pipelined_e2e_matches_device_step(case):
     step = bench.make_step(spec, 0, "cuda", fused=case == "fused", vocab_shards=2 if case == "vocab2" else 0,
                            seq_level=case == "seq", entropy_bwd=case == "entropy_bwd")
     want = _device_outputs(step)
+    if case == "grpo_token_ranges":          # 16 parts: each sequence in four token ranges
+        step.E2E_PART_BYTES = 8 << 20
     step.e2e_setup()
+    if case == "grpo_token_ranges":
+        assert len(step.e2e_bounds) == 16 and all(b1 - b0 == 1 for b0, b1, _, _ in step.e2e_bounds)
     assert len(step.e2e_bounds) > 1
     step.dlogits.fill_(float("nan"))          # the e2e path must write every row again
     step.e2e_step()
