@@ -566,7 +566,7 @@ def run_linear(args):
     tflops = step.flops_per_step / (step_ms * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
-        ms = e2e_run(step, min(K, 10), 2)
+        ms = aggregate_max_ms(e2e_run(step, min(K, 10), 2), world, device)  # the slowest rank
         e2e = {"value": round(spec.rows * world / (ms * 1e-3), 1), "unit": "rows/s", "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4),
                "path": "public Python API, pinned host hidden states and per-row inputs, loss and grad_hidden "
@@ -1416,7 +1416,9 @@ def main(argv=None):
     e2e = None
     if not args.no_e2e:
         Ke = min(K, max(5, int(1500.0 / max(step_ms, 1e-3) / 10)), 200)
-        ms = e2e_run(step, Ke, 2)
+        if world > 1:  # every rank times the same number of steps
+            Ke = int(aggregate_max_ms(float(Ke), world, device))
+        ms = aggregate_max_ms(e2e_run(step, Ke, 2), world, device)  # the slowest rank's time per step
         e2e_val = step_bytes * world / (ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4), "steps": Ke,
