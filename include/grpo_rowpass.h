@@ -68,7 +68,7 @@ typedef struct CUstream_st* grpo_stream_t;
 typedef enum {
   GRPO_OK = 0,
   GRPO_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, bad size, stride, scalar or aliasing */
-  GRPO_ERR_UNSUPPORTED = 2, /* valid arguments this build does not handle (e.g. B*L >= 2^31) */
+  GRPO_ERR_UNSUPPORTED = 2, /* valid arguments the library does not handle (e.g. B*L >= 2^31) */
   GRPO_ERR_CUDA = 3         /* the kernel launch failed */
 } grpo_status;
 

@@ -625,7 +625,7 @@ const char* grpo_status_string(grpo_status status) {
   switch (status) {
     case GRPO_OK: return "GRPO_OK";
     case GRPO_ERR_INVALID_ARG: return "GRPO_ERR_INVALID_ARG: invalid pointer, size, stride, scalar or aliasing";
-    case GRPO_ERR_UNSUPPORTED: return "GRPO_ERR_UNSUPPORTED: valid arguments outside what this build handles";
+    case GRPO_ERR_UNSUPPORTED: return "GRPO_ERR_UNSUPPORTED: valid arguments outside what the library handles";
     case GRPO_ERR_CUDA: return "GRPO_ERR_CUDA: the kernel launch failed";
     default: return "unknown grpo_status";
   }

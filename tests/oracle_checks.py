@@ -25,7 +25,7 @@ import numpy as np
 
 try:
     import mpmath
-except ImportError:  # the GPU machine has no mpmath; long double stands in
+except ImportError:  # without mpmath, long double stands in
     mpmath = None
 
 
