@@ -162,3 +162,13 @@ def test_e2e_parts_cover_every_row_once():
             for b in range(b0, b1):
                 seen[b * L + l0:b * L + l1] += 1
         assert np.all(seen == 1), (B, L, P, whole)
+
+
+def test_fused_row_bytes_classes():
+    """The fused step reads an unmasked row's logits once and writes every row's dlogits."""
+    spec = W.get("grpo_b4_l512_v32000")
+    Vs = spec.V * 2
+    b = bench.fused_row_bytes(spec, np.array([1, 0], bool), has_mask=True, has_old=True, has_ref=True)
+    assert list(b) == [1 + 21 + Vs + Vs + 8 + 4 + 4 + 4, 1 + 21 + Vs]
+    b = bench.fused_row_bytes(spec, np.array([1], bool), has_mask=False, has_old=False, has_ref=False)
+    assert list(b) == [21 + Vs + Vs + 8 + 4]
