@@ -287,6 +287,7 @@ class PipelinedE2E:
     E2E_PARTS = 16               # at most; parts of at least E2E_PART_BYTES of logits
     E2E_PART_BYTES = 32 << 20    # below this the calls' host-side cost outweighs a part's copy time
     E2E_WHOLE_SEQUENCES = False  # True where a part must hold whole sequences
+    E2E_VIEWS = True             # e2e_part takes the part's input views (False: it has its own)
 
     def e2e_setup(self):
         dev = self.inp.logits.device
@@ -303,6 +304,9 @@ class PipelinedE2E:
         n = int(max(1, min(self.E2E_PARTS, (logit_bytes + self.E2E_PART_BYTES // 2) // self.E2E_PART_BYTES)))
         self.e2e_bounds = e2e_parts(self.spec.B, self.spec.L, n, self.E2E_WHOLE_SEQUENCES)
         self.e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
+        # the per-part copy-in views, made once
+        self.e2e_in_views = [[(self._cut(self.d_in[k], "bl", part), self._cut(h, "bl", part))
+                              for k, h in self.h_in.items() if self.lay_in[k] == "bl"] for part in self.e2e_bounds]
 
     def _cut(self, t, lay, part):
         b0, b1, l0, l1 = part
@@ -322,10 +326,9 @@ class PipelinedE2E:
             for k, h in self.h_in.items():  # per-row and per-sequence inputs: once per step
                 if self.lay_in[k] != "bl":
                     self.d_in[k].copy_(h, non_blocking=True)
-            for part in self.e2e_bounds:
-                for k, h in self.h_in.items():
-                    if self.lay_in[k] == "bl":
-                        self._cut(self.d_in[k], "bl", part).copy_(self._cut(h, "bl", part), non_blocking=True)
+            for views in self.e2e_in_views:
+                for dst, src in views:
+                    dst.copy_(src, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(s_in)
                 landed.append(ev)
@@ -333,7 +336,7 @@ class PipelinedE2E:
         with torch.cuda.stream(s_run):
             for part, ev in zip(self.e2e_bounds, landed):
                 s_run.wait_event(ev)
-                d = {k: self._cut(t, self.lay_in[k], part) for k, t in self.d_in.items()}
+                d = {k: self._cut(t, self.lay_in[k], part) for k, t in self.d_in.items()} if self.E2E_VIEWS else None
                 out = self.e2e_part(d, part)
                 ev2 = torch.cuda.Event()
                 ev2.record(s_run)
@@ -365,6 +368,7 @@ class GrpoStep(PipelinedE2E):
     """grpo_loss_fwd (+entropy, kl, is_clipped) then grpo_loss_bwd over one batch."""
 
     oracle_kind = "grpo"
+    E2E_PART_BYTES = 16 << 20  # its e2e calls go through the C ABI (e2e_setup)
 
     def __init__(self, spec, seed, device, inputs=None):
         self.spec = spec
@@ -434,7 +438,43 @@ class GrpoStep(PipelinedE2E):
         return {"dlogits": (tuple(self.dlogits.shape), self.dlogits.dtype, "bl"),
                 "loss": ((self.spec.rows,), torch.float32, "r")}
 
+    def e2e_setup(self):
+        """The Python-API calls cost ~0.1 ms of host time a part; through the C ABI with the
+        outputs allocated once and each part's arguments made here, a part costs a few
+        microseconds, so the batch can be cut into parts of 16 MB."""
+        super().e2e_setup()
+        if type(self).e2e_part is not GrpoStep.e2e_part:
+            return  # a subclass with its own calls
+        spec, R = self.spec, self.spec.rows
+        dev = self.d_in["logits"].device
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.e2e_dev_out = {k: torch.empty(R, **f32) for k in ("loss", "logp", "lse", "kl", "entropy")}
+        self.e2e_dev_out["is_clipped"] = torch.empty(R, dtype=torch.uint8, device=dev)
+        s_run = self.e2e_streams[1].cuda_stream
+        T, beta, el, eh = spec.T, spec.beta, spec.eps_low, spec.eps_high
+        self.e2e_calls = {}
+        for part in self.e2e_bounds:
+            x, dx = self._cut(self.d_in["logits"], "bl", part), self._cut(self.dlogits, "bl", part)
+            xd, dxd = rp.rows_of(x), rp.rows_of(dx)
+            g = lambda k: _p(self._cut(self.d_in[k], self.lay_in[k], part)) if k in self.d_in else None
+            o = {k: self._cut(v, "r", part) for k, v in self.e2e_dev_out.items()}
+            fa = (ctypes.byref(xd), g("idx"), g("old"), g("ref"), g("adv"), g("mask"), T, beta, el, eh, _p(o["loss"]),
+                  _p(o["logp"]), _p(o["lse"]), _p(o["kl"]), _p(o["is_clipped"]), _p(o["entropy"]), None, s_run)
+            ba = (ctypes.byref(xd), g("idx"), g("old"), g("ref"), g("adv"), g("mask"), g("dloss"), _p(o["logp"]),
+                  _p(o["lse"]), T, beta, el, eh, ctypes.byref(dxd), None, s_run)
+            self.e2e_calls[part] = (xd, dxd, fa, ba, {"dlogits": dx, "loss": o["loss"]})
+        self.E2E_VIEWS = False
+
     def e2e_part(self, d, part):
+        if d is None:  # the C-ABI path set up in e2e_setup
+            _, _, fa, ba, out = self.e2e_calls[part]
+            st = self._fwd(*fa)
+            if st:
+                raise rp.GrpoError("grpo_loss_fwd", st)
+            st = self._bwd(*ba)
+            if st:
+                raise rp.GrpoError("grpo_loss_bwd", st)
+            return out
         spec = self.spec
         f = rp.grpo_loss_fwd(d["logits"], d["idx"], d["adv"], T=spec.T, beta=spec.beta, eps_low=spec.eps_low,
                              eps_high=spec.eps_high, old_logp=d.get("old"), ref_logp=d.get("ref"), mask=d.get("mask"),
@@ -448,6 +488,8 @@ class GrpoStep(PipelinedE2E):
 
 class FusedStep(GrpoStep):
     """grpo_loss_fused: forward outputs and dlogits in one kernel (dloss known in advance)."""
+
+    E2E_PART_BYTES = 32 << 20  # public Python API calls per part
 
     def __init__(self, spec, seed, device, inputs=None):
         super().__init__(spec, seed, device, inputs)
@@ -637,6 +679,8 @@ class VocabShardStep(GrpoStep):
     [shards, B*L, 4] buffer, where an all-gather would put it), grpo_vocab_combine, then
     grpo_loss_bwd_vocab_shard on every shard into its columns of dlogits."""
 
+    E2E_PART_BYTES = 32 << 20  # public Python API calls per part
+
     def __init__(self, spec, seed, device, shards, inputs=None):
         super().__init__(spec, seed, device, inputs)
         lib = rp.load_library()
@@ -782,6 +826,8 @@ class SeqStep(GrpoStep):
     """Sequence-level GRPO: selective_log_softmax_fwd (logp, lse), grpo_seq_terms (the
     per-sequence ratio, clip and KL terms and the per-token dlogp), then
     selective_log_softmax_bwd (dlogits; rows whose dlogp is 0 are written without a read)."""
+
+    E2E_PART_BYTES = 32 << 20  # public Python API calls per part
 
     oracle_kind = "seq"
     E2E_WHOLE_SEQUENCES = True
@@ -1423,9 +1469,11 @@ def main(argv=None):
         e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4), "steps": Ke,
                "parts": len(step.e2e_bounds),
-               "path": "public Python API, pinned host inputs, outputs copied back; the batch in parts (whole "
-                       "sequences, or token ranges of one sequence for the token-level passes), the logits copied "
-                       "in, the kernels and the outputs copied out per part on three streams"}
+               "path": ("the C-ABI entry points with outputs allocated once" if not step.E2E_VIEWS else
+                        "the public Python API") +
+                       ", pinned host inputs, outputs copied back; the batch in parts (whole sequences, or token "
+                       "ranges of one sequence for the token-level passes), the logits copied in, the kernels and "
+                       "the outputs copied out per part on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
