@@ -3,13 +3,16 @@
 
 One step = one pass of the whole hot path over one batch of synthetic logits:
 
-* GRPO workloads (default ``grpo_b4_l512_v32000``, the GRPO backward workload of the
-  Liger-Kernel GRPO Loss Backward write-up: (B, L, V, zero-grad%) = (4, 512, 32000, 50%)):
+* GRPO workloads (default ``sweep_b16_l4096_v151936``: B=16, L=4096, V=151936, ~20 GB of
+  bf16 logits, T=0.7, beta=0.04, 8 of 16 sequences with advantage 0 -- the largest of the
+  Qwen3-vocabulary shapes; ``grpo_b4_l512_v32000`` is the GRPO backward workload of the
+  Liger-Kernel GRPO Loss Backward write-up, (B, L, V, zero-grad%) = (4, 512, 32000, 50%)):
   ``grpo_loss_fwd`` (loss, logp, lse, kl, is_clipped, entropy) then ``grpo_loss_bwd``;
   with ``--fused``, the single kernel ``grpo_loss_fused`` (dloss known in advance); with
   ``--seq-level``, the sequence-level form (``selective_log_softmax_fwd``,
   ``grpo_seq_terms``, ``selective_log_softmax_bwd``); with ``--vocab-shards S``, the
-  vocabulary-parallel form with its S shards run one after another.
+  vocabulary-parallel form with its S shards run one after another.  The same line
+  carries ``entropy``: ``entropy_from_logits`` timed alone over the same logits.
 * ``entropy_slsm_b16_l4096_v32000``: ``entropy_from_logits``, ``selective_log_softmax_fwd``
   and ``selective_log_softmax_bwd``; with ``--entropy-bwd``, ``entropy_from_logits`` (with
   lse) and ``entropy_from_logits_bwd``.
@@ -21,8 +24,11 @@ unmasked row's logits read once by the forward; each backward row with a non-zer
 factor read once and written once; each zero row written once; plus the per-row
 scalars), and rows per second.  Inputs are resident in HBM when the timed region
 starts; L2 is flushed (a 256 MB write, then a 256 MB read so no dirty lines remain)
-before every timed step and the flush is not timed.  ``e2e`` repeats the measurement through the public Python API with the inputs
-in pinned host memory and the outputs copied back, copies inside the timed region.
+before every timed step and the flush is not timed.  ``e2e`` repeats the measurement
+through the C-ABI entry points with the inputs in pinned host memory and the outputs
+copied back, copies inside the timed region.  ``cpu_baseline`` (and ``--impl
+reference``) time the fp64 oracle on the host cores over one fixed seeded slice of
+2048 rows of the same workload: warm-up runs, then the median of the timed runs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -42,6 +48,7 @@ import statistics
 import subprocess
 import sys
 import time
+import weakref
 
 import numpy as np
 import torch
@@ -271,6 +278,51 @@ SLSM_ROW_BYTES = {"entropy_from_logits": lambda V, s: V * s + 4,
                   "selective_log_softmax_bwd": lambda V, s: 2 * V * s + 8 + 4 + 4}
 
 
+def _unregister_host(ptr):
+    torch.cuda.cudart().cudaHostUnregister(ptr)
+
+
+def pinned_host(shape, dtype, src=None):
+    """A page-locked host tensor of exactly this size (torch's pinned allocator rounds each
+    block up to a power of two: 32 GB for the 20 GB logits), filled from ``src`` if given.
+    The pages are registered with cudaHostRegister and released when the tensor goes."""
+    t = torch.empty(shape, dtype=dtype)
+    nbytes = t.numel() * t.element_size()
+    if nbytes and int(torch.cuda.cudart().cudaHostRegister(t.data_ptr(), nbytes, 0)) == 0:
+        weakref.finalize(t, _unregister_host, t.data_ptr())
+    elif nbytes:
+        t = t.pin_memory()
+    if src is not None:
+        t.copy_(src)
+    return t
+
+
+def host_memory_available() -> int:
+    """Bytes this process may still take: MemAvailable, capped by the cgroup's limit."""
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    for lim_p, use_p in (("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory.current"),
+                         ("/sys/fs/cgroup/memory/memory.limit_in_bytes", "/sys/fs/cgroup/memory/memory.usage_in_bytes")):
+        try:
+            with open(lim_p) as f:
+                lim = f.read().strip()
+            with open(use_p) as f:
+                use = int(f.read().strip())
+            if lim != "max" and int(lim) < (1 << 60):
+                left = int(lim) - use
+                avail = left if avail is None else min(avail, left)
+            break
+        except (OSError, ValueError):
+            continue
+    return avail if avail is not None else 1 << 62
+
+
 class PipelinedE2E:
     """End-to-end through the public API with host buffers.  The batch is cut into parts: a
     part is a group of whole sequences, or, for the token-level passes when there are
@@ -292,11 +344,20 @@ class PipelinedE2E:
     def e2e_setup(self):
         dev = self.inp.logits.device
         ins = {k: v for k, v in self.e2e_inputs().items() if v[0] is not None}
-        self.h_in = {k: t.detach().contiguous().cpu().pin_memory() for k, (t, _) in ins.items()}
+        outs = self.e2e_outputs()
+        # the step's per-element outputs (dlogits) come back too when the host has room for
+        # them beside the inputs; else only the per-row results (loss ...) do
+        nb = lambda shape, dt: math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        in_bytes = sum(t.numel() * t.element_size() for t, _ in ins.values())
+        out_bytes = sum(nb(shape, dt) for shape, dt, _ in outs.values())
+        self.e2e_outputs_kept = "all"
+        if in_bytes + out_bytes > 0.5 * host_memory_available():
+            outs = {k: v for k, v in outs.items() if v[2] != "bl"}
+            self.e2e_outputs_kept = "per-row results only (the host has no room for the per-element outputs)"
+        self.h_in = {k: pinned_host(t.shape, t.dtype, src=t) for k, (t, _) in ins.items()}
         self.d_in = {k: torch.empty(t.shape, dtype=t.dtype, device=dev) for k, (t, _) in ins.items()}
         self.lay_in = {k: lay for k, (_, lay) in ins.items()}
-        outs = self.e2e_outputs()
-        self.h_out = {k: torch.empty(shape, dtype=dt).pin_memory() for k, (shape, dt, _) in outs.items()}
+        self.h_out = {k: pinned_host(shape, dt) for k, (shape, dt, _) in outs.items()}
         self.lay_out = {k: lay for k, (_, _, lay) in outs.items()}
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
         self.d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
@@ -345,6 +406,8 @@ class PipelinedE2E:
             for part, (ev, out) in zip(self.e2e_bounds, done):
                 s_out.wait_event(ev)
                 for k, t in out.items():
+                    if k not in self.h_out:
+                        continue
                     t.record_stream(s_out)  # allocated on s_run, read here
                     self._cut(self.h_out[k], self.lay_out[k], part).copy_(t, non_blocking=True)
         main.wait_stream(s_out)
@@ -633,7 +696,7 @@ def run_linear(args):
                              "flops_per_step": int(step.flops_per_step)},
                 "memory": {"workspace_bytes": int(step.ws.numel()), "full_batch_logits_bytes_bf16": int(full_logits),
                            "full_batch_logits_and_dlogits_bytes_bf16": int(2 * full_logits)},
-                "cpu_baseline": cpu, "e2e": e2e,
+                "cpu_baseline": cpu, "e2e": e2e, "entropy": ent,
                 "gpu_launches": step.launches_per_step * K,
                 "gpu_launches_note": "per chunk: 3 cuBLASLt GEMMs (library kernels) and 1 row-pass kernel",
                 "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
@@ -1038,6 +1101,42 @@ def e2e_run(step, K, Wm):
     return s.elapsed_time(e) / K
 
 
+def entropy_run(step, K, Wm, flush_buf, peak):
+    """entropy_from_logits alone over the step's logits (the row pass's entropy kernel,
+    reading each row once): Wm untimed launches, then K launches with L2 flushed before
+    each and CUDA events around each, on the launching stream."""
+    lib = rp.load_library()
+    spec = step.spec
+    R = spec.rows
+    ent = torch.empty(R, dtype=torch.float32, device=step.inp.idx.device)
+    args = (ctypes.byref(step.x_desc), spec.T, _p(ent), None, step.stream)
+
+    def call():
+        st = lib.entropy_from_logits(*args)
+        if st:
+            raise rp.GrpoError("entropy_from_logits", st)
+
+    for i in range(Wm):
+        flush_buf(i)
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush_buf(i + 1)
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = R * SLSM_ROW_BYTES["entropy_from_logits"](spec.V, spec.elem_size)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    traffic = measured_traffic("entropy_from_logits", spec.name)
+    return {"kernel": "entropy_from_logits", "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 5),
+            "bytes": int(nbytes), "rows_per_s": round(R / (ms * 1e-3), 1), "hbm_frac": round(gbs / peak, 4),
+            "launches": K, "traffic": traffic,
+            "dram_frac": None if traffic is None else round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -1060,15 +1159,6 @@ def oracle_sample(step, rows):
     if step.oracle_kind == "seq":
         smp["adv_seq"] = inp.adv.cpu().double().numpy()[np.asarray(rows)[::spec.L] // spec.L]
     return smp
-
-
-def sample_units(spec, kind, n, seed):
-    """Rows of a bounded oracle sample: n rows, or for the sequence-level step whole
-    sequences (its ratio is a sum over a sequence) of about n rows in total."""
-    if kind != "seq":
-        return W.sample_rows(spec.rows, n, seed)
-    seqs = W.sample_rows(spec.B, max(1, -(-n // spec.L)), seed)
-    return (seqs[:, None] * spec.L + np.arange(spec.L)[None, :]).reshape(-1)
 
 
 def oracle_step(spec, smp, kind):
@@ -1102,27 +1192,78 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+ORACLE_ROWS = 2048  # rows of the fixed oracle sample
+# The workers' first runs over a sample are slower (1.8, 1.4, 1.2 s on 16 Grace cores for
+# the 2048 rows at V = 151936), so the cpu_baseline leg takes as many warm-up runs as the
+# default reference arm before its median.
+ORACLE_WARMUP, ORACLE_REPEATS = 5, 7
+
+
+def oracle_slice(spec, kind, n=ORACLE_ROWS, seed=11):
+    """The fixed seeded slice of rows the oracle is timed on: n consecutive rows starting at
+    a seeded multiple of n, or for the sequence-level pass (its ratio is a sum over a
+    sequence) the whole sequences of about n rows starting at a seeded sequence."""
+    R, L = spec.rows, spec.L
+    rng = np.random.default_rng(seed)
+    if kind == "seq":
+        nseq = max(1, min(spec.B, -(-n // L)))
+        b0 = int(rng.integers(0, spec.B // nseq)) * nseq
+        return np.arange(b0 * L, (b0 + nseq) * L, dtype=np.int64)
+    n = min(n, R)
+    r0 = int(rng.integers(0, R // n)) * n
+    return np.arange(r0, r0 + n, dtype=np.int64)
+
+
+def sample_bytes(spec, kind, smp):
+    """Minimal bytes of the timed pass over the sample's rows (the same accounting as the
+    GPU step's, with the row classes read off the oracle's own results)."""
+    import oracle
+    n = len(smp["idx"])
+    V, s = spec.V, spec.elem_size
+    if kind == "entropy_bwd":
+        return n * (V * s + 8) + n * (4 + V * s) + int((smp["up"] != 0).sum()) * (8 + V * s)
+    if kind == "slsm":
+        return n * sum(f(V, s) for f in SLSM_ROW_BYTES.values())
+    live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
+    lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
+    if kind == "seq":
+        t = oracle.grpo_seq_terms(lp, smp["old"], smp["ref"], smp["adv_seq"], smp["mask"], smp["dloss"],
+                                  n // spec.L, spec.L, spec.beta, spec.eps_low, spec.eps_high)
+        m, o, r = (smp["mask"] is not None), 4 * (smp["old"] is not None), 4 * (smp["ref"] is not None)
+        nz = int((t["dlogp"] != 0).sum())
+        return (n * (V * s + 16) + n * (m + 12) + int(live.sum()) * (8 + o + r) + (n // spec.L) * 9
+                + n * (4 + V * s) + nz * (12 + V * s))
+    g = oracle.grpo_dlogp(lp, smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.beta, spec.eps_low,
+                          spec.eps_high) * smp["dloss"]
+    f, b = grpo_row_bytes(spec, live, g == 0, smp["mask"] is not None, smp["old"] is not None,
+                          smp["ref"] is not None)
+    return int(f.sum() + b.sum())
+
+
 def _oracle_worker(conn, spec, kind):
-    """One host core's share of an oracle sample: receive the rows, report ready, run
-    oracle_step when told to, send back the time it took; None ends the worker."""
+    """One host core's share of an oracle sample: keep the part it is sent (a dict), run
+    oracle_step on it at every "go" and send back the time it took; None ends the worker."""
     import oracle  # noqa: F401  (imported before any timing)
+    part = None
     while True:
-        smp = conn.recv()
-        if smp is None:
+        msg = conn.recv()
+        if msg is None:
             return
-        conn.send("ready")
-        conn.recv()
+        if isinstance(msg, dict):
+            part = msg
+            conn.send("ready")
+            continue
         t = time.perf_counter()
-        oracle_step(spec, smp, kind)
+        oracle_step(spec, part, kind)
         conn.send(time.perf_counter() - t)
-        del smp
 
 
 class OraclePool:
     """The oracle on several host cores: spawned worker processes (one per core, one numpy
     thread each) run oracle_step, unchanged, on disjoint parts of one sample (whole
-    sequences for the sequence-level pass).  The rows are handed over before the clock
-    starts; the time is the wall time from the start signal until the last part is done."""
+    sequences for the sequence-level pass).  The parts are handed over once, before any
+    clock starts; a run's time is the wall time from the start signal until the last part
+    is done."""
 
     _THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 
@@ -1132,7 +1273,7 @@ class OraclePool:
         saved = {k: os.environ.get(k) for k in self._THREAD_VARS}
         for k in self._THREAD_VARS:
             os.environ[k] = "1"
-        self.spec, self.kind, self.conns, self.procs = spec, kind, [], []
+        self.spec, self.kind, self.conns, self.procs, self.active = spec, kind, [], [], []
         try:
             for _ in range(n):
                 a, b = ctx.Pipe()
@@ -1166,20 +1307,23 @@ class OraclePool:
             parts.append(part)
         return parts
 
-    def run(self, smp):
-        """Wall seconds for the whole sample over the workers, and the number of workers used."""
+    def load(self, smp):
+        """Hand the sample's parts to the workers (untimed)."""
         parts = self.split(smp)
-        conns = self.conns[:len(parts)]
-        for c, part in zip(conns, parts):
+        self.active = self.conns[:len(parts)]
+        for c, part in zip(self.active, parts):
             c.send(part)
-        for c in conns:
+        for c in self.active:
             assert c.recv() == "ready"
+
+    def go(self):
+        """Wall seconds of one run of the loaded sample over the workers."""
         t = time.perf_counter()
-        for c in conns:
+        for c in self.active:
             c.send("go")
-        for c in conns:
+        for c in self.active:
             c.recv()
-        return time.perf_counter() - t, len(parts)
+        return time.perf_counter() - t
 
     def close(self):
         for c in self.conns:
@@ -1188,35 +1332,64 @@ class OraclePool:
             p.join(timeout=30)
 
 
-def cpu_baseline(step, bytes_per_row, budget_s=12.0):
-    """Time the oracle, as it stands, on a bounded sample of rows of this workload: on one
-    core, then the same sample over all host cores (OraclePool)."""
-    spec, kind = step.spec, step.oracle_kind
+def time_oracle(spec, kind, smp, warmup=1, repeats=3):
+    """The oracle over one sample on all host cores, timed the one way both the
+    cpu_baseline and the reference arm use: the sample handed to the workers, `warmup`
+    untimed runs, then `repeats` timed runs.  Returns (median seconds, cores used, times)."""
     cores = host_cores()
-    pool = OraclePool(cores, spec, kind) if cores > 1 else None  # spawned now, ready by the time it is used
-    probe = sample_units(spec, kind, 16, 7)
-    smp = oracle_sample(step, probe)
+    if cores <= 1:
+        times = []
+        for i in range(warmup + repeats):
+            t = time.perf_counter()
+            oracle_step(spec, smp, kind)
+            times.append(time.perf_counter() - t)
+        return statistics.median(times[warmup:]), 1, times[warmup:]
+    pool = OraclePool(cores, spec, kind)
+    try:
+        pool.load(smp)
+        for _ in range(warmup):
+            pool.go()
+        times = [pool.go() for _ in range(repeats)]
+        return statistics.median(times), len(pool.active), times
+    finally:
+        pool.close()
+
+
+def one_core_figure(spec, kind, smp, budget_s=8.0):
+    """The oracle on this process's one thread over the sample's leading rows (whole
+    sequences for the sequence-level pass), as many as fit in about budget_s."""
+    unit = spec.L if kind == "seq" else 1
+    n = len(smp["idx"])
+    cut = lambda k: {key: (v if v is None or np.ndim(v) == 0 else (v[:k // unit] if key == "adv_seq" else v[:k]))
+                     for key, v in smp.items()}
+    probe = cut(min(n, max(unit, 8)))
     t = time.perf_counter()
-    oracle_step(spec, smp, kind)
-    per_row = (time.perf_counter() - t) / len(probe)
-    n = int(max(16, min(spec.rows, budget_s / max(per_row, 1e-9))))
-    rows = sample_units(spec, kind, n, 11)
+    oracle_step(spec, probe, kind)
+    per_row = (time.perf_counter() - t) / len(probe["idx"])
+    k = max(unit, min(n, int(budget_s / max(per_row, 1e-9)) // unit * unit))
+    sub = cut(k)
+    t = time.perf_counter()
+    oracle_step(spec, sub, kind)
+    dt = time.perf_counter() - t
+    return {"value": round(sample_bytes(spec, kind, sub) / dt / 1e9, 6), "cores": 1,
+            "rows_per_s": round(len(sub["idx"]) / dt, 2), "rows": len(sub["idx"]), "seconds": round(dt, 2)}
+
+
+def cpu_baseline(step):
+    """The oracle, as it stands, on the fixed seeded slice of this workload's rows, on all
+    host cores (time_oracle), with a one-core figure beside it."""
+    spec, kind = step.spec, step.oracle_kind
+    rows = oracle_slice(spec, kind)
     smp = oracle_sample(step, rows)
-    t = time.perf_counter()
-    oracle_step(spec, smp, kind)
-    dt1 = time.perf_counter() - t
-    one = {"value": round(bytes_per_row * len(rows) / dt1 / 1e9, 6), "cores": 1, "rows_per_s": round(len(rows) / dt1, 2),
-           "seconds": round(dt1, 2)}
-    dt, used = dt1, 1
-    if pool is not None:
-        try:
-            dt, used = pool.run(smp)
-        finally:
-            pool.close()
-    return {"value": round(bytes_per_row * len(rows) / dt / 1e9, 6), "unit": "GB/s", "cores": used,
-            "kind": "oracle", "rows_per_s": round(len(rows) / dt, 2), "one_core": one,
-            "sample": f"{len(rows)} of {spec.rows} rows of {spec.name} ({kind} fwd+bwd, fp64 numpy), split over "
-                      f"{used} spawned processes of one thread each: {dt:.2f} s (one thread: {dt1:.1f} s)"}
+    nbytes = sample_bytes(spec, kind, smp)
+    one = one_core_figure(spec, kind, smp)
+    dt, used, times = time_oracle(spec, kind, smp, warmup=ORACLE_WARMUP, repeats=ORACLE_REPEATS)
+    return {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "rows_per_s": round(len(rows) / dt, 2), "one_core": one,
+            "seconds": [round(t, 3) for t in times],
+            "sample": f"rows [{rows[0]}, {rows[-1] + 1}) of {spec.rows} of {spec.name} ({kind} fwd+bwd, fp64 "
+                      f"numpy), split over {used} spawned processes of one thread each; {ORACLE_WARMUP} warm-up "
+                      f"runs, then the median of {len(times)}: {dt:.2f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -1229,7 +1402,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 2 s of steps)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="grpo_b4_l512_v32000",
+    ap.add_argument("--workload", default="sweep_b16_l4096_v151936",
                     choices=list(GRPO_WORKLOADS) + ["entropy_slsm_b16_l4096_v32000", LINEAR_WORKLOAD])
     ap.add_argument("--chunk-rows", type=int, default=2048,
                     help="rows per chunk of the LM-head workload (grpo_fused_linear)")
@@ -1266,8 +1439,9 @@ def base_line(args, spec, world):
 
 def run_reference(args):
     """The oracle as the reference arm, on the host cores only: inputs drawn on the CPU
-    from the same generators, old/ref placed with the oracle's own logp, and each step
-    one bounded sample of the workload's rows (fwd + bwd)."""
+    from the same generators (only the sampled rows' logits), old/ref placed with the
+    oracle's own logp, and each step one run of the fixed seeded slice of the workload's
+    rows (fwd + bwd), timed as cpu_baseline times it."""
     rank, world, local = dist_env()
     if rank != 0:
         return 0
@@ -1275,91 +1449,40 @@ def run_reference(args):
     if args.workload == LINEAR_WORKLOAD:
         return run_reference_linear(args, oracle)
     spec = make_spec(args)
-    inp = W.generate(spec, args.seed, device="cpu")
-    R, L = spec.rows, spec.L
-    grpo = not spec.name.startswith("entropy_slsm")
     kind = step_kind(args, spec)
-    adv_rows = oracle.per_row(inp.adv.numpy(), L)
-
-    def sample(rows):
-        x = inp.logits.reshape(-1, spec.V) if not spec.strided else inp.logits[rows // L, rows % L]
-        x = x[rows] if not spec.strided else x
-        xd = oracle.bf16_bits_to_fp64(x.view(torch.int16).numpy().view(np.uint16)) if x.dtype == torch.bfloat16 \
-            else x.double().numpy()
-        smp = {"x": xd, "idx": inp.idx.numpy()[rows], "adv": adv_rows[rows],
-               "mask": None if inp.mask is None else inp.mask.numpy()[rows]}
-        if grpo:
-            lp, _ = oracle.selective_log_softmax(xd, smp["idx"], spec.T)
-            add = lambda off: None if off is None else oracle.round_to_fp32(lp + off.numpy()[rows]).astype(np.float64)
-            smp["old"] = add(inp.old_offset)
-            smp["ref"] = add(inp.ref_offset) if spec.beta != 0 else None
-            smp["dloss"] = inp.dloss.numpy().astype(np.float64)[rows]
-        else:
-            smp["up"] = inp.upstream.numpy().astype(np.float64)[rows]
-        if kind == "seq":
-            smp["adv_seq"] = inp.adv.numpy().astype(np.float64)[rows[::L] // L]
-        return smp
-
-    def sample_bytes(smp):
-        n = len(smp["idx"])
-        V, s = spec.V, spec.elem_size
-        if kind == "entropy_bwd":
-            return n * (V * s + 8) + n * (4 + V * s) + int((smp["up"] != 0).sum()) * (8 + V * s)
-        if not grpo:
-            return n * sum(f(V, s) for f in SLSM_ROW_BYTES.values())
-        if kind == "seq":
-            live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
-            lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
-            t = oracle.grpo_seq_terms(lp, smp["old"], smp["ref"], smp["adv_seq"], smp["mask"], smp["dloss"],
-                                      n // L, L, spec.beta, spec.eps_low, spec.eps_high)
-            m, o, r = (smp["mask"] is not None), 4 * (smp["old"] is not None), 4 * (smp["ref"] is not None)
-            nz = int((t["dlogp"] != 0).sum())
-            return (n * (V * s + 16) + n * (m + 12) + int(live.sum()) * (8 + o + r) + (n // L) * 9
-                    + n * (4 + V * s) + nz * (12 + V * s))
-        live = np.ones(n, bool) if smp["mask"] is None else smp["mask"] != 0
-        lp, _ = oracle.selective_log_softmax(smp["x"], smp["idx"], spec.T)
-        g = oracle.grpo_dlogp(lp, smp["old"], smp["ref"], smp["adv"], smp["mask"], spec.beta, spec.eps_low,
-                              spec.eps_high) * smp["dloss"]
-        f, b = grpo_row_bytes(spec, live, g == 0, smp["mask"] is not None, smp["old"] is not None,
-                              smp["ref"] is not None)
-        return int(f.sum() + b.sum())
+    inp = W.generate(spec, args.seed, device="cpu", with_logits=False)
+    L = spec.L
+    grpo = kind in ("grpo", "seq")
+    rows = oracle_slice(spec, kind)
+    x = W.logits_rows(spec, args.seed, int(rows[0]), int(rows[-1]) + 1)
+    xd = oracle.bf16_bits_to_fp64(x.view(torch.int16).numpy().view(np.uint16)) if x.dtype == torch.bfloat16 \
+        else x.double().numpy()
+    del x
+    smp = {"x": xd, "idx": inp.idx.numpy()[rows], "adv": oracle.per_row(inp.adv.numpy(), L)[rows],
+           "mask": None if inp.mask is None else inp.mask.numpy()[rows]}
+    if grpo:
+        lp, _ = oracle.selective_log_softmax(xd, smp["idx"], spec.T)
+        add = lambda off: None if off is None else oracle.round_to_fp32(lp + off.numpy()[rows]).astype(np.float64)
+        smp["old"] = add(inp.old_offset)
+        smp["ref"] = add(inp.ref_offset) if spec.beta != 0 else None
+        smp["dloss"] = inp.dloss.numpy().astype(np.float64)[rows]
+    else:
+        smp["up"] = inp.upstream.numpy().astype(np.float64)[rows]
+    if kind == "seq":
+        smp["adv_seq"] = inp.adv.numpy().astype(np.float64)[rows[::L] // L]
 
     K = args.steps if args.steps is not None else 10
     Wm = args.warmup
-    cores = host_cores()
-    pool = OraclePool(cores, spec, kind) if cores > 1 else None
-    probe_rows = sample_units(spec, kind, 8, 3)
-    probe = sample(probe_rows)
-    t = time.perf_counter()
-    oracle_step(spec, probe, kind)
-    per_row = (time.perf_counter() - t) / len(probe_rows)
-    held = max(1, int(2e9 // (spec.V * 8)))  # fp64 rows of one step's sample held at once
-    rows_per_step = int(max(1, min(R, held, 150.0 * cores / max(1, K + Wm) / max(per_row, 1e-9))))
-    times, nbytes, nrows, used = [], 0, 0, 1
-    try:
-        for i in range(Wm + K):
-            smp = sample(sample_units(spec, kind, rows_per_step, 100 + i))
-            if pool is not None:
-                dt, used = pool.run(smp)
-            else:
-                t = time.perf_counter()
-                oracle_step(spec, smp, kind)
-                dt = time.perf_counter() - t
-            if i >= Wm:
-                times.append(dt)
-                nbytes += sample_bytes(smp)
-                nrows += len(smp["idx"])
-    finally:
-        if pool is not None:
-            pool.close()
-    total = sum(times)
-    value = nbytes / total / 1e9
+    nbytes = sample_bytes(spec, kind, smp)
+    med, used, times = time_oracle(spec, kind, smp, warmup=max(1, Wm), repeats=max(1, K))
+    value = nbytes / med / 1e9
     line = base_line(args, spec, 1)
     line.update({"impl": "reference", "value": round(value, 6), "steps": K, "warmup": Wm,
-                 "ms_per_step": round(1e3 * total / K, 3), "dtype": "f64",
-                 "rows_per_s": round(nrows / total, 2)})
-    sample_txt = (f"{nrows // K} of {R} rows of {spec.name} per step ({kind} fwd+bwd, fp64 numpy), split over "
-                  f"{used} spawned processes of one thread each")
+                 "ms_per_step": round(1e3 * med, 3), "dtype": "f64",
+                 "rows_per_s": round(len(rows) / med, 2)})
+    sample_txt = (f"rows [{rows[0]}, {rows[-1] + 1}) of {spec.rows} of {spec.name} per step ({kind} fwd+bwd, "
+                  f"fp64 numpy), split over {used} spawned processes of one thread each; the median of "
+                  f"{len(times)} steps after {max(1, Wm)} warm-up")
     line["cpu_baseline"] = {"value": line["value"], "unit": "GB/s", "cores": used, "kind": "oracle",
                             "sample": sample_txt}
     line["e2e"] = {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
@@ -1468,16 +1591,20 @@ def main(argv=None):
         e2e_val = step_bytes * world / (ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": int(step.h2d),
                "d2h_bytes_per_step": int(step.d2h), "ms_per_step": round(ms, 4), "steps": Ke,
-               "parts": len(step.e2e_bounds),
+               "parts": len(step.e2e_bounds), "outputs_copied_back": step.e2e_outputs_kept,
                "path": ("the C-ABI entry points with outputs allocated once" if not step.E2E_VIEWS else
                         "the public Python API") +
                        ", pinned host inputs, outputs copied back; the batch in parts (whole sequences, or token "
                        "ranges of one sequence for the token-level passes), the logits copied in, the kernels and "
                        "the outputs copied out per part on three streams"}
 
+    ent = None
+    if step_kind(args, spec) == "grpo" and not args.vocab_shards:
+        ent = entropy_run(step, K, Wm, flush_buf, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(step, step_bytes / spec.rows)
+        cpu = cpu_baseline(step)
 
     if rank == 0:
         line = base_line(args, spec, world)
@@ -1491,10 +1618,12 @@ def main(argv=None):
                             "GB_per_s": round(per_launch[n] / (kern_ms[n] * 1e-3) / 1e9, 1)} for n in kern_ms},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "dram_frac": None if traffic is None else
+                         round(traffic / (kern_ms[dom] * 1e-3) / 1e9 / peak, 4),
                          "source_hash": kernel_source_hash(dom) if dom in KERNEL_UNITS else None,
                          "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": int(per_launch[dom])},
-            "cpu_baseline": cpu, "e2e": e2e,
+            "cpu_baseline": cpu, "e2e": e2e, "entropy": ent,
             "gpu_launches": getattr(step, "launches_per_step", len(step.kernels)) * K,
             "gpu_launches_note": "in the headline pass (the per-kernel pass launches as many again)",
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],

@@ -22,17 +22,27 @@
 namespace grpo {
 namespace {
 
-// Per-row factor g of the GRPO loss of an unmasked token from its logp (fp32, same
-// operation order as the definition).
-__device__ __forceinline__ float grpo_factor(float logp, const float* old_logp, const float* ref_logp, float A,
-                                             float dloss, float beta, float lo, float hi, float T, int64_t r) {
-  const float ratio = old_logp ? expf(logp - old_logp[r]) : 1.f;
+// Per-row factor g of the GRPO loss of an unmasked token from its scalars (fp32, same
+// operation order as the definition): d(pg + kl)/dlogp * dloss / T.  This is the one body
+// of the formula; the backward, fused and LM-head kernels all call it.
+__device__ __forceinline__ float grpo_factor_of(float logp, float old, bool has_old, float ref, float A,
+                                                float dloss, float beta, float lo, float hi, float T) {
+  const float ratio = has_old ? expf(logp - old) : 1.f;
   const float clipped = ratio < lo ? lo : (ratio > hi ? hi : ratio);
   // unclipped branch is the minimum (ties included): d(-ratio*A)/dlogp; else constant
   const float dpg = (ratio * A <= clipped * A) ? -A * ratio : 0.f;
   float dkl = 0.f;
-  if (beta != 0.f) dkl = -beta * expm1f(ref_logp[r] - logp);  // beta (1 - e^(ref - logp))
+  if (beta != 0.f) dkl = -beta * expm1f(ref - logp);  // beta (1 - e^(ref - logp))
   return (dpg + dkl) * dloss / T;
+}
+
+// The same factor with old/ref read from their arrays (NULL old: ratio 1; ref is read
+// only when beta != 0).
+__device__ __forceinline__ float grpo_factor(float logp, const float* old_logp, const float* ref_logp, float A,
+                                             float dloss, float beta, float lo, float hi, float T, int64_t r) {
+  const float old = old_logp ? old_logp[r] : logp;
+  const float ref = beta != 0.f ? ref_logp[r] : 0.f;
+  return grpo_factor_of(logp, old, old_logp != nullptr, ref, A, dloss, beta, lo, hi, T);
 }
 
 // All of a row's scalars are loaded before any of them is used, so the row waits for
@@ -47,12 +57,7 @@ __device__ __forceinline__ float grpo_row_factor(const BwdParams& p, int64_t r, 
   const float dloss = p.dloss[r];
   kept = live && !(p.beta == 0.f && A == 0.f);
   if (!live) return 0.f;
-  const float ratio = p.old_logp ? expf(logp - old) : 1.f;
-  const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
-  const float dpg = (ratio * A <= clipped * A) ? -A * ratio : 0.f;
-  float dkl = 0.f;
-  if (p.beta != 0.f) dkl = -p.beta * expm1f(ref - logp);  // beta (1 - e^(ref - logp))
-  return (dpg + dkl) * dloss / p.T;
+  return grpo_factor_of(logp, old, p.old_logp != nullptr, ref, A, dloss, p.beta, p.lo, p.hi, p.T);
 }
 
 // The part of a row one CTA handles: vectors [v0, v1), plus the scalar head and tail.

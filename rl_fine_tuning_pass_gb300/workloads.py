@@ -22,7 +22,8 @@ Workloads (the shapes and distributions of the pages' benchmarks):
 * ``grpo_qwen3_b16_l1024_v151936``  B=16 (4 prompts x 4 completions), L=1024,
                            V=151936 (a Qwen3-0.6B-shaped LM head, no weights).
 * ``sweep_b16_l4096_v151936``       B=16, L=4096, V=151936 (~20 GB bf16 logits),
-                           beta and the zero-advantage fraction swept.
+                           T=0.7; beta (0.04 by default, or 0) and the zero-advantage
+                           fraction (8 of 16 sequences by default) swept.
 * ``linear_qwen3_b16_l1024_h1024_v151936``  the Qwen3-shaped GRPO batch above given as
                            hidden states [B*L, H=1024] and an LM-head weight [V, H]
                            (Qwen3-0.6B's hidden size), bf16, for the loss on top of the
@@ -43,8 +44,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-__all__ = ["WorkloadSpec", "WORKLOADS", "get", "Inputs", "generate", "LinearInputs", "generate_linear",
-           "sample_rows"]
+__all__ = ["WorkloadSpec", "WORKLOADS", "get", "Inputs", "generate", "logits_rows", "LinearInputs",
+           "generate_linear", "sample_rows"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -105,7 +106,7 @@ WORKLOADS = {
         old_sigma=0.15, ref_sigma=0.05, group_size=4, H=1024),
     "sweep_b16_l4096_v151936": WorkloadSpec(
         "sweep_b16_l4096_v151936", B=16, L=4096, V=151936, dtype="bf16", sigma=2.0, T=0.7,
-        beta=0.0, eps_low=0.2, eps_high=0.2, adv="sweep", mask="none",
+        beta=0.04, eps_low=0.2, eps_high=0.2, adv="sweep", mask="none",
         old_sigma=0.05, ref_sigma=0.05, zero_adv_seqs=8),
 }
 
@@ -129,7 +130,7 @@ def _gen(seed: int, what: str, device="cpu", chunk: int = 0) -> torch.Generator:
 @dataclasses.dataclass
 class Inputs:
     spec: WorkloadSpec
-    logits: torch.Tensor               # [B, L, V] (possibly a strided view), bf16 or fp32
+    logits: Optional[torch.Tensor]     # [B, L, V] (possibly a strided view), bf16 or fp32; None if not drawn
     idx: torch.Tensor                  # [B*L] int64
     adv: torch.Tensor                  # [B] fp32
     mask: Optional[torch.Tensor]       # [B*L] uint8, or None (all tokens count)
@@ -242,25 +243,67 @@ def _row_inputs(spec: WorkloadSpec, seed: int):
     return adv, mask, dloss, old_offset, ref_offset, upstream, lengths
 
 
-def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", rows_per_chunk: int = 4096) -> Inputs:
+def _idx(spec: WorkloadSpec, seed: int) -> torch.Tensor:
+    return torch.randint(0, spec.V, (spec.rows,), generator=_gen(seed, "idx"), dtype=torch.int64)
+
+
+def _peaks(spec: WorkloadSpec, seed: int, idx: torch.Tensor):
+    """Rows (sorted) and columns of the peaked logits: a seeded choice of
+    round(peaked_frac * R) rows; even-numbered peaked rows are peaked on the sampled token,
+    odd ones on a random column."""
+    R, V = spec.rows, spec.V
+    gp = _gen(seed, "peak")
+    n_peak = int(round(spec.peaked_frac * R))
+    rows = torch.sort(torch.randperm(R, generator=gp)[:n_peak]).values
+    cols_rand = torch.randint(0, V, (n_peak,), generator=gp, dtype=torch.int64)
+    cols = torch.where(torch.arange(n_peak) % 2 == 0, idx.cpu()[rows], cols_rand)
+    return rows, cols
+
+
+def logits_rows(spec: WorkloadSpec, seed: int, r0: int, r1: int, device="cpu",
+                rows_per_chunk: int = 4096) -> torch.Tensor:
+    """Rows [r0, r1) of the [B*L, V] logits, with the values ``generate`` gives them on the
+    same device type, drawing only the generator chunks that hold them (a bounded sample of
+    a batch too large to draw whole on the host)."""
+    B, L, V = spec.B, spec.L, spec.V
+    Lp = L + 1 if spec.strided else L
+    dev_type = torch.device(device).type
+    flat = torch.arange(r0, r1, dtype=torch.int64)
+    base_rows = (flat // L) * Lp + flat % L  # rows of the [B*Lp, V] buffer
+    out = torch.empty((r1 - r0, V), dtype=_torch_dtype(spec.dtype), device=device)
+    lo, hi = int(base_rows[0]) if len(flat) else 0, int(base_rows[-1]) + 1 if len(flat) else 0
+    for c in range(lo // rows_per_chunk, (hi + rows_per_chunk - 1) // rows_per_chunk):
+        c0, c1 = c * rows_per_chunk, min(B * Lp, (c + 1) * rows_per_chunk)
+        g = _gen(seed, "logits", dev_type, chunk=c)
+        blk = torch.randn((c1 - c0, V), generator=g, device=device, dtype=torch.float32)
+        blk.mul_(spec.sigma)
+        sel = (base_rows >= c0) & (base_rows < c1)
+        if bool(sel.any()):
+            out[sel.to(out.device)] = blk[(base_rows[sel] - c0).to(blk.device)].to(out.dtype)
+        del blk
+    if spec.peaked_frac > 0.0:
+        rows, cols = _peaks(spec, seed, _idx(spec, seed))
+        keep = (rows >= r0) & (rows < r1)
+        rr, cc = (rows[keep] - r0).to(out.device), cols[keep].to(out.device)
+        out[rr, cc] = (out[rr, cc].float() + spec.peak_height).to(out.dtype)
+    return out
+
+
+def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", rows_per_chunk: int = 4096,
+             with_logits: bool = True) -> Inputs:
     """All inputs of one workload, seeded.  Large logits should be generated with
     ``device='cuda'`` (drawn on the GPU in row chunks); the small per-row arrays are
-    always drawn on the host and then moved to ``device``."""
+    always drawn on the host and then moved to ``device``.  ``with_logits=False`` leaves
+    the logits out (``logits`` is None; ``logits_rows`` draws a slice of them)."""
     B, L, V, R = spec.B, spec.L, spec.V, spec.rows
-    logits = _fill_logits(spec, seed, device, rows_per_chunk)
+    logits = _fill_logits(spec, seed, device, rows_per_chunk) if with_logits else None
 
-    gi = _gen(seed, "idx")
-    idx = torch.randint(0, V, (R,), generator=gi, dtype=torch.int64)
+    idx = _idx(spec, seed)
 
-    if spec.peaked_frac > 0.0:
-        gp = _gen(seed, "peak")
-        n_peak = int(round(spec.peaked_frac * R))
-        rows = torch.sort(torch.randperm(R, generator=gp)[:n_peak]).values
-        cols_rand = torch.randint(0, V, (n_peak,), generator=gp, dtype=torch.int64)
-        # even-numbered peaked rows: peak on the sampled token; odd ones: a random column
-        cols = torch.where(torch.arange(n_peak) % 2 == 0, idx[rows], cols_rand)
+    if spec.peaked_frac > 0.0 and with_logits:
+        rows, cols = _peaks(spec, seed, idx)
         flat = logits.reshape(R, V) if not spec.strided else None
-        for k in range(0, n_peak, 65536):
+        for k in range(0, len(rows), 65536):
             rr, cc = rows[k:k + 65536], cols[k:k + 65536]
             if flat is not None:
                 rd, cd = rr.to(logits.device), cc.to(logits.device)

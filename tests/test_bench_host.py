@@ -77,13 +77,23 @@ def test_reference_arm_line_shape():
     """Rank 0 of the reference arm: one JSON line with the oracle's throughput (small steps)."""
     env = dict(os.environ, RANK="0", WORLD_SIZE="1")
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--steps", "2", "--warmup", "0"], capture_output=True, text=True, env=env,
-                         timeout=600, cwd=ROOT)
+                          "--workload", "grpo_b4_l512_v32000", "--steps", "2", "--warmup", "0"],
+                         capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "grpo_b4_l512_v32000"
+    assert "rows [0, 2048)" in line["cpu_baseline"]["sample"]
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    """With no flags the bench times the 20 GB (16, 4096, 151936) GRPO step at beta 0.04 with
+    8 of 16 zero-advantage sequences."""
+    args = bench.parse_args([])
+    spec = bench.make_spec(args)
+    assert spec.name == "sweep_b16_l4096_v151936" and (spec.B, spec.L, spec.V) == (16, 4096, 151936)
+    assert spec.beta == 0.04 and spec.zero_adv_seqs == 8 and spec.dtype == "bf16"
 
 
 def test_vocab_shard_starts_cover_the_vocabulary():
@@ -104,11 +114,34 @@ def test_step_kind_and_sequence_samples():
     ent = W.get("entropy_slsm_b16_l4096_v32000")
     assert bench.step_kind(bench.parse_args(["--entropy-bwd"]), ent) == "entropy_bwd"
     assert bench.step_kind(bench.parse_args([]), ent) == "slsm"
-    rows = bench.sample_units(spec, "seq", 700, 5)
-    assert len(rows) == 2 * spec.L
-    seqs = rows.reshape(-1, spec.L)
-    assert (np.diff(seqs, axis=1) == 1).all() and (seqs[:, 0] % spec.L == 0).all()
-    assert len(bench.sample_units(spec, "grpo", 700, 5)) == 700
+    rows = bench.oracle_slice(spec, "seq", 700, 5)
+    assert len(rows) == 2 * spec.L and rows[0] % spec.L == 0 and (np.diff(rows) == 1).all()
+    big = W.get("sweep_b16_l4096_v151936")
+    for kind in ("grpo", "seq"):
+        a, b = bench.oracle_slice(big, kind), bench.oracle_slice(big, kind)
+        assert np.array_equal(a, b), "the oracle sample is fixed"
+        assert (np.diff(a) == 1).all() and 0 <= a[0] and a[-1] < big.rows
+    r = bench.oracle_slice(big, "grpo")
+    assert len(r) == 2048 and r[0] % 2048 == 0
+    assert len(bench.oracle_slice(big, "seq")) == big.L  # one whole sequence
+
+
+def test_oracle_pool_times_the_same_sample_each_run():
+    """Both baseline legs time the oracle through time_oracle: the sample handed over once,
+    a warm-up run, then the median of the repeats."""
+    spec = W.get("tiny_fp32")
+    inp = W.generate(spec, 0)
+    import oracle
+    rows = np.arange(spec.rows)
+    x = inp.logits.reshape(-1, spec.V).double().numpy()
+    lp, _ = oracle.selective_log_softmax(x, inp.idx.numpy(), spec.T)
+    smp = {"x": x, "idx": inp.idx.numpy(), "adv": oracle.per_row(inp.adv.numpy(), spec.L), "mask": None,
+           "old": lp + inp.old_offset.double().numpy(), "ref": lp + inp.ref_offset.double().numpy(),
+           "dloss": inp.dloss.double().numpy()}
+    med, used, times = bench.time_oracle(spec, "grpo", smp, warmup=1, repeats=3)
+    assert len(times) == 3 and med == sorted(times)[1] and used >= 1
+    assert bench.sample_bytes(spec, "grpo", smp) > 0
+    assert len(rows) == spec.rows
 
 
 def test_oracle_pool_splits_whole_units_and_runs():
@@ -129,8 +162,9 @@ def test_oracle_pool_splits_whole_units_and_runs():
             assert all(len(p["idx"]) % unit == 0 for p in parts)
             if kind == "seq":
                 assert np.array_equal(np.concatenate([p["adv_seq"] for p in parts]), smp["adv_seq"])
-            dt, used = pool.run(smp)
-            assert used == 2 and dt > 0
+            pool.load(smp)
+            assert len(pool.active) == 2
+            assert pool.go() > 0 and pool.go() > 0  # the loaded sample runs again
         finally:
             pool.close()
 
