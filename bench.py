@@ -614,7 +614,7 @@ class LinearStep:
         self.ref = (f0["logp"] + li.ref_offset).contiguous()
         del f0
         self.kernels = [("grpo_fused_linear", self.call)]
-        self.launches_per_step = 4 * ((R + self.chunk - 1) // self.chunk)
+        self.launches_per_step = 5 * ((R + self.chunk - 1) // self.chunk)
         self.flops_per_step = 6 * R * V * H
 
     def call(self, hidden=None, idx=None, adv=None, dloss=None, mask=None, old=None, ref=None):
@@ -696,9 +696,10 @@ def run_linear(args):
                              "flops_per_step": int(step.flops_per_step)},
                 "memory": {"workspace_bytes": int(step.ws.numel()), "full_batch_logits_bytes_bf16": int(full_logits),
                            "full_batch_logits_and_dlogits_bytes_bf16": int(2 * full_logits)},
-                "cpu_baseline": cpu, "e2e": e2e, "entropy": ent,
+                "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": step.launches_per_step * K,
-                "gpu_launches_note": "per chunk: 3 cuBLASLt GEMMs (library kernels) and 1 row-pass kernel",
+                "gpu_launches_note": "per chunk: the logits GEMM, the row pass, grad_hidden's split GEMM and the "
+                                     "sum of its splits, the grad_weight GEMM (all this library's kernels)",
                 "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                            "samples": clk["samples"]},
                 "timed_wall_s": round(wall, 3), "kernel_source": kernel_source_hash()}

@@ -76,6 +76,9 @@ typedef enum { GRPO_FP32 = 0, GRPO_BF16 = 1 } grpo_dtype;
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define GRPO_DEVERR_IDX_OUT_OF_RANGE 1
+/* A tensor-core GEMM of grpo_fused_linear(_noalloc) gave up waiting for its own copies or
+ * MMAs (about 2 s): its outputs are not valid.  It returns without trapping, TMEM freed. */
+#define GRPO_DEVERR_TIMEOUT 2
 
 /* A [B, L, V] logits (or dlogits) tensor: ptr + b*stride_b + l*stride_l + j. */
 typedef struct {
@@ -374,7 +377,12 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  *   x_c = h_c W^T (fp32, tensor-core GEMM)  ->  the row pass of grpo_loss_fused on x_c
  *   (forward outputs, dlogits in bf16)  ->  grad_hidden_c = dlogits_c W,
  *   grad_weight += dlogits_c^T h_c  (tensor-core GEMMs, fp32 accumulation).
- * The GEMMs run through cuBLASLt; the row pass is this library's kernel.
+ * All of it runs in this library's kernels: the GEMMs are tcgen05 kernels with TMA-staged
+ * bf16 operands and fp32 accumulators in tensor memory; the logits GEMM also forms each
+ * row's softmax statistic per 128 columns, so the row pass reads the fp32 logits once.
+ * grad_hidden's GEMM is split along the vocabulary and its splits are summed in a fixed
+ * order, and each element of grad_weight receives one add per chunk, so the results do not
+ * depend on timing.
  *
  *   hidden        [B*L, H] bf16, row-major, 16-byte aligned;  H a multiple of 8
  *   weight        [V, H] bf16, row-major, 16-byte aligned
@@ -382,13 +390,17 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  *   lse, kl, is_clipped, entropy, dev_err: as in grpo_loss_fused (per-row arrays [B*L])
  *   chunk_rows    rows per chunk, >= 1 (the last chunk may be shorter)
  *   workspace     device scratch of at least grpo_fused_linear_workspace_size() bytes,
- *                 256-byte aligned; its contents are not kept between calls
+ *                 256-byte aligned; its contents are not kept between calls.  The size is
+ *                 one chunk's fp32 logits, bf16 dlogits and statistics (6 V8 + 32
+ *                 ceil(V / 256) bytes a row, V8 = V rounded up to a multiple of 8) plus
+ *                 128 MiB for the K splits of grad_hidden (as many splits of
+ *                 chunk_rows * H * 4 bytes as fit, at most 32)
  *   grad_hidden   [B*L, H] fp32 output (overwritten), or NULL
  *   grad_weight   [V, H] fp32, ACCUMULATED into (+=), or NULL; 16-byte aligned
  *
  * The logits are formed in fp32; dlogits are rounded to bf16 (the weight's type) for the
- * two backward GEMMs.  Calls on the same stream run in order; the library keeps one
- * cuBLASLt handle per device.
+ * two backward GEMMs.  Calls on the same stream run in order.  A GEMM whose own copies or
+ * MMAs stall for about 2 s gives up, sets GRPO_DEVERR_TIMEOUT in *dev_err and returns.
  */
 grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes);
 grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H, int64_t V,
@@ -405,21 +417,23 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
  * handed to a pool it does not control, or a step that must not stall on an allocation).
  * The pages have no counterpart; this is a convenience of this library.
  *
- * Its scratch (one chunk's fp32 logits and bf16 dlogits, and a 4 MiB workspace for the
- * GEMMs) is a fixed 32 MiB device array inside the library, which every device context that
- * loads the library holds until the process exits.  Limit: chunk_rows * 6 * V8 bytes, each
- * of the two chunk buffers rounded up to 256 bytes, plus 4 MiB must fit in 32 MiB
+ * Its scratch (one chunk's fp32 logits, bf16 dlogits and per-128-column statistics, and the
+ * K splits of grad_hidden) is a fixed 32 MiB device array inside the library, which every
+ * device context that loads the library holds until the process exits.  Limit: the three
+ * chunk buffers, chunk_rows * (4 V8 + 2 V8 + 32 ceil(V / 256)) bytes, each rounded up to
+ * 256 bytes, plus one split of grad_hidden, chunk_rows * H * 4 bytes, must fit in 32 MiB
  * (V8 = V rounded up to a multiple of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before
- * any launch.  For V = 151936 that is at most 32 rows per chunk.
+ * any launch.  For V = 151936 and H = 1024 that is at most 35 rows per chunk.
  *
- * The first call on a device does the set-up: it looks up the array's device address and,
- * like every GEMM path of this library, creates the library's cuBLASLt handle for that
- * device.  Make that first call before any stream capture.  Every call uses the whole
- * array, so calls that overlap on the GPU race on it: run them on one stream, or one after
- * the other.  The array keeps the last call's contents; nothing in it has to start at zero.
+ * The first call on a device (and the first after a cudaDeviceReset) does the set-up: it
+ * looks up the array's device address in the current context.  Make that first call
+ * before any stream capture.  Every call uses the whole array, so calls that overlap on the
+ * GPU race on it: run them on one stream, or one after the other.  The array keeps the last
+ * call's contents; nothing in it has to start at zero.
  *
  * Arguments: those of grpo_fused_linear without workspace / workspace_bytes; the results
- * equal grpo_fused_linear's to within the GEMMs' fp32 summation order.
+ * equal grpo_fused_linear's at the same chunk_rows, to within the fp32 summation order of
+ * grad_hidden's K splits (fewer splits may fit here).
  */
 grpo_status grpo_fused_linear_noalloc(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H,
                                       int64_t V, const int64_t* idx, const float* old_logp, const float* ref_logp,

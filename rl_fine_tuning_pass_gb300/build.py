@@ -2,8 +2,9 @@
 ``rl_fine_tuning_pass_gb300/libgrpo_rowpass.so`` for sm_103a (GB300).
 
 Each translation unit is compiled in parallel with one ``-gencode`` (a minute or less),
-then linked with the static CUDA runtime and the toolkit's cuBLASLt (the LM-head GEMMs of
-grpo_fused_linear).  Nothing is installed outside this directory.
+then linked with the static CUDA runtime; the tensor-map encoder is looked up through the
+runtime at first use, so no other library is linked.  Nothing is installed outside this
+directory.
 
     python -m rl_fine_tuning_pass_gb300.build          # build if sources changed
     python -m rl_fine_tuning_pass_gb300.build --force  # rebuild
@@ -40,11 +41,6 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the row-pass library")
 
 
-def cuda_lib_dir() -> str:
-    """The toolkit's library directory (next to nvcc), for cuBLASLt."""
-    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
-
-
 def _deps():
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "grpo_rowpass.h")]
 
@@ -76,9 +72,7 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     tmp = LIB_PATH + ".tmp"
-    lib_dir = cuda_lib_dir()
-    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-L", lib_dir, "-lcublasLt",
-           "-Xlinker", f"-rpath,{lib_dir}"]
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")

@@ -538,17 +538,15 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
 }  // extern "C"
 
 namespace {
-constexpr uint64_t kLinearGemmWs = uint64_t(32) << 20;  // the GEMMs' workspace
-uint64_t round256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
-int64_t linear_ld(int64_t V) { return (V + 7) / 8 * 8; }
+// Room for the K splits of grad_hidden's GEMM: 16 splits of a 2048-row chunk at H = 1024.
+constexpr uint64_t kLinearSplitWs = uint64_t(128) << 20;
 }  // namespace
 
 extern "C" {
 
 grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes) {
   if (bytes == nullptr || V < 1 || V > kMaxV || chunk_rows < 1 || chunk_rows > kMaxRows) return GRPO_ERR_INVALID_ARG;
-  const uint64_t ld = static_cast<uint64_t>(linear_ld(V));
-  *bytes = round256(ld * chunk_rows * 4) + round256(ld * chunk_rows * 2) + kLinearGemmWs;
+  *bytes = grpo::linear_chunk_bytes(V, chunk_rows) + kLinearSplitWs;
   return GRPO_OK;
 }
 
@@ -577,7 +575,6 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
     return GRPO_ERR_INVALID_ARG;
   if (beta != 0.f && !ok_f32(ref_logp)) return GRPO_ERR_INVALID_ARG;
   if (ref_logp != nullptr && !aligned(ref_logp, 4)) return GRPO_ERR_INVALID_ARG;
-  const int64_t ld = linear_ld(V);
   grpo::FusedLinearParams q{};
   q.hidden = static_cast<const uint16_t*>(hidden);
   q.weight = static_cast<const uint16_t*>(weight);
@@ -585,12 +582,8 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
   q.H = H;
   q.V = V;
   q.chunk = chunk;
-  q.ld = ld;
-  char* w = static_cast<char*>(workspace);
-  q.logits = reinterpret_cast<float*>(w);
-  q.dlogits = reinterpret_cast<uint16_t*>(w + round256(static_cast<uint64_t>(ld) * chunk * 4));
-  q.ws = w + round256(static_cast<uint64_t>(ld) * chunk * 4) + round256(static_cast<uint64_t>(ld) * chunk * 2);
-  q.ws_bytes = kLinearGemmWs;
+  q.ld = grpo::linear_ld(V);
+  grpo::linear_carve(q, static_cast<char*>(workspace), need);
   q.grad_hidden = grad_hidden;
   q.grad_weight = grad_weight;
   grpo::LinearChunkParams& cp = q.chunk_params;
@@ -613,9 +606,6 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
   p.is_clipped = is_clipped;
   p.entropy = entropy;
   p.dev_err = dev_err;
-  cp.logits = q.logits;
-  cp.dlogits = q.dlogits;
-  cp.ld = ld;
   cp.dloss = dloss;
   cp.T = T;
   return from_cuda(grpo::launch_fused_linear(q, reinterpret_cast<cudaStream_t>(stream)));

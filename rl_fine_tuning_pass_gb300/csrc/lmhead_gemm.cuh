@@ -1,0 +1,565 @@
+// The three contractions of the GRPO loss on top of the LM head ("Liger GRPO meets TRL",
+// sections 3 and 4: the chunk's logits are its hidden states times the head weight, and the
+// gradients of the hidden states and of the head weight are formed from the chunk's
+// dlogits), as one tcgen05 GEMM kernel for sm_103a:
+//
+//   D[M, N] = A[M, K] B[K, N]    bf16 operands, fp32 accumulation in tensor memory
+//
+// with three epilogues:
+//   kEpiLogits  D is the chunk's fp32 logits (M = rows, N = V, K = H); besides storing
+//               them, each tile forms the online softmax statistic (a, s, u) of each half
+//               (128 columns) of every row, so the row pass that follows needs one sweep
+//               over the row instead of two;
+//   kEpiStore   D is stored (one K split of grad_hidden: M = rows, N = H, K = V);
+//   kEpiAccum   D is added to the fp32 output (grad_weight += dlogits^T h: M = V, N = H,
+//               K = rows).
+//
+// Layout and pipeline.  One persistent CTA per SM walks a static list of 128 x 256 output
+// tiles (and K splits).  Warp 0 streams the operands with TMA into a 4-stage ring of
+// 128-byte-swizzled shared-memory tiles (64 K-elements deep: A 16 KB, B 32 KB); warp 1
+// allocates 512 TMEM columns (two 256-column fp32 accumulators) and one of its threads
+// issues tcgen05.mma (M = 128, N = 256, K = 16) for every 16-deep slice; warps 2-9 read the
+// finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes = 32 rows of
+// its quarter; two warps share a quarter, one for each half of the columns) while the MMAs
+// of the next tile fill the other accumulator.  Each warp writes 32 x 32 fp32 boxes into
+// its 128-byte-swizzled staging buffer and one lane stores them with a TMA tensor store
+// (kEpiLogits, kEpiStore) or a TMA reduce-add (kEpiAccum); the tensor maps clip the ragged
+// edges.  Operands may be K-major (K
+// contiguous: h, W in the logits GEMM, dlogits in grad_hidden) or MN-major (M or N
+// contiguous: W in grad_hidden, dlogits^T and h in grad_weight); the MN-major tiles are
+// loaded as 64-wide boxes and described to the MMA with the MN-major bit.
+//
+// Every wait on an mbarrier gives up after about two seconds: it sets the CTA's abort flag,
+// every role leaves its loop, the in-flight copies and MMAs are waited for (again with a
+// limit), TMEM is freed and the kernel returns with GRPO_DEVERR_TIMEOUT_BIT set in the
+// caller's error word.  Nothing traps.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "rowpass_fwd.cuh"
+
+namespace grpo {
+namespace gemm {
+
+constexpr int BM = 128;     // rows of a tile (TMEM lanes)
+constexpr int BN = 256;     // columns of a tile (TMEM columns of one accumulator)
+constexpr int BK = 64;      // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, each half of the tile's columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr uint32_t kStageA = BM * BK * 2;  // 16 KB
+constexpr uint32_t kStageB = BN * BK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr uint32_t kStageC = 32 * 32 * 4;        // one epilogue warp's 32 x 32 fp32 output box
+constexpr uint32_t kSmemC = kEpiWarps * kStageC;  // one staging box per epilogue warp
+constexpr uint32_t kBarBytes = 256;
+constexpr uint32_t kSmemBytes = 1024 + kStages * (kStageA + kStageB) + kSmemC + kBarBytes;
+constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
+
+enum Epi : int { kEpiLogits = 0, kEpiStore = 1, kEpiAccum = 2 };
+
+struct Params {
+  int M, N;            // output rows and columns
+  int k_blocks;        // ceil(K / 64)
+  int m_tiles, n_tiles, splits;
+  int m_fastest;       // 1: consecutive tiles share a B tile; 0: share an A tile
+  float* C;            // fp32 output [M][ldc] (+ split * split_stride)
+  int64_t ldc, split_stride;
+  // kEpiLogits only
+  float4* stats;       // [M][2 n_tiles]: (a, s, u, 0) of each half tile's 128 columns
+  float c;             // log2(e) / T
+  int* err;            // device error word (nullable)
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete.  Gives up (false) when the CTA's abort
+// flag is set (if honor_abort) or after kWaitCycles, which sets the flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 127u) == 0u) {
+      if (honor_abort && *abort_flag) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// No committed bulk group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled tile (start, leading and stride
+// byte offsets in 16-byte units, descriptor version 1, swizzle mode 2 = 128 B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, their majorness,
+// N / 8 and M / 16.
+template <bool A_MN, bool B_MN>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The tile list: tile t -> (m, n, split) and the split's K blocks [kb0, kb1).
+struct Tile {
+  int m, n, s, kb0, kb1;
+};
+__device__ __forceinline__ Tile tile_of(const Params& p, int t) {
+  Tile u;
+  const int mn = p.m_tiles * p.n_tiles;
+  u.s = t / mn;
+  const int r = t - u.s * mn;
+  if (p.m_fastest) {
+    u.m = r % p.m_tiles;
+    u.n = r / p.m_tiles;
+  } else {
+    u.n = r % p.n_tiles;
+    u.m = r / p.n_tiles;
+  }
+  u.kb0 = static_cast<int>(static_cast<int64_t>(p.k_blocks) * u.s / p.splits);
+  u.kb1 = static_cast<int>(static_cast<int64_t>(p.k_blocks) * (u.s + 1) / p.splits);
+  return u;
+}
+
+// ---------------------------------------------------------------------------
+// epilogues (one thread = one row of the tile, 32 columns at a time)
+// ---------------------------------------------------------------------------
+// Row `lane` of a warp's 32 x 32 fp32 box into its 128-byte-swizzled staging buffer: the
+// 16-byte chunk q of row r sits at chunk q ^ (r % 8), so the eight rows a quarter-warp
+// writes at once fall in eight different bank groups.
+__device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&v)[32]) {
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t dst = row + static_cast<uint32_t>((q ^ (lane & 7)) * 16);
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v[4 * q]), "f"(v[4 * q + 1]),
+                 "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                 : "memory");
+  }
+}
+
+// Fold 32 logits (the first `valid` of them) into the tile's running statistic, with the
+// numerics of the row kernels' stream (rowpass_fwd.cuh: one rescale per chunk, packed f32x2
+// sums).
+template <bool kH>
+__device__ __forceinline__ void stat_cols(Running& rs, float (&v)[32], int valid, float c) {
+  if (valid < 32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i >= valid) v[i] = -INFINITY;  // adds 2^-inf = 0; t * 0 is guarded below
+  }
+  float cm = v[0];
+#pragma unroll
+  for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+  if (cm > rs.m) run_rescale<kH>(rs, cm, c);
+  const float2 c2 = make_float2(c, c), na2 = make_float2(-rs.a, -rs.a);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float2 x = make_float2(v[2 * i], v[2 * i + 1]);
+    if (kH) {
+      x.x = fmaxf(x.x, kNegClamp);  // -inf (padding or input) adds 0 to u, not 0 * -inf
+      x.y = fmaxf(x.y, kNegClamp);
+    }
+    run_pair<kH>(rs, x, c2, na2);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int EPI, bool A_MN, bool B_MN, bool kH>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kStages * kStageA;
+  unsigned char* sC = sB + kStages * kStageB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kSmemC);
+  // full[s], empty[s], tmem_full[2], tmem_empty[2], drain
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  wait_for_previous_grids();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = p.m_tiles * p.n_tiles * p.splits;
+
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;  // stages filled and not yet known to be consumed (for the abort path)
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile u = tile_of(p, t);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, kStageA + kStageB);
+          const uint32_t a_dst = smem_u32(sA + stage * kStageA), b_dst = smem_u32(sB + stage * kStageB);
+          const int k0 = kb * BK;
+          if constexpr (A_MN) {
+            tma_load_2d(a_dst, &tmA, u.m * BM, k0, fb);
+            tma_load_2d(a_dst + 8192, &tmA, u.m * BM + 64, k0, fb);
+          } else {
+            tma_load_2d(a_dst, &tmA, k0, u.m * BM, fb);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tma_load_2d(b_dst + 8192 * i, &tmB, u.n * BN + 64 * i, k0, fb);
+          } else {
+            tma_load_2d(b_dst, &tmB, k0, u.n * BN, fb);
+          }
+          issued = issued < kStages ? issued + 1 : kStages;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // copies may still be landing in the ring: wait (bounded) for each stage's full
+        // phase before the CTA's shared memory can go away
+        for (int i = 0; i < issued; ++i) {
+          if (--stage < 0) {
+            stage = kStages - 1;
+            phase ^= 1u;
+          }
+          mbar_wait(full0 + 8 * stage, phase, abort_flag, false);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16<A_MN, B_MN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+        const Tile u = tile_of(p, t);
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kStageA), b_base = smem_u32(sB + stage * kStageB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sw128_desc(a_base + kk * 2048, 8192, 1024) : sw128_desc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sw128_desc(b_base + kk * 2048, 8192, 1024) : sw128_desc(b_base + kk * 32, 16, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);  // the stage is free once these MMAs are done
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(tfull0 + 8 * acc);  // the accumulator is ready
+      }
+      // no MMA may still be running when TMEM is freed
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag, false);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 2..9; TMEM lanes 32 * (warp % 4) ..., columns half * 128 ... ----
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
+    int local = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+      const Tile u = tile_of(p, t);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int row0 = u.m * BM + quarter * 32;  // this warp's first row
+      const int row = row0 + lane;
+      const bool row_ok = row < p.M;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN + half * (BN / 2));
+      const int col_base = u.n * BN + half * (BN / 2);
+      Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+      for (int j = 0; j < BN / 64; ++j) {
+        const int col0 = col_base + 32 * j;
+        const int valid = p.N - col0;
+        if (valid <= 0) break;  // the rest of the tile lies beyond the last column
+        float v[32];
+        tmem_ld32(taddr + 32 * j, v);
+        // the staging box must have been read out by the previous box's TMA
+        if (lane == 0) bulk_wait_read_0();
+        __syncwarp();
+        stage_row(buf, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (EPI == kEpiLogits) tma_store_2d(&tmC, buf, col0, row0);
+          else if constexpr (EPI == kEpiStore) tma_store_3d(&tmC, buf, col0, row0, u.s);
+          else tma_reduce_add_2d(&tmC, buf, col0, row0);
+          bulk_commit();
+        }
+        if constexpr (EPI == kEpiLogits) {
+          if (row_ok) stat_cols<kH>(rs, v, valid, p.c);
+        }
+      }
+      if constexpr (EPI == kEpiLogits) {
+        if (row_ok && col_base < p.N)
+          p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] =
+              make_float4(rs.a, rs.s.x + rs.s.y, rs.u.x + rs.u.y, 0.f);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);  // this thread is done with the accumulator
+    }
+    if (lane == 0) bulk_wait_all();  // every output box written before the CTA ends
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.err != nullptr) atomicOr(p.err, GRPO_DEVERR_TIMEOUT_BIT);
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps and the launch
+// ---------------------------------------------------------------------------
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against the driver
+// library).
+inline TensorMapEncodeFn tensor_map_encoder() {
+  static const TensorMapEncodeFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<TensorMapEncodeFn>(nullptr);
+    return reinterpret_cast<TensorMapEncodeFn>(f);
+  }();
+  return fn;
+}
+
+// A bf16 matrix of `outer` rows of `inner` elements, `row_elems` apart (a multiple of 8),
+// read in boxes of box_outer rows x box_inner elements (box_inner = 64: one 128-byte
+// swizzle row).  Elements outside [0, inner) x [0, outer) read as zero.
+inline bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
+                          uint32_t box_inner, uint32_t box_outer) {
+  const TensorMapEncodeFn enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_elems * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor map of one operand: K-major (K contiguous: [MN rows][K], one box of `mn_box`
+// rows x 64) or MN-major (MN contiguous: [K rows][MN], boxes of 64 rows x 64).
+inline bool make_operand_map(CUtensorMap* map, const void* base, bool mn_major, uint64_t mn, uint64_t k,
+                             uint64_t row_elems, uint32_t mn_box) {
+  return mn_major ? make_bf16_map(map, base, mn, k, row_elems, 64, BK)
+                  : make_bf16_map(map, base, k, mn, row_elems, BK, mn_box);
+}
+
+// The fp32 output [depth][outer][inner] (depth = K splits, `depth_elems` apart; rows
+// `row_elems` apart) written in 32 x 32 boxes through the 128-byte-swizzled staging
+// buffers; rank 3 when depth_elems != 0, else rank 2.  Elements outside the extents are
+// not written.
+inline bool make_f32_out_map(CUtensorMap* map, void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
+                             uint64_t depth = 1, uint64_t depth_elems = 0) {
+  const TensorMapEncodeFn enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint32_t rank = depth_elems != 0 ? 3 : 2;
+  const cuuint64_t dims[3] = {inner, outer, depth};
+  const cuuint64_t strides[2] = {row_elems * 4, depth_elems * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, base, dims, strides, box, elem_strides,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+// Launch one GEMM: the grid is min(tiles, SMs) persistent CTAs (one per SM).
+template <int EPI, bool A_MN, bool B_MN, bool kH>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const Params& p,
+                        cudaStream_t stream) {
+  auto kernel = gemm_kernel<EPI, A_MN, B_MN, kH>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int total = p.m_tiles * p.n_tiles * p.splits;
+  if (total <= 0) return cudaSuccess;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, b, c, p);
+}
+
+}  // namespace gemm
+}  // namespace grpo

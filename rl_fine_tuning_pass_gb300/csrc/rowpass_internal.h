@@ -31,6 +31,8 @@ inline cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, di
 
 // Error bit OR-ed into the caller's device error word (GRPO_DEVERR_IDX_OUT_OF_RANGE).
 constexpr int GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT = 1;
+// A tensor-core GEMM's bounded wait ran out (GRPO_DEVERR_TIMEOUT).
+constexpr int GRPO_DEVERR_TIMEOUT_BIT = 2;
 
 // 16-byte loads in flight per thread: single-warp CTAs keep more of them so that a
 // warp streaming a whole row still covers the memory latency.
@@ -178,8 +180,10 @@ struct LinearChunkParams {
   FwdParams f;            // per-row inputs and outputs of the whole batch; f.x.L = tokens per
                           // sequence, f.x.V = vocabulary
   const float* logits;    // the chunk's logits [rows][ld] fp32
+  const float4* stats;    // the chunk's per-128-column statistics [rows][n_stat]
   uint16_t* dlogits;      // the chunk's dlogits [rows][ld] bf16
   int64_t ld;             // elements between rows, a multiple of 8
+  int n_stat;             // statistics slots per row (two per 256-column tile)
   int64_t row0;           // the chunk's first row in the batch
   const float* dloss;     // [batch rows]
   float T;
@@ -192,12 +196,33 @@ struct FusedLinearParams {
   int64_t ld;              // row stride of the chunk buffers (V rounded up to 8)
   float* logits;           // workspace: [chunk][ld] fp32
   uint16_t* dlogits;       // workspace: [chunk][ld] bf16
-  void* ws;                // workspace for the GEMMs
-  size_t ws_bytes;
+  float4* stats;           // workspace: [chunk][2 ceil(V / 256)] statistics of the logits GEMM
+  float* part;             // workspace: the K splits of grad_hidden [splits][chunk][H] fp32
+  uint64_t part_bytes;     // its size (sets the number of splits)
   float* grad_hidden;      // [rows][H] fp32, or null
   float* grad_weight;      // [V][H] fp32, accumulated into, or null
   LinearChunkParams chunk_params;
 };
+// Sizes of the workspace parts for V and a chunk of rows (each rounded up to 256 bytes).
+inline uint64_t linear_round256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+inline int64_t linear_ld(int64_t V) { return (V + 7) / 8 * 8; }
+inline int64_t linear_n_stat(int64_t V) { return 2 * ((V + 255) / 256); }
+inline uint64_t linear_chunk_bytes(int64_t V, int64_t chunk) {
+  const uint64_t ld = static_cast<uint64_t>(linear_ld(V)), c = static_cast<uint64_t>(chunk);
+  return linear_round256(ld * c * 4) + linear_round256(ld * c * 2) +
+         linear_round256(static_cast<uint64_t>(linear_n_stat(V)) * c * 16);
+}
+// Carve the chunk buffers out of `base`; the rest (part_bytes) holds grad_hidden's K splits.
+inline void linear_carve(FusedLinearParams& q, char* base, uint64_t total_bytes) {
+  const uint64_t ld = static_cast<uint64_t>(q.ld), c = static_cast<uint64_t>(q.chunk);
+  const uint64_t lb = linear_round256(ld * c * 4), db = linear_round256(ld * c * 2);
+  const uint64_t sb = linear_round256(static_cast<uint64_t>(linear_n_stat(q.V)) * c * 16);
+  q.logits = reinterpret_cast<float*>(base);
+  q.dlogits = reinterpret_cast<uint16_t*>(base + lb);
+  q.stats = reinterpret_cast<float4*>(base + lb + db);
+  q.part = reinterpret_cast<float*>(base + lb + db + sb);
+  q.part_bytes = total_bytes - (lb + db + sb);
+}
 cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream);
 
 // Merge of gathered vocabulary-shard statistics (one thread per row).

@@ -4,26 +4,29 @@
 // chunk's hidden states (dlogits W) and of the head weight (+= dlogits^T h) are formed
 // before the next chunk, so the logits of the whole batch never exist at once.
 //
-// The three contractions are plain GEMMs on the tensor cores through cuBLASLt (bf16
-// operands, fp32 accumulation).  The row pass between them is this file's kernel: one CTA
-// per row of the chunk reads the chunk's fp32 logits (just written, mostly from L2) for
-// the online statistic and the epilogue, decides the row factor g, and sweeps the row again
-// to write dlogits in bf16, the operand type of the two backward GEMMs.  The idx element
-// is g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
-#include <cublasLt.h>
-
+// The three contractions are this library's tcgen05 GEMMs (lmhead_gemm.cuh: bf16 operands
+// staged by TMA, fp32 accumulation in tensor memory).  The logits GEMM also forms, in its
+// epilogue, the online softmax statistic of every 128 columns of every row.  The row pass
+// between the GEMMs is this file's kernel: one CTA per row of the chunk merges the row's
+// statistics, runs the forward epilogue, decides the row factor g, and sweeps the fp32 row
+// once to write dlogits in bf16, the operand type of the two backward GEMMs.  The idx
+// element is g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
+// grad_hidden's contraction runs over the whole vocabulary, so it is split along K; the
+// splits are summed in a fixed order by a small kernel, so results do not depend on timing.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <map>
 #include <mutex>
-#include <tuple>
 
 #include "grpo_rowpass.h"
+#include "lmhead_gemm.cuh"
 #include "rowpass_bwd.cuh"
-#include "rowpass_fwd.cuh"
 
 namespace grpo {
 namespace {
+
+// Threads of the row-pass CTA (one row each).
+constexpr int kLinearThreads = 512;
 
 // Row pass over one chunk: fp32 logits [rows][ld] in, bf16 dlogits [rows][ld] out.
 template <int THREADS, int UNROLL, bool kH, bool NEG>
@@ -80,8 +83,10 @@ __device__ __forceinline__ void fill_bf16_row(uint16_t* out, int V, uint32_t pai
   if (j < V) out[j] = static_cast<uint16_t>(pair & 0xFFFFu);
 }
 
+// One CTA per row of the chunk: merge the row's statistics, the forward epilogue and the row
+// factor, then one sweep over the fp32 row writing bf16 dlogits.
 template <int THREADS, int UNROLL, bool kH>
-__global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunkParams q) {
+__global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkParams q) {
   wait_for_previous_grids();
   constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
   const FwdParams& p = q.f;
@@ -103,30 +108,15 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
 
-  // sweep 1: the online statistic of the fp32 row (16-byte aligned: ld % 8 == 0).  The row
-  // is kept in L2 (evict_last) for sweep 2, which lets it go (evict_first); one CTA of 1024
-  // threads per SM keeps some 150 rows in flight, few enough for L2 to hold them.
-  Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  const uint4* vb = reinterpret_cast<const uint4*>(row);
-  const int nvec = V / 4;
-  if (tid < V - 4 * nvec) run_scalar<kH>(rs, row[4 * nvec + tid], c);
-  int i = tid;
-  for (; i + (UNROLL - 1) * THREADS < nvec; i += UNROLL * THREADS) {
-    uint4 v[UNROLL];
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = ld_v4_evict_last(vb + i + k * THREADS);
-    run_vectors<F32, kH>(rs, v, c);
-  }
-  for (; i < nvec; i += THREADS) {
-    uint4 v[1];
-    v[0] = ld_v4_evict_last(vb + i);
-    run_vectors<F32, kH>(rs, v, c);
+  // the row's statistic: its 128-column parts, merged in a fixed order
+  const int n_valid = (V + 127) / 128;
+  const float4* st_row = q.stats + rl * q.n_stat;
+  Stat mine{-INFINITY, 0.f, 0.f};
+  for (int k = tid; k < n_valid; k += THREADS) {
+    const float4 e = st_row[k];
+    mine = stat_combine(mine, Stat{e.x, e.y, e.z});
   }
   const float x_idx = tid == 0 ? row[idx] : 0.f;
-  Stat mine;
-  mine.a = rs.a;
-  mine.s = rs.s.x + rs.s.y;
-  mine.u = rs.u.x + rs.u.y;
   const Stat st = stat_block_reduce<THREADS>(mine);
 
   __shared__ float sh_g, sh_nK;
@@ -139,17 +129,15 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   }
   __syncthreads();
   const float g = sh_g;
-  if (g == 0.f) {  // early-out: +0.0 over the row
+  if (g == 0.f) {  // early-out: +0.0 over the row, its logits never read
     fill_bf16_row(out, V, 0u, THREADS);
-    l2_demote<THREADS>(row, static_cast<int64_t>(V) * 4);
     return;
   }
   if (bad_idx) {
     fill_bf16_row(out, V, BF16::kNaNPair, THREADS);
-    l2_demote<THREADS>(row, static_cast<int64_t>(V) * 4);
     return;
   }
-  // sweep 2: d_j = -sign(g) |g| p_j in bf16, and g (1 - p_idx) at idx
+  // the sweep: d_j = -sign(g) |g| p_j in bf16, and g (1 - p_idx) at idx
   bool owner = false;
   const float nK = sh_nK;
   const float q_part = g > 0.f ? linear_sweep2<THREADS, UNROLL, kH, true>(row, out, V, idx, c, nK, owner)
@@ -158,127 +146,142 @@ __global__ void __launch_bounds__(THREADS) linear_chunk_kernel(const LinearChunk
   if (owner) BF16::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
 
-// ---------------------------------------------------------------------------
-// cuBLASLt: one handle per device, the heuristic's algorithm cached per problem
-// ---------------------------------------------------------------------------
-
-struct LtHandle {
-  cublasLtHandle_t h = nullptr;
-  bool ok = false;
-};
-
-cublasLtHandle_t lt_handle() {
-  static LtHandle handles[64];
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!handles[dev].ok) {
-    if (cublasLtCreate(&handles[dev].h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    handles[dev].ok = true;
+// grad_hidden rows [row0, row0 + c) = the sum of the K splits, in split order.
+__global__ void __launch_bounds__(256) split_sum_kernel(const float4* __restrict__ part, float4* __restrict__ out,
+                                                        int64_t n4, int splits, int64_t split4) {
+  wait_for_previous_grids();
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = part[s * split4 + i];
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    out[i] = a;
   }
-  return handles[dev].h;
 }
 
-// Column-major D[m, n] = alpha op(A) op(B) + beta C (C = D), A, B bf16, D fp32 or bf16,
-// fp32 accumulation.
-struct GemmKey {
-  int dev, ta, tb, dtype_d;
-  int64_t m, n, k, lda, ldb, ldd;
-  size_t ws;
-  bool operator<(const GemmKey& o) const {
-    return std::tie(dev, ta, tb, dtype_d, m, n, k, lda, ldb, ldd, ws) <
-           std::tie(o.dev, o.ta, o.tb, o.dtype_d, o.m, o.n, o.k, o.lda, o.ldb, o.ldd, o.ws);
+// K splits of grad_hidden's GEMM: as many as the workspace holds (at most 32), picked so
+// that the split tiles fill the persistent CTAs' passes most evenly.
+int grad_hidden_splits(int64_t tiles, int64_t k_blocks, uint64_t part_bytes, uint64_t split_bytes, int sms) {
+  int best = 1;
+  double best_eff = 0.0;
+  const int64_t cap = std::min<int64_t>(32, std::min<int64_t>(k_blocks, static_cast<int64_t>(part_bytes / split_bytes)));
+  for (int s = 1; s <= cap; ++s) {
+    const int64_t units = tiles * s;
+    const int64_t grid = std::min<int64_t>(units, sms);
+    const int64_t passes = (units + grid - 1) / grid;
+    const double eff = static_cast<double>(units) / static_cast<double>(passes * sms);
+    if (eff > best_eff + 1e-3) {
+      best_eff = eff;
+      best = s;
+    }
   }
-};
-
-cudaError_t lt_gemm(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const void* A, int64_t lda, const void* B,
-                    int64_t ldb, void* D, int64_t ldd, cudaDataType_t dtype_d, float beta, void* ws,
-                    size_t ws_bytes, cudaStream_t stream) {
-  cublasLtHandle_t h = lt_handle();
-  if (h == nullptr) return cudaErrorNotSupported;
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
-  cudaError_t err = cudaErrorUnknown;
-  const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-  do {
-    if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) break;
-    if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) != CUBLAS_STATUS_SUCCESS) break;
-    if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) != CUBLAS_STATUS_SUCCESS) break;
-    if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, ta ? k : m, ta ? m : k, lda) != CUBLAS_STATUS_SUCCESS) break;
-    if (cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, tb ? n : k, tb ? k : n, ldb) != CUBLAS_STATUS_SUCCESS) break;
-    if (cublasLtMatrixLayoutCreate(&ld, dtype_d, m, n, ldd) != CUBLAS_STATUS_SUCCESS) break;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const GemmKey key{dev, ta, tb, static_cast<int>(dtype_d), m, n, k, lda, ldb, ldd, ws_bytes};
-    static std::map<GemmKey, cublasLtMatmulAlgo_t> cache;
-    static std::mutex mu;
-    cublasLtMatmulAlgo_t algo;
-    bool have = false;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      auto it = cache.find(key);
-      if (it != cache.end()) {
-        algo = it->second;
-        have = true;
-      }
-    }
-    if (!have) {
-      cublasLtMatmulPreference_t pref = nullptr;
-      if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
-      cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
-                                           sizeof(ws_bytes));
-      cublasLtMatmulHeuristicResult_t res;
-      int found = 0;
-      const cublasStatus_t hs = cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &found);
-      cublasLtMatmulPreferenceDestroy(pref);
-      if (hs != CUBLAS_STATUS_SUCCESS || found < 1) {
-        err = cudaErrorNotSupported;
-        break;
-      }
-      algo = res.algo;
-      std::lock_guard<std::mutex> lock(mu);
-      cache[key] = algo;
-    }
-    const float alpha = 1.f;
-    const cublasStatus_t s = cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, D, ld, D, ld, &algo, ws, ws_bytes,
-                                            stream);
-    err = s == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorLaunchFailure;
-  } while (false);
-  if (ld) cublasLtMatrixLayoutDestroy(ld);
-  if (lb) cublasLtMatrixLayoutDestroy(lb);
-  if (la) cublasLtMatrixLayoutDestroy(la);
-  if (op) cublasLtMatmulDescDestroy(op);
-  return err;
+  return best;
 }
 
 }  // namespace
 
 cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream) {
+  using namespace gemm;
   const int64_t R = q.rows, H = q.H, V = q.V, ld = q.ld;
+  const bool kH = q.chunk_params.f.entropy != nullptr;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  int* err = q.chunk_params.f.dev_err;
+  CUtensorMap tW_k, tW_mn;  // the head weight, K-major (logits) and MN-major (grad_hidden)
+  if (!make_operand_map(&tW_k, q.weight, false, V, H, H, BN) || !make_operand_map(&tW_mn, q.weight, true, H, V, H, BN))
+    return cudaErrorInvalidValue;
+  CUtensorMap tGW;
+  if (q.grad_weight != nullptr && !make_f32_out_map(&tGW, q.grad_weight, H, V, H)) return cudaErrorInvalidValue;
   for (int64_t r0 = 0; r0 < R; r0 += q.chunk) {
     const int64_t c = R - r0 < q.chunk ? R - r0 : q.chunk;
     const uint16_t* h = q.hidden + r0 * H;
-    // logits^T [V, c] (column-major, ld) = W [V, H] h^T: W is the column-major [H, V] matrix
-    cudaError_t e = lt_gemm(true, false, V, c, H, q.weight, H, h, H, q.logits, ld, CUDA_R_32F, 0.f, q.ws,
-                            q.ws_bytes, stream);
+    // 1. logits [c, V] fp32 = h W^T, with the statistics of every 128 columns
+    CUtensorMap tA, tL;
+    if (!make_operand_map(&tA, h, false, c, H, H, BM) || !make_f32_out_map(&tL, q.logits, V, c, ld))
+      return cudaErrorInvalidValue;
+    Params pl{};
+    pl.M = static_cast<int>(c);
+    pl.N = static_cast<int>(V);
+    pl.k_blocks = static_cast<int>((H + BK - 1) / BK);
+    pl.m_tiles = static_cast<int>((c + BM - 1) / BM);
+    pl.n_tiles = static_cast<int>((V + BN - 1) / BN);
+    pl.splits = 1;
+    pl.m_fastest = 1;
+    pl.C = q.logits;
+    pl.ldc = ld;
+    pl.stats = q.stats;
+    pl.c = q.chunk_params.f.c;
+    pl.err = err;
+    cudaError_t e = kH ? launch_gemm<kEpiLogits, false, false, true>(tA, tW_k, tL, pl, stream)
+                       : launch_gemm<kEpiLogits, false, false, false>(tA, tW_k, tL, pl, stream);
     if (e != cudaSuccess) return e;
+    // 2. the row pass
     LinearChunkParams lp = q.chunk_params;
     lp.row0 = r0;
+    lp.logits = q.logits;
+    lp.stats = q.stats;
+    lp.dlogits = q.dlogits;
+    lp.ld = ld;
+    lp.n_stat = static_cast<int>(linear_n_stat(V));
     const dim3 grid(static_cast<unsigned>(c));
-    e = lp.f.entropy ? launch_after_previous(linear_chunk_kernel<1024, kUnroll, true>, grid, dim3(1024), stream, lp)
-                     : launch_after_previous(linear_chunk_kernel<1024, kUnroll, false>, grid, dim3(1024), stream, lp);
+    e = kH ? launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, true>, grid, dim3(kLinearThreads),
+                                   stream, lp)
+           : launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, false>, grid, dim3(kLinearThreads),
+                                   stream, lp);
     if (e != cudaSuccess) return e;
+    CUtensorMap tD;  // dlogits [c, V] bf16 (row stride ld)
     if (q.grad_hidden != nullptr) {
-      // grad_h^T [H, c] = W^T-as-[H, V] x dlogits^T [V, c]
-      e = lt_gemm(false, false, H, c, V, q.weight, H, q.dlogits, ld, q.grad_hidden + r0 * H, H, CUDA_R_32F, 0.f,
-                  q.ws, q.ws_bytes, stream);
+      // 3. grad_h [c, H] = dlogits W, split along the vocabulary, then summed in split order
+      CUtensorMap tDk, tP;
+      Params ph{};
+      ph.M = static_cast<int>(c);
+      ph.N = static_cast<int>(H);
+      ph.k_blocks = static_cast<int>((V + BK - 1) / BK);
+      ph.m_tiles = static_cast<int>((c + BM - 1) / BM);
+      ph.n_tiles = static_cast<int>((H + BN - 1) / BN);
+      const uint64_t split_bytes = static_cast<uint64_t>(c) * H * 4;
+      ph.splits = grad_hidden_splits(int64_t(ph.m_tiles) * ph.n_tiles, ph.k_blocks, q.part_bytes, split_bytes, sms);
+      ph.m_fastest = 1;
+      float* gh = q.grad_hidden + r0 * H;
+      ph.C = ph.splits == 1 ? gh : q.part;
+      ph.ldc = H;
+      ph.split_stride = c * H;
+      ph.err = err;
+      if (!make_operand_map(&tDk, q.dlogits, false, c, V, ld, BM) ||
+          !make_f32_out_map(&tP, ph.C, H, c, H, ph.splits, static_cast<uint64_t>(c * H)))
+        return cudaErrorInvalidValue;
+      e = launch_gemm<kEpiStore, false, true, false>(tDk, tW_mn, tP, ph, stream);
       if (e != cudaSuccess) return e;
+      if (ph.splits > 1) {
+        const int64_t n4 = c * H / 4;
+        const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, int64_t(sms) * 8));
+        e = launch_after_previous(split_sum_kernel, dim3(blocks), dim3(256), stream,
+                                  reinterpret_cast<const float4*>(q.part), reinterpret_cast<float4*>(gh), n4,
+                                  ph.splits, n4);
+        if (e != cudaSuccess) return e;
+      }
     }
     if (q.grad_weight != nullptr) {
-      // grad_W^T [H, V] += h^T [H, c] x dlogits [c, V]
-      e = lt_gemm(false, true, H, V, c, h, H, q.dlogits, ld, q.grad_weight, H, CUDA_R_32F, 1.f, q.ws,
-                  q.ws_bytes, stream);
+      // 4. grad_W [V, H] += dlogits^T h (TMA reduce-add into the caller's fp32 gradient)
+      CUtensorMap tHm;
+      if (!make_operand_map(&tD, q.dlogits, true, V, c, ld, BM) || !make_operand_map(&tHm, h, true, H, c, H, BN))
+        return cudaErrorInvalidValue;
+      Params pw{};
+      pw.M = static_cast<int>(V);
+      pw.N = static_cast<int>(H);
+      pw.k_blocks = static_cast<int>((c + BK - 1) / BK);
+      pw.m_tiles = static_cast<int>((V + BM - 1) / BM);
+      pw.n_tiles = static_cast<int>((H + BN - 1) / BN);
+      pw.splits = 1;
+      pw.m_fastest = 0;
+      pw.C = q.grad_weight;
+      pw.ldc = H;
+      pw.err = err;
+      e = launch_gemm<kEpiAccum, true, true, false>(tD, tHm, tGW, pw, stream);
       if (e != cudaSuccess) return e;
     }
   }
@@ -294,10 +297,10 @@ cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream)
 // For callers that must not allocate device memory at call time (an allocator-free
 // runtime, a host process that has handed all device memory to a pool it does not own, a
 // code path that must not synchronise on an allocation).  The scratch grpo_fused_linear
-// takes from the caller (one chunk's fp32 logits and bf16 dlogits, and the GEMMs'
-// workspace) lives here in one array of kNoallocScratchBytes, reserved in every device
-// context that loads this library and held until the process exits.  Every call uses the
-// whole array: calls that run at the same time on the GPU (different streams, threads or
+// takes from the caller (one chunk's fp32 logits, bf16 dlogits and statistics, and the K
+// splits of grad_hidden) lives here in one array of kNoallocScratchBytes, reserved in every
+// device context that loads this library and held until the process exits.  Every call uses
+// the whole array: calls that run at the same time on the GPU (different streams, threads or
 // host processes sharing the context) race on it.  Nothing in it has to start at zero: each
 // call writes every part before reading it.
 
@@ -305,115 +308,46 @@ namespace grpo {
 namespace {
 
 constexpr uint64_t kNoallocScratchBytes = uint64_t(32) << 20;  // 32 MiB per device
-constexpr uint64_t kNoallocGemmWs = uint64_t(4) << 20;         // of which the GEMMs' workspace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// The array's device address, looked up once per device with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CUcontext current_context() {
+  static const CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  CUcontext ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+// The array's device address, looked up with the device current the first time a device
+// (context) calls, and again whenever the device's context has changed since (a
+// cudaDeviceReset makes a new one, where the array lives at a new address).
 void* noalloc_scratch_address() {
-  static void* addr[64] = {nullptr};
+  struct Entry {
+    CUcontext ctx;
+    void* addr;
+  };
+  static Entry cache[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  cudaFree(nullptr);  // makes the device's primary context current (allocates nothing)
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (cache[dev].addr == nullptr || cache[dev].ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    addr[dev] = p;
+    cache[dev] = Entry{ctx, p};
   }
-  return addr[dev];
-}
-
-// lt_gemm with its descriptors in caller-provided (stack) storage and the chosen
-// algorithms in a fixed table, so that a call allocates nothing, on the host either.
-cudaError_t lt_gemm_noalloc(bool ta, bool tb, int64_t m, int64_t n, int64_t k, const void* A, int64_t lda,
-                            const void* B, int64_t ldb, void* D, int64_t ldd, float beta, void* ws, size_t ws_bytes,
-                            cudaStream_t stream) {
-  cublasLtHandle_t h = lt_handle();
-  if (h == nullptr) return cudaErrorNotSupported;
-  cublasLtMatmulDescOpaque_t op_s;
-  cublasLtMatrixLayoutOpaque_t la_s, lb_s, ld_s;
-  cublasLtMatmulDesc_t op = &op_s;
-  cublasLtMatrixLayout_t la = &la_s, lb = &lb_s, ldl = &ld_s;
-  const cublasOperation_t opa = ta ? CUBLAS_OP_T : CUBLAS_OP_N, opb = tb ? CUBLAS_OP_T : CUBLAS_OP_N;
-  if (cublasLtMatmulDescInit(op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof(opa)) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof(opb)) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutInit(la, CUDA_R_16BF, ta ? k : m, ta ? m : k, lda) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutInit(lb, CUDA_R_16BF, tb ? n : k, tb ? k : n, ldb) != CUBLAS_STATUS_SUCCESS ||
-      cublasLtMatrixLayoutInit(ldl, CUDA_R_32F, m, n, ldd) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorNotSupported;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const GemmKey key{dev, ta, tb, static_cast<int>(CUDA_R_32F), m, n, k, lda, ldb, ldd, ws_bytes};
-  struct Entry {
-    GemmKey key;
-    cublasLtMatmulAlgo_t algo;
-    bool used;
-  };
-  static Entry table[64];
-  static int next = 0;
-  static std::mutex mu;
-  cublasLtMatmulAlgo_t algo;
-  bool have = false;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (const Entry& e : table)
-      if (e.used && !(e.key < key) && !(key < e.key)) {
-        algo = e.algo;
-        have = true;
-        break;
-      }
-  }
-  if (!have) {
-    cublasLtMatmulPreferenceOpaque_t pref_s;
-    cublasLtMatmulPreference_t pref = &pref_s;
-    if (cublasLtMatmulPreferenceInit(pref) != CUBLAS_STATUS_SUCCESS) return cudaErrorNotSupported;
-    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
-                                         sizeof(ws_bytes));
-    cublasLtMatmulHeuristicResult_t res;
-    int found = 0;
-    if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ldl, ldl, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS ||
-        found < 1)
-      return cudaErrorNotSupported;
-    algo = res.algo;
-    std::lock_guard<std::mutex> lock(mu);
-    table[next] = Entry{key, algo, true};  // a fixed table: the oldest entry makes room
-    next = (next + 1) % 64;
-  }
-  const float alpha = 1.f;
-  return cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, D, ldl, D, ldl, &algo, ws, ws_bytes, stream) ==
-                 CUBLAS_STATUS_SUCCESS
-             ? cudaSuccess
-             : cudaErrorLaunchFailure;
-}
-
-cudaError_t launch_fused_linear_noalloc(const FusedLinearParams& q, cudaStream_t stream) {
-  const int64_t R = q.rows, H = q.H, V = q.V, ld = q.ld;
-  for (int64_t r0 = 0; r0 < R; r0 += q.chunk) {
-    const int64_t c = R - r0 < q.chunk ? R - r0 : q.chunk;
-    const uint16_t* h = q.hidden + r0 * H;
-    cudaError_t e = lt_gemm_noalloc(true, false, V, c, H, q.weight, H, h, H, q.logits, ld, 0.f, q.ws, q.ws_bytes,
-                                    stream);
-    if (e != cudaSuccess) return e;
-    LinearChunkParams lp = q.chunk_params;
-    lp.row0 = r0;
-    const dim3 grid(static_cast<unsigned>(c));
-    e = lp.f.entropy ? launch_after_previous(linear_chunk_kernel<1024, kUnroll, true>, grid, dim3(1024), stream, lp)
-                     : launch_after_previous(linear_chunk_kernel<1024, kUnroll, false>, grid, dim3(1024), stream, lp);
-    if (e != cudaSuccess) return e;
-    if (q.grad_hidden != nullptr) {
-      e = lt_gemm_noalloc(false, false, H, c, V, q.weight, H, q.dlogits, ld, q.grad_hidden + r0 * H, H, 0.f, q.ws,
-                          q.ws_bytes, stream);
-      if (e != cudaSuccess) return e;
-    }
-    if (q.grad_weight != nullptr) {
-      e = lt_gemm_noalloc(false, true, H, V, c, h, H, q.dlogits, ld, q.grad_weight, H, 1.f, q.ws, q.ws_bytes,
-                          stream);
-      if (e != cudaSuccess) return e;
-    }
-  }
-  return cudaSuccess;
+  return cache[dev].addr;
 }
 
 bool noalloc_f32(const void* p, bool required) {
@@ -439,12 +373,11 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
     return GRPO_ERR_UNSUPPORTED;
   const int64_t rows = B * L;
   if (rows == 0) return GRPO_OK;
-  const int64_t ld = (V + 7) / 8 * 8;
   const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
-  const uint64_t logits_bytes = (static_cast<uint64_t>(ld) * chunk * 4 + 255) & ~uint64_t(255);
-  const uint64_t dlogits_bytes = (static_cast<uint64_t>(ld) * chunk * 2 + 255) & ~uint64_t(255);
-  // the fixed array's limit: chunk * 6 * ld bytes (rounded to 256) + the GEMMs' 4 MiB <= 32 MiB
-  if (logits_bytes + dlogits_bytes + grpo::kNoallocGemmWs > grpo::kNoallocScratchBytes) return GRPO_ERR_UNSUPPORTED;
+  // the fixed array's limit: the chunk's buffers (fp32 logits, bf16 dlogits, statistics,
+  // each rounded up to 256 bytes) and one chunk of grad_hidden (chunk * H fp32) <= 32 MiB
+  const uint64_t chunk_bytes = grpo::linear_chunk_bytes(V, chunk);
+  if (chunk_bytes + static_cast<uint64_t>(chunk) * H * 4 > grpo::kNoallocScratchBytes) return GRPO_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
   if (!a16(hidden) || !a16(weight)) return GRPO_ERR_INVALID_ARG;
   if (idx == nullptr || (reinterpret_cast<uintptr_t>(idx) % 8) != 0 || !noalloc_f32(old_logp, false) ||
@@ -457,8 +390,7 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
   if (beta != 0.f && !noalloc_f32(ref_logp, true)) return GRPO_ERR_INVALID_ARG;
   if (!noalloc_f32(ref_logp, false)) return GRPO_ERR_INVALID_ARG;
 
-  // set-up on this device's first call: the array's address (and the library's cuBLASLt
-  // handle for the device, created on first use by every GEMM path of this library)
+  // set-up on this device's first call (and after a device reset): the array's address
   char* scratch = static_cast<char*>(grpo::noalloc_scratch_address());
   if (scratch == nullptr) return GRPO_ERR_CUDA;
 
@@ -469,11 +401,8 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
   q.H = H;
   q.V = V;
   q.chunk = chunk;
-  q.ld = ld;
-  q.logits = reinterpret_cast<float*>(scratch);
-  q.dlogits = reinterpret_cast<uint16_t*>(scratch + logits_bytes);
-  q.ws = scratch + logits_bytes + dlogits_bytes;
-  q.ws_bytes = grpo::kNoallocGemmWs;
+  q.ld = grpo::linear_ld(V);
+  grpo::linear_carve(q, scratch, grpo::kNoallocScratchBytes);
   q.grad_hidden = grad_hidden;
   q.grad_weight = grad_weight;
   grpo::LinearChunkParams& cp = q.chunk_params;
@@ -496,12 +425,8 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
   p.is_clipped = is_clipped;
   p.entropy = entropy;
   p.dev_err = dev_err;
-  cp.logits = q.logits;
-  cp.dlogits = q.dlogits;
-  cp.ld = ld;
   cp.dloss = dloss;
   cp.T = T;
-  return grpo::launch_fused_linear_noalloc(q, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? GRPO_OK
-             : GRPO_ERR_CUDA;
+  return grpo::launch_fused_linear(q, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GRPO_OK
+                                                                                              : GRPO_ERR_CUDA;
 }

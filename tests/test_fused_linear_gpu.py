@@ -133,6 +133,49 @@ def test_fused_linear_qwen3_head_rows():
     check_against_oracle(pb, out, "qwen3 head")
 
 
+def test_fused_linear_bench_shape_against_oracle():
+    """The benchmark's LM-head shape (H = 1024, V = 151936: fp32 logit rows of 594 KB, the
+    last 256-column tile half empty) in its launch configuration (chunks of 2048 rows),
+    with one full chunk and a ragged second one (2148 rows): the forward outputs of every
+    row, grad_hidden on sampled rows and grad_weight on sampled vocabulary rows against the
+    oracle on all rows."""
+    spec = W.get("linear_qwen3_b16_l1024_h1024_v151936", B=4, L=537)
+    li = W.generate_linear(spec, 0, device="cpu")
+    R, V, H, T = spec.rows, spec.V, spec.H, spec.T
+    hf, Wf = rows_f64(li.hidden), rows_f64(li.weight)
+    lp0, _ = oracle.selective_log_softmax(hf @ Wf.T, li.idx.numpy(), T)
+    old = oracle.round_to_fp32(lp0 + li.old_offset.double().numpy())
+    ref = oracle.round_to_fp32(lp0 + li.ref_offset.double().numpy())
+    pb = dict(h=li.hidden, W=li.weight, idx=li.idx, adv=li.adv, mask=li.mask, dloss=li.dloss, old=old, ref=ref, T=T,
+              beta=spec.beta, el=spec.eps_low, eh=spec.eps_high, B=spec.B, L=spec.L, hf=hf, Wf=Wf)
+    out, err = run_gpu(pb, 2048)
+    assert err == 0
+    adv_row = oracle.per_row(li.adv.numpy(), spec.L)
+    mask = li.mask.numpy()
+    f, gh, gW, dx = oracle.fused_linear_grpo(hf, Wf, li.idx.numpy(), old, ref, adv_row, mask,
+                                             li.dloss.double().numpy(), T, spec.beta, spec.eps_low, spec.eps_high)
+    for k in ("loss", "logp", "lse", "kl", "entropy"):
+        assert_scalar_close(out[k], f[k], f"bench shape {k}")
+    amb = ambiguous_rows(f["ratio"], adv_row, mask, spec.eps_low, spec.eps_high)
+    clip = out["is_clipped"].cpu().numpy().astype(bool)
+    assert np.array_equal(clip[~amb], f["is_clipped"][~amb]), "bench shape is_clipped"
+    assert (mask == 0).any() and (mask != 0).any()
+
+    rows = np.unique(np.concatenate([W.sample_rows(R, 48, 1), [0, 2047, 2048, R - 1]]))
+    got_h = out["grad_hidden"].double().cpu().numpy()[rows]
+    bound_h = 2.0 ** -8 * (np.abs(dx[rows]) @ np.abs(Wf)) + 1e-5 * np.abs(gh[rows]) + 1e-7
+    bad = np.abs(got_h - gh[rows]) > bound_h
+    assert not bad.any(), f"grad_hidden: {bad.sum()} elements out, worst {np.abs(got_h - gh[rows])[bad].max():.3g}"
+    assert np.all(got_h[np.all(dx[rows] == 0.0, axis=1)] == 0.0)
+
+    cols = np.unique(np.concatenate([W.sample_rows(V, 40, 2), li.idx.numpy()[rows[:8]],
+                                     np.arange(V - 130, V), [V - 257, 255, 256]]))
+    got_W = out["grad_weight"].double().cpu().numpy()[cols]
+    bound_W = 2.0 ** -8 * (np.abs(dx[:, cols]).T @ np.abs(hf)) + 1e-5 * np.abs(gW[cols]) + 1e-7
+    bad = np.abs(got_W - gW[cols]) > bound_W
+    assert not bad.any(), f"grad_weight: {bad.sum()} elements out, worst {np.abs(got_W - gW[cols])[bad].max():.3g}"
+
+
 def test_fused_linear_out_of_range_idx_is_flagged():
     """The row's logp is NaN and the error bit is set; with beta > 0 its row factor is NaN
     too, so its dlogits and hidden-state gradient are NaN (with beta = 0 and no old_logp
