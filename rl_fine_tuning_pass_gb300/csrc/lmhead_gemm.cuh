@@ -14,25 +14,30 @@
 //   kEpiAccum   D is added to the fp32 output (grad_weight += dlogits^T h: M = V, N = H,
 //               K = rows).
 //
-// Layout and pipeline.  One persistent CTA per SM walks a static list of 128 x 256 output
-// tiles (and K splits).  Warp 0 streams the operands with TMA into a 4-stage ring of
-// 128-byte-swizzled shared-memory tiles (64 K-elements deep: A 16 KB, B 32 KB); warp 1
-// allocates 512 TMEM columns (two 256-column fp32 accumulators) and one of its threads
-// issues tcgen05.mma (M = 128, N = 256, K = 16) for every 16-deep slice; warps 2-9 read the
-// finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes = 32 rows of
-// its quarter; two warps share a quarter, one for each half of the columns) while the MMAs
-// of the next tile fill the other accumulator.  Each warp writes 32 x 32 fp32 boxes into
-// its 128-byte-swizzled staging buffer and one lane stores them with a TMA tensor store
-// (kEpiLogits, kEpiStore) or a TMA reduce-add (kEpiAccum); the tensor maps clip the ragged
-// edges.  Operands may be K-major (K
-// contiguous: h, W in the logits GEMM, dlogits in grad_hidden) or MN-major (M or N
-// contiguous: W in grad_hidden, dlogits^T and h in grad_weight); the MN-major tiles are
-// loaded as 64-wide boxes and described to the MMA with the MN-major bit.
+// Layout and pipeline.  The kernel runs on pairs of CTAs (a cluster of two SMs); a pair
+// computes one 256 x 256 output tile at a time with tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16): each CTA stages its 128 rows of A and its 128 columns of B, so each SM
+// moves a third less operand data through shared memory than a one-SM 128 x 256 tile would.
+// In each CTA, warp 0 streams that CTA's halves with TMA into a 6-stage ring of
+// 128-byte-swizzled tiles (64 K-elements deep: 16 KB of A and 16 KB of B), signalling the
+// pair's leader (cluster rank 0); warp 1 holds 512 TMEM columns (two 256-column fp32
+// accumulators, allocated for the pair), and one thread of the leader's warp 1 issues the
+// MMAs and commits them to both CTAs' barriers.  Warps 2-9 of each CTA read its 128 rows
+// of the finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes of its
+// quarter; two warps share a quarter, one for each half of the columns) while the MMAs of
+// the next tile fill the other accumulator.  Each warp passes its 32 x 32 fp32 boxes through
+// a 128-byte-swizzled staging buffer (one row per lane in, four rows of 128 bytes per
+// instruction out), so that its global stores (kEpiLogits, kEpiStore) or vector reduce-adds
+// (kEpiAccum) write whole 128-byte lines; stores are fire-and-forget, so many lines per SM
+// are in flight.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
+// grad_hidden) or MN-major (M or N contiguous: W in grad_hidden, dlogits^T and h in
+// grad_weight); the MN-major tiles are loaded as 64-wide boxes and described to the MMA
+// with the MN-major bit.
 //
 // Every wait on an mbarrier gives up after about two seconds: it sets the CTA's abort flag,
 // every role leaves its loop, the in-flight copies and MMAs are waited for (again with a
-// limit), TMEM is freed and the kernel returns with GRPO_DEVERR_TIMEOUT_BIT set in the
-// caller's error word.  Nothing traps.
+// limit), both CTAs of the pair meet at a cluster barrier, TMEM is freed and the kernel
+// returns with GRPO_DEVERR_TIMEOUT_BIT set in the caller's error word.  Nothing traps.
 #pragma once
 
 #include <cuda.h>
@@ -46,14 +51,15 @@
 namespace grpo {
 namespace gemm {
 
-constexpr int BM = 128;     // rows of a tile (TMEM lanes)
+constexpr int BM = 128;     // rows of a CTA's half tile (TMEM lanes); the pair's tile has 2 BM
 constexpr int BN = 256;     // columns of a tile (TMEM columns of one accumulator)
+constexpr int BNH = BN / 2;  // columns of B each CTA of the pair stages
 constexpr int BK = 64;      // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;   // two per TMEM lane quarter, each half of the tile's columns
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
-constexpr uint32_t kStageA = BM * BK * 2;  // 16 KB
-constexpr uint32_t kStageB = BN * BK * 2;  // 32 KB
+constexpr uint32_t kStageA = BM * BK * 2;   // 16 KB
+constexpr uint32_t kStageB = BNH * BK * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr uint32_t kStageC = 32 * 32 * 4;        // one epilogue warp's 32 x 32 fp32 output box
 constexpr uint32_t kSmemC = kEpiWarps * kStageC;  // one staging box per epilogue warp
@@ -66,14 +72,15 @@ enum Epi : int { kEpiLogits = 0, kEpiStore = 1, kEpiAccum = 2 };
 struct Params {
   int M, N;            // output rows and columns
   int k_blocks;        // ceil(K / 64)
-  int m_tiles, n_tiles, splits;
+  int m_tiles, n_tiles, splits;  // m_tiles counts the pair's 256-row tiles
   int m_fastest;       // 1: consecutive tiles share a B tile; 0: share an A tile
-  float* C;            // fp32 output [M][ldc] (+ split * split_stride)
+  float* C;            // fp32 output [M][ldc] (+ split * split_stride); ldc a multiple of 4
   int64_t ldc, split_stride;
   // kEpiLogits only
   float4* stats;       // [M][2 n_tiles]: (a, s, u, 0) of each half tile's 128 columns
   float c;             // log2(e) / T
   int* err;            // device error word (nullable)
+  int pair_limit;      // at most this many CTA pairs (0: as many as fit on the GPU)
 };
 
 // ---------------------------------------------------------------------------
@@ -117,43 +124,52 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
+// A TMA load into this CTA's shared memory whose completion is signalled on `bar`, a
+// shared::cluster address that may be the pair leader's barrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// No committed bulk group of this thread still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of this CTA's shared variable at `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Both CTAs of the pair reach this point (every thread of both).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// An arrival that orders nothing but this thread's completed tcgen05 reads before it (the
+// tcgen05.fence::before_thread_sync ahead of it): relaxed, so that it does not wait for the
+// thread's global stores still in flight.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
 
 // Shared-memory matrix descriptor of a 128-byte-swizzled tile (start, leading and stride
 // byte offsets in 16-byte units, descriptor version 1, swizzle mode 2 = 128 B).
@@ -166,26 +182,38 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, their majorness,
-// N / 8 and M / 16.
+// N / 8 and M / 16 (M = 256: the pair's tile).
 template <bool A_MN, bool B_MN>
 __host__ __device__ constexpr uint32_t idesc_bf16() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 }
+// Issued by one thread of the pair's leader: D[256 x 256] (+)= A B, A's rows 0-127 and B's
+// columns 0-127 from this CTA's shared memory, the rest from the peer's at the same offsets;
+// each CTA's TMEM receives its 128 rows.
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
           tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// Arrive on the barrier at offset `bar` in both CTAs of the pair once every MMA this thread
+// issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
 }
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// Arrive on this CTA's barrier `bar` once every MMA this thread issued has completed.
+__device__ __forceinline__ void umma_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread), without
+// waiting for them (tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float (&v)[32]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
       "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -194,10 +222,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // The tile list: tile t -> (m, n, split) and the split's K blocks [kb0, kb1).
 struct Tile {
@@ -237,6 +263,39 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&
   }
 }
 
+// Write a staged 32 x 32 box to rows [0, rows) and columns [0, cols) of the fp32 matrix at
+// `dst` (row stride ld, a multiple of 4): lane l takes 16-byte chunk l % 8 of rows
+// l / 8 + 4 i, so each instruction covers four whole 128-byte rows.  kEpiAccum adds instead.
+template <int EPI>
+__device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, int64_t ld, int rows, int cols) {
+  const int q = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    float4 x;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                 : "r"(buf + static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) * 16))));
+    if (r >= rows || 4 * q >= cols) continue;
+    float* d = dst + r * ld + 4 * q;
+    if (4 * q + 4 <= cols) {
+      if constexpr (EPI == kEpiAccum)
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(d), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
+                     : "memory");
+      else
+        *reinterpret_cast<float4*>(d) = x;
+    } else {
+      const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (4 * q + k >= cols) break;
+        if constexpr (EPI == kEpiAccum) atomicAdd(d + k, e[k]);
+        else d[k] = e[k];
+      }
+    }
+  }
+}
+
 // Fold 32 logits (the first `valid` of them) into the tile's running statistic, with the
 // numerics of the row kernels' stream (rowpass_fwd.cuh: one rescale per chunk, packed f32x2
 // sums).
@@ -268,8 +327,7 @@ __device__ __forceinline__ void stat_cols(Running& rs, float (&v)[32], int valid
 // ---------------------------------------------------------------------------
 template <int EPI, bool A_MN, bool B_MN, bool kH>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -277,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sB = smem + kStages * kStageA;
   unsigned char* sC = sB + kStages * kStageB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kSmemC);
-  // full[s], empty[s], tmem_full[2], tmem_empty[2], drain
+  // full[s] (the leader's are used), empty[s], tmem_full[2], tmem_empty[2] (the leader's),
+  // drain
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
@@ -285,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the pair's leader, which issues the MMAs
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -292,57 +353,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpiWarps * 32);
+      mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);  // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
-    prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   wait_for_previous_grids();
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = p.m_tiles * p.n_tiles * p.splits;
+  const int first = static_cast<int>(cluster_id()), step = static_cast<int>(cluster_count());
 
   if (warp == 0) {
-    // ---- TMA producer ----
+    // ---- TMA producer (each CTA its halves of A and B) ----
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // stages filled and not yet known to be consumed (for the abort path)
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = first; t < total && ok; t += step) {
         const Tile u = tile_of(p, t);
+        const int arow = u.m * 2 * BM + static_cast<int>(rank) * BM;  // this CTA's A rows
+        const int bcol = u.n * BN + static_cast<int>(rank) * BNH;      // this CTA's B columns
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, kStageA + kStageB);
+          // both CTAs' copies complete on the leader's full barrier, which expects them all
+          const uint32_t fb = map_to_rank(full0 + 8 * stage, 0);
+          if (leader) mbar_expect_tx(full0 + 8 * stage, 2 * (kStageA + kStageB));
           const uint32_t a_dst = smem_u32(sA + stage * kStageA), b_dst = smem_u32(sB + stage * kStageB);
           const int k0 = kb * BK;
           if constexpr (A_MN) {
-            tma_load_2d(a_dst, &tmA, u.m * BM, k0, fb);
-            tma_load_2d(a_dst + 8192, &tmA, u.m * BM + 64, k0, fb);
+            tma_load_2d(a_dst, &tmA, arow, k0, fb);
+            tma_load_2d(a_dst + 8192, &tmA, arow + 64, k0, fb);
           } else {
-            tma_load_2d(a_dst, &tmA, k0, u.m * BM, fb);
+            tma_load_2d(a_dst, &tmA, k0, arow, fb);
           }
           if constexpr (B_MN) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tma_load_2d(b_dst + 8192 * i, &tmB, u.n * BN + 64 * i, k0, fb);
+            tma_load_2d(b_dst, &tmB, bcol, k0, fb);
+            tma_load_2d(b_dst + 8192, &tmB, bcol + 64, k0, fb);
           } else {
-            tma_load_2d(b_dst, &tmB, k0, u.n * BN, fb);
+            tma_load_2d(b_dst, &tmB, k0, bcol, fb);
           }
           issued = issued < kStages ? issued + 1 : kStages;
           if (++stage == kStages) {
@@ -351,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // copies may still be landing in the ring: wait (bounded) for each stage's full
         // phase before the CTA's shared memory can go away
         for (int i = 0; i < issued; ++i) {
@@ -365,14 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer ----
-    if (lane == 0) {
+    // ---- MMA issuer: one thread of the leader ----
+    if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16<A_MN, B_MN>();
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++local) {
+      for (int t = first; t < total && ok; t += step, ++local) {
         const Tile u = tile_of(p, t);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
@@ -392,16 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = B_MN ? sw128_desc(b_base + kk * 2048, 8192, 1024) : sw128_desc(b_base + kk * 32, 16, 1024);
             umma_bf16(d, ad, bd, idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(empty0 + 8 * stage);  // the stage is free once these MMAs are done
+          umma_commit_pair(empty0 + 8 * stage);  // both CTAs' stage is free once these MMAs are done
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(tfull0 + 8 * acc);  // the accumulator is ready
+        if (ok) umma_commit_pair(tfull0 + 8 * acc);  // both CTAs' accumulator halves are ready
       }
-      // no MMA may still be running when TMEM is freed
-      umma_commit(drain);
+      // no MMA may still be writing either CTA's TMEM when it is freed
+      umma_commit_local(drain);
       mbar_wait(drain, 0, abort_flag, false);
     }
     __syncwarp();
@@ -411,58 +475,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
     int local = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
+    for (int t = first; t < total; t += step, ++local) {
       const Tile u = tile_of(p, t);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const int row0 = u.m * BM + quarter * 32;  // this warp's first row
+      const int row0 = u.m * 2 * BM + static_cast<int>(rank) * BM + quarter * 32;  // this warp's first row
       const int row = row0 + lane;
       const bool row_ok = row < p.M;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN + half * (BN / 2));
       const int col_base = u.n * BN + half * (BN / 2);
+      float* cbase = p.C + static_cast<int64_t>(u.s) * p.split_stride;
       Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
+      const int boxes = min(BN / 64, (p.N - col_base + 31) / 32);  // boxes with columns below N
+      // all of this warp's 128 accumulator columns into registers with one wait, then the
+      // accumulator goes back to the MMA while the statistic and the stores proceed
+      float v[BN / 64][32];
+#pragma unroll
+      for (int j = 0; j < BN / 64; ++j) tmem_ld32_async(taddr + 32 * j, v[j]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(map_to_rank(tempty0 + 8 * acc, 0));  // done with it
+#pragma unroll
       for (int j = 0; j < BN / 64; ++j) {
+        if (j >= boxes) break;
         const int col0 = col_base + 32 * j;
         const int valid = p.N - col0;
-        if (valid <= 0) break;  // the rest of the tile lies beyond the last column
-        float v[32];
-        tmem_ld32(taddr + 32 * j, v);
-        // the staging box must have been read out by the previous box's TMA
-        if (lane == 0) bulk_wait_read_0();
-        __syncwarp();
-        stage_row(buf, lane, v);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (EPI == kEpiLogits) tma_store_2d(&tmC, buf, col0, row0);
-          else if constexpr (EPI == kEpiStore) tma_store_3d(&tmC, buf, col0, row0, u.s);
-          else tma_reduce_add_2d(&tmC, buf, col0, row0);
-          bulk_commit();
-        }
         if constexpr (EPI == kEpiLogits) {
-          if (row_ok) stat_cols<kH>(rs, v, valid, p.c);
+          if (row_ok) stat_cols<kH>(rs, v[j], valid, p.c);  // columns at or past N become -inf, not stored
         }
+        stage_row(buf, lane, v[j]);
+        __syncwarp();
+        write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, p.M - row0, valid);
+        __syncwarp();  // every lane has read the box before the next one is staged
       }
       if constexpr (EPI == kEpiLogits) {
         if (row_ok && col_base < p.N)
           p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] =
               make_float4(rs.a, rs.s.x + rs.s.y, rs.u.x + rs.u.y, 0.f);
       }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8 * acc);  // this thread is done with the accumulator
     }
-    if (lane == 0) bulk_wait_all();  // every output box written before the CTA ends
-    __syncwarp();
   }
   __syncthreads();
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other's copies, MMAs or arrivals may target it
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
   if (threadIdx.x == 0 && *abort_flag && p.err != nullptr) atomicOr(p.err, GRPO_DEVERR_TIMEOUT_BIT);
 }
@@ -512,53 +575,58 @@ inline bool make_operand_map(CUtensorMap* map, const void* base, bool mn_major, 
                   : make_bf16_map(map, base, k, mn, row_elems, BK, mn_box);
 }
 
-// The fp32 output [depth][outer][inner] (depth = K splits, `depth_elems` apart; rows
-// `row_elems` apart) written in 32 x 32 boxes through the 128-byte-swizzled staging
-// buffers; rank 3 when depth_elems != 0, else rank 2.  Elements outside the extents are
-// not written.
-inline bool make_f32_out_map(CUtensorMap* map, void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
-                             uint64_t depth = 1, uint64_t depth_elems = 0) {
-  const TensorMapEncodeFn enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  const cuuint32_t rank = depth_elems != 0 ? 3 : 2;
-  const cuuint64_t dims[3] = {inner, outer, depth};
-  const cuuint64_t strides[2] = {row_elems * 4, depth_elems * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
-  const cuuint32_t elem_strides[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, base, dims, strides, box, elem_strides,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 inline int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
+  static int count_of_device[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (count_of_device[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    count_of_device[dev] = n;
+  }
+  return count_of_device[dev];
 }
 
-// Launch one GEMM: the grid is min(tiles, SMs) persistent CTAs (one per SM).
+// Launch one GEMM: min(tiles, the pairs that fit at once) persistent CTA pairs.  The
+// kernel's shared-memory attribute and its number of co-resident pairs are set up once per
+// device (the occupancy query costs far more host time than a launch).
 template <int EPI, bool A_MN, bool B_MN, bool kH>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const Params& p,
-                        cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t stream) {
   auto kernel = gemm_kernel<EPI, A_MN, B_MN, kH>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   const int total = p.m_tiles * p.n_tiles * p.splits;
   if (total <= 0) return cudaSuccess;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
+  static int pairs_of_device[64] = {};  // 0: not yet known
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a, b, c, p);
+  int pairs = pairs_of_device[dev];
+  if (pairs == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    cfg.gridDim = dim3(2 * 512);
+    e = cudaOccupancyMaxActiveClusters(&pairs, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (pairs <= 0) return cudaErrorInvalidConfiguration;
+    pairs_of_device[dev] = pairs;
+  }
+  if (p.pair_limit > 0 && p.pair_limit < pairs) pairs = p.pair_limit;
+  cfg.numAttrs = 2;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (total < pairs ? total : pairs)));
+  return cudaLaunchKernelEx(&cfg, kernel, a, b, p);
 }
 
 }  // namespace gemm

@@ -181,12 +181,19 @@ struct LinearChunkParams {
                           // sequence, f.x.V = vocabulary
   const float* logits;    // the chunk's logits [rows][ld] fp32
   const float4* stats;    // the chunk's per-128-column statistics [rows][n_stat]
-  uint16_t* dlogits;      // the chunk's dlogits [rows][ld] bf16
+  uint16_t* dlogits;      // the chunk's dlogits [rows][ld] bf16 (written)
   int64_t ld;             // elements between rows, a multiple of 8
   int n_stat;             // statistics slots per row (two per 256-column tile)
   int64_t row0;           // the chunk's first row in the batch
   const float* dloss;     // [batch rows]
   float T;
+};
+// One chunk's buffers: its fp32 logits [chunk][ld], bf16 dlogits [chunk][ld] and the
+// statistics of the logits GEMM [chunk][2 ceil(V / 256)].
+struct LinearChunkBufs {
+  float* logits;
+  uint16_t* dlogits;
+  float4* stats;
 };
 struct FusedLinearParams {
   const uint16_t* hidden;  // [rows][H] bf16
@@ -194,9 +201,7 @@ struct FusedLinearParams {
   int64_t rows, H, V;
   int64_t chunk;           // rows per chunk
   int64_t ld;              // row stride of the chunk buffers (V rounded up to 8)
-  float* logits;           // workspace: [chunk][ld] fp32
-  uint16_t* dlogits;       // workspace: [chunk][ld] bf16
-  float4* stats;           // workspace: [chunk][2 ceil(V / 256)] statistics of the logits GEMM
+  LinearChunkBufs bufs;    // workspace: one chunk's buffers
   float* part;             // workspace: the K splits of grad_hidden [splits][chunk][H] fp32
   uint64_t part_bytes;     // its size (sets the number of splits)
   float* grad_hidden;      // [rows][H] fp32, or null
@@ -212,14 +217,13 @@ inline uint64_t linear_chunk_bytes(int64_t V, int64_t chunk) {
   return linear_round256(ld * c * 4) + linear_round256(ld * c * 2) +
          linear_round256(static_cast<uint64_t>(linear_n_stat(V)) * c * 16);
 }
-// Carve the chunk buffers out of `base`; the rest (part_bytes) holds grad_hidden's K splits.
+// Carve the chunk buffers out of `base`; the rest of total_bytes holds grad_hidden's K splits.
 inline void linear_carve(FusedLinearParams& q, char* base, uint64_t total_bytes) {
   const uint64_t ld = static_cast<uint64_t>(q.ld), c = static_cast<uint64_t>(q.chunk);
   const uint64_t lb = linear_round256(ld * c * 4), db = linear_round256(ld * c * 2);
   const uint64_t sb = linear_round256(static_cast<uint64_t>(linear_n_stat(q.V)) * c * 16);
-  q.logits = reinterpret_cast<float*>(base);
-  q.dlogits = reinterpret_cast<uint16_t*>(base + lb);
-  q.stats = reinterpret_cast<float4*>(base + lb + db);
+  q.bufs = LinearChunkBufs{reinterpret_cast<float*>(base), reinterpret_cast<uint16_t*>(base + lb),
+                           reinterpret_cast<float4*>(base + lb + db)};
   q.part = reinterpret_cast<float*>(base + lb + db + sb);
   q.part_bytes = total_bytes - (lb + db + sb);
 }

@@ -164,16 +164,16 @@ __global__ void __launch_bounds__(256) split_sum_kernel(const float4* __restrict
 }
 
 // K splits of grad_hidden's GEMM: as many as the workspace holds (at most 32), picked so
-// that the split tiles fill the persistent CTAs' passes most evenly.
-int grad_hidden_splits(int64_t tiles, int64_t k_blocks, uint64_t part_bytes, uint64_t split_bytes, int sms) {
+// that the split tiles fill the persistent CTA pairs' passes most evenly.
+int grad_hidden_splits(int64_t tiles, int64_t k_blocks, uint64_t part_bytes, uint64_t split_bytes, int pairs) {
   int best = 1;
   double best_eff = 0.0;
   const int64_t cap = std::min<int64_t>(32, std::min<int64_t>(k_blocks, static_cast<int64_t>(part_bytes / split_bytes)));
   for (int s = 1; s <= cap; ++s) {
     const int64_t units = tiles * s;
-    const int64_t grid = std::min<int64_t>(units, sms);
+    const int64_t grid = std::min<int64_t>(units, pairs);
     const int64_t passes = (units + grid - 1) / grid;
-    const double eff = static_cast<double>(units) / static_cast<double>(passes * sms);
+    const double eff = static_cast<double>(units) / static_cast<double>(passes * pairs);
     if (eff > best_eff + 1e-3) {
       best_eff = eff;
       best = s;
@@ -184,106 +184,136 @@ int grad_hidden_splits(int64_t tiles, int64_t k_blocks, uint64_t part_bytes, uin
 
 }  // namespace
 
-cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream) {
-  using namespace gemm;
-  const int64_t R = q.rows, H = q.H, V = q.V, ld = q.ld;
-  const bool kH = q.chunk_params.f.entropy != nullptr;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  int* err = q.chunk_params.f.dev_err;
-  CUtensorMap tW_k, tW_mn;  // the head weight, K-major (logits) and MN-major (grad_hidden)
-  if (!make_operand_map(&tW_k, q.weight, false, V, H, H, BN) || !make_operand_map(&tW_mn, q.weight, true, H, V, H, BN))
-    return cudaErrorInvalidValue;
-  CUtensorMap tGW;
-  if (q.grad_weight != nullptr && !make_f32_out_map(&tGW, q.grad_weight, H, V, H)) return cudaErrorInvalidValue;
-  for (int64_t r0 = 0; r0 < R; r0 += q.chunk) {
-    const int64_t c = R - r0 < q.chunk ? R - r0 : q.chunk;
-    const uint16_t* h = q.hidden + r0 * H;
-    // 1. logits [c, V] fp32 = h W^T, with the statistics of every 128 columns
-    CUtensorMap tA, tL;
-    if (!make_operand_map(&tA, h, false, c, H, H, BM) || !make_f32_out_map(&tL, q.logits, V, c, ld))
-      return cudaErrorInvalidValue;
+namespace {
+
+// The launches of one fused-linear call: the head weight's tensor maps, made once, and one
+// function per stage of a chunk.
+struct LinearLauncher {
+  const FusedLinearParams& q;
+  bool kH;
+  int sms;
+  CUtensorMap tW_k, tW_mn;  // the head weight K-major (logits) and MN-major (grad_hidden)
+
+  explicit LinearLauncher(const FusedLinearParams& params) : q(params) {
+    kH = q.chunk_params.f.entropy != nullptr;
+    sms = gemm::sm_count();
+  }
+  bool init() {
+    using namespace gemm;
+    if (sms <= 0) return false;
+    return make_operand_map(&tW_k, q.weight, false, q.V, q.H, q.H, BNH) &&
+           make_operand_map(&tW_mn, q.weight, true, q.H, q.V, q.H, BNH);
+  }
+
+  // logits [c, V] fp32 = h W^T, with the statistics of every 128 columns
+  cudaError_t logits(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
+    using namespace gemm;
+    CUtensorMap tA;
+    if (!make_operand_map(&tA, q.hidden + r0 * q.H, false, c, q.H, q.H, BM)) return cudaErrorInvalidValue;
     Params pl{};
     pl.M = static_cast<int>(c);
-    pl.N = static_cast<int>(V);
-    pl.k_blocks = static_cast<int>((H + BK - 1) / BK);
-    pl.m_tiles = static_cast<int>((c + BM - 1) / BM);
-    pl.n_tiles = static_cast<int>((V + BN - 1) / BN);
+    pl.N = static_cast<int>(q.V);
+    pl.k_blocks = static_cast<int>((q.H + BK - 1) / BK);
+    pl.m_tiles = static_cast<int>((c + 2 * BM - 1) / (2 * BM));
+    pl.n_tiles = static_cast<int>((q.V + BN - 1) / BN);
     pl.splits = 1;
     pl.m_fastest = 1;
-    pl.C = q.logits;
-    pl.ldc = ld;
-    pl.stats = q.stats;
+    pl.C = b.logits;
+    pl.ldc = q.ld;
+    pl.stats = b.stats;
     pl.c = q.chunk_params.f.c;
-    pl.err = err;
-    cudaError_t e = kH ? launch_gemm<kEpiLogits, false, false, true>(tA, tW_k, tL, pl, stream)
-                       : launch_gemm<kEpiLogits, false, false, false>(tA, tW_k, tL, pl, stream);
-    if (e != cudaSuccess) return e;
-    // 2. the row pass
+    pl.err = q.chunk_params.f.dev_err;
+    return kH ? launch_gemm<kEpiLogits, false, false, true>(tA, tW_k, pl, s)
+              : launch_gemm<kEpiLogits, false, false, false>(tA, tW_k, pl, s);
+  }
+
+  // the row pass: forward outputs and bf16 dlogits of the chunk
+  cudaError_t rows(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
     LinearChunkParams lp = q.chunk_params;
     lp.row0 = r0;
-    lp.logits = q.logits;
-    lp.stats = q.stats;
-    lp.dlogits = q.dlogits;
-    lp.ld = ld;
-    lp.n_stat = static_cast<int>(linear_n_stat(V));
+    lp.logits = b.logits;
+    lp.stats = b.stats;
+    lp.dlogits = b.dlogits;
+    lp.ld = q.ld;
+    lp.n_stat = static_cast<int>(linear_n_stat(q.V));
     const dim3 grid(static_cast<unsigned>(c));
-    e = kH ? launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, true>, grid, dim3(kLinearThreads),
-                                   stream, lp)
-           : launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, false>, grid, dim3(kLinearThreads),
-                                   stream, lp);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tD;  // dlogits [c, V] bf16 (row stride ld)
+    return kH ? launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, true>, grid,
+                                      dim3(kLinearThreads), s, lp)
+              : launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, false>, grid,
+                                      dim3(kLinearThreads), s, lp);
+  }
+
+  // grad_h [c, H] = dlogits W (split along the vocabulary, the splits summed in order) and
+  // grad_W [V, H] += dlogits^T h (vector reduce-adds into the caller's fp32 gradient)
+  cudaError_t grads(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
+    using namespace gemm;
+    const int64_t H = q.H, V = q.V;
+    cudaError_t e = cudaSuccess;
     if (q.grad_hidden != nullptr) {
-      // 3. grad_h [c, H] = dlogits W, split along the vocabulary, then summed in split order
-      CUtensorMap tDk, tP;
+      CUtensorMap tDk;
       Params ph{};
       ph.M = static_cast<int>(c);
       ph.N = static_cast<int>(H);
       ph.k_blocks = static_cast<int>((V + BK - 1) / BK);
-      ph.m_tiles = static_cast<int>((c + BM - 1) / BM);
+      ph.m_tiles = static_cast<int>((c + 2 * BM - 1) / (2 * BM));
       ph.n_tiles = static_cast<int>((H + BN - 1) / BN);
       const uint64_t split_bytes = static_cast<uint64_t>(c) * H * 4;
-      ph.splits = grad_hidden_splits(int64_t(ph.m_tiles) * ph.n_tiles, ph.k_blocks, q.part_bytes, split_bytes, sms);
+      ph.splits = grad_hidden_splits(int64_t(ph.m_tiles) * ph.n_tiles, ph.k_blocks, q.part_bytes, split_bytes,
+                                     sms / 2);
       ph.m_fastest = 1;
       float* gh = q.grad_hidden + r0 * H;
       ph.C = ph.splits == 1 ? gh : q.part;
       ph.ldc = H;
       ph.split_stride = c * H;
-      ph.err = err;
-      if (!make_operand_map(&tDk, q.dlogits, false, c, V, ld, BM) ||
-          !make_f32_out_map(&tP, ph.C, H, c, H, ph.splits, static_cast<uint64_t>(c * H)))
-        return cudaErrorInvalidValue;
-      e = launch_gemm<kEpiStore, false, true, false>(tDk, tW_mn, tP, ph, stream);
+      ph.err = q.chunk_params.f.dev_err;
+      if (!make_operand_map(&tDk, b.dlogits, false, c, V, q.ld, BM)) return cudaErrorInvalidValue;
+      e = launch_gemm<kEpiStore, false, true, false>(tDk, tW_mn, ph, s);
       if (e != cudaSuccess) return e;
       if (ph.splits > 1) {
         const int64_t n4 = c * H / 4;
         const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, int64_t(sms) * 8));
-        e = launch_after_previous(split_sum_kernel, dim3(blocks), dim3(256), stream,
+        e = launch_after_previous(split_sum_kernel, dim3(blocks), dim3(256), s,
                                   reinterpret_cast<const float4*>(q.part), reinterpret_cast<float4*>(gh), n4,
                                   ph.splits, n4);
         if (e != cudaSuccess) return e;
       }
     }
     if (q.grad_weight != nullptr) {
-      // 4. grad_W [V, H] += dlogits^T h (TMA reduce-add into the caller's fp32 gradient)
-      CUtensorMap tHm;
-      if (!make_operand_map(&tD, q.dlogits, true, V, c, ld, BM) || !make_operand_map(&tHm, h, true, H, c, H, BN))
+      CUtensorMap tD, tHm;
+      if (!make_operand_map(&tD, b.dlogits, true, V, c, q.ld, BM) ||
+          !make_operand_map(&tHm, q.hidden + r0 * H, true, H, c, H, BNH))
         return cudaErrorInvalidValue;
       Params pw{};
       pw.M = static_cast<int>(V);
       pw.N = static_cast<int>(H);
       pw.k_blocks = static_cast<int>((c + BK - 1) / BK);
-      pw.m_tiles = static_cast<int>((V + BM - 1) / BM);
+      pw.m_tiles = static_cast<int>((V + 2 * BM - 1) / (2 * BM));
       pw.n_tiles = static_cast<int>((H + BN - 1) / BN);
       pw.splits = 1;
       pw.m_fastest = 0;
       pw.C = q.grad_weight;
       pw.ldc = H;
-      pw.err = err;
-      e = launch_gemm<kEpiAccum, true, true, false>(tD, tHm, tGW, pw, stream);
-      if (e != cudaSuccess) return e;
+      pw.err = q.chunk_params.f.dev_err;
+      e = launch_gemm<kEpiAccum, true, true, false>(tD, tHm, pw, s);
     }
+    return e;
+  }
+};
+
+}  // namespace
+
+cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream) {
+  LinearLauncher run(q);
+  if (!run.init()) return cudaErrorInvalidValue;
+  // logits, row pass and gradients of each chunk in turn.  (Running a chunk's row pass on a
+  // second stream next to its neighbours' GEMMs, with two sets of chunk buffers, measured no
+  // faster: the GEMMs and the row pass both lean on the L2 and DRAM bandwidth they share.)
+  for (int64_t r0 = 0; r0 < q.rows; r0 += q.chunk) {
+    const int64_t c = std::min(q.chunk, q.rows - r0);
+    cudaError_t e = run.logits(q.bufs, r0, c, stream);
+    if (e == cudaSuccess) e = run.rows(q.bufs, r0, c, stream);
+    if (e == cudaSuccess) e = run.grads(q.bufs, r0, c, stream);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
