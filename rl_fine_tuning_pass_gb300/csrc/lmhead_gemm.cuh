@@ -86,9 +86,6 @@ struct Params {
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -139,31 +136,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// The shared::cluster address of this CTA's shared variable at `addr` in CTA `rank`.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Both CTAs of the pair reach this point (every thread of both).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // An arrival that orders nothing but this thread's completed tcgen05 reads before it (the
 // tcgen05.fence::before_thread_sync ahead of it): relaxed, so that it does not wait for the
 // thread's global stores still in flight.
@@ -337,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sC + kSmemC);
   // full[s] (the leader's are used), empty[s], tmem_full[2], tmem_empty[2] (the leader's),
   // drain
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kStages);
+  const uint32_t tfull0 = smem_addr(bars + 2 * kStages), tempty0 = smem_addr(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_addr(bars + 2 * kStages + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -362,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmB);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
@@ -394,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // both CTAs' copies complete on the leader's full barrier, which expects them all
           const uint32_t fb = map_to_rank(full0 + 8 * stage, 0);
           if (leader) mbar_expect_tx(full0 + 8 * stage, 2 * (kStageA + kStageB));
-          const uint32_t a_dst = smem_u32(sA + stage * kStageA), b_dst = smem_u32(sB + stage * kStageB);
+          const uint32_t a_dst = smem_addr(sA + stage * kStageA), b_dst = smem_addr(sB + stage * kStageB);
           const int k0 = kb * BK;
           if constexpr (A_MN) {
             tma_load_2d(a_dst, &tmA, arow, k0, fb);
@@ -449,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * kStageA), b_base = smem_u32(sB + stage * kStageB);
+          const uint32_t a_base = smem_addr(sA + stage * kStageA), b_base = smem_addr(sB + stage * kStageB);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sw128_desc(a_base + kk * 2048, 8192, 1024) : sw128_desc(a_base + kk * 32, 16, 1024);
@@ -473,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue: warps 2..9; TMEM lanes 32 * (warp % 4) ..., columns half * 128 ... ----
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const uint32_t buf = smem_u32(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
+    const uint32_t buf = smem_addr(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
     int local = 0;
     for (int t = first; t < total; t += step, ++local) {
       const Tile u = tile_of(p, t);
