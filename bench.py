@@ -283,17 +283,24 @@ def _unregister_host(ptr):
 
 
 def pinned_host(shape, dtype, src=None):
-    """A page-locked host tensor of exactly this size (torch's pinned allocator rounds each
-    block up to a power of two: 32 GB for the 20 GB logits), filled from ``src`` if given.
-    The pages are registered with cudaHostRegister and released when the tensor goes."""
+    """A page-locked host tensor, filled from ``src`` if given.
+
+    Inputs (src given) come from the CUDA host allocator (cudaHostAlloc; torch rounds the
+    block up to a power of two), outputs are malloc'd pages registered with cudaHostRegister
+    at exactly their size.  On GB300 machines each kind kept its full copy rate in its own
+    direction after a long-running process had churned the host memory (20 GB host->device
+    from registered pages dropped to ~12 GB/s there, from cudaHostAlloc's it did not; the
+    reverse held for device->host), while on a fresh box both are at ~190-210 GB/s."""
+    if src is not None:
+        t = torch.empty(shape, dtype=dtype, pin_memory=True)
+        t.copy_(src)
+        return t
     t = torch.empty(shape, dtype=dtype)
     nbytes = t.numel() * t.element_size()
     if nbytes and int(torch.cuda.cudart().cudaHostRegister(t.data_ptr(), nbytes, 0)) == 0:
         weakref.finalize(t, _unregister_host, t.data_ptr())
     elif nbytes:
         t = t.pin_memory()
-    if src is not None:
-        t.copy_(src)
     return t
 
 
