@@ -611,7 +611,7 @@ class LinearStep:
         R, V, H = spec.rows, spec.V, spec.H
         f32 = dict(dtype=torch.float32, device=device)
         self.grad_w = torch.zeros(V, H, **f32)
-        self.ws = torch.empty(rp.grpo_fused_linear_workspace_size(V, self.chunk), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(rp.grpo_fused_linear_workspace_size(H, V, self.chunk), dtype=torch.uint8, device=device)
         # old / ref placed near the current logp with a first pass of the same call (setup)
         f0 = rp.grpo_fused_linear(li.hidden, li.weight, li.idx, li.adv, li.dloss, B=spec.B, L=spec.L, T=spec.T,
                                   beta=0.0, eps_low=spec.eps_low, eps_high=spec.eps_high, mask=li.mask,
@@ -621,8 +621,10 @@ class LinearStep:
         self.ref = (f0["logp"] + li.ref_offset).contiguous()
         del f0
         self.kernels = [("grpo_fused_linear", self.call)]
-        self.launches_per_step = 5 * ((R + self.chunk - 1) // self.chunk)
-        self.flops_per_step = 6 * R * V * H
+        self.launches_per_step = 7 * ((R + self.chunk - 1) // self.chunk) + (li.mask is not None)
+        # the GEMMs run on the unmasked rows only (masked rows are left out of the chunks)
+        self.rows_computed = R if li.mask is None else int(li.mask.sum().item())
+        self.flops_per_step = 6 * self.rows_computed * V * H
 
     def call(self, hidden=None, idx=None, adv=None, dloss=None, mask=None, old=None, ref=None):
         spec, li = self.spec, self.li
@@ -653,8 +655,9 @@ class LinearStep:
 
 
 def run_linear(args):
-    """Bench line of the LM-head workload: rows/s and the tensor-core roofline of the step
-    (6 R V H flops: the logits GEMM and the two gradient GEMMs)."""
+    """Bench line of the LM-head workload: rows/s of the batch and the tensor-core roofline
+    of the step (6 R V H flops over its R unmasked rows: the logits GEMM and the two gradient
+    GEMMs; masked rows are left out of the chunks)."""
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -697,6 +700,7 @@ def run_linear(args):
                            "parallelism": f"{world} independent batch(es), one per GPU"},
                 "value": round(rows_per_s, 1), "steps": K, "warmup": Wm, "ms_per_step": round(step_ms, 4),
                 "dtype": "bf16", "rows_per_s": round(rows_per_s, 1),
+                "rows_unmasked": step.rows_computed,
                 "roofline": {"bound": "tensor", "kernel": "grpo_fused_linear (3 GEMMs + row pass per chunk)",
                              "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
                              "frac": round(tflops / peak, 4), "traffic": None, "peak_source": peak_src,
@@ -705,8 +709,11 @@ def run_linear(args):
                            "full_batch_logits_and_dlogits_bytes_bf16": int(2 * full_logits)},
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": step.launches_per_step * K,
-                "gpu_launches_note": "per chunk: the logits GEMM, the row pass, grad_hidden's split GEMM and the "
-                                     "sum of its splits, the grad_weight GEMM (all this library's kernels)",
+                "gpu_launches_note": "once: the masked rows' zero outputs; per chunk (sized for an unmasked "
+                                     "batch; chunks past the last unmasked row return at once): the row "
+                                     "selection, the gather of the chunk's hidden rows, the logits GEMM, the row "
+                                     "pass, grad_hidden's split GEMM and the sum of its splits, the grad_weight "
+                                     "GEMM (all this library's kernels)",
                 "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                            "samples": clk["samples"]},
                 "timed_wall_s": round(wall, 3), "kernel_source": kernel_source_hash()}

@@ -384,6 +384,13 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  * order, and each element of grad_weight receives one add per chunk, so the results do not
  * depend on timing.
  *
+ * Masked rows (mask[r] == 0) are left out of the chunks: their outputs and their grad_hidden
+ * rows are zero, and they add nothing to grad_weight, so their logits are never formed.  The
+ * chunks hold the unmasked rows in batch order, chunk_rows of them each; the packing is done
+ * on the device, so the call does not synchronise with the host.  (The zero-gradient
+ * early-out of [Liger-bwd], taken for whole masked rows before their logits exist.)  The
+ * chunk a row falls in, and so the fp32 summation order of grad_weight, depends on the mask.
+ *
  *   hidden        [B*L, H] bf16, row-major, 16-byte aligned;  H a multiple of 8
  *   weight        [V, H] bf16, row-major, 16-byte aligned
  *   idx, old_logp, ref_logp, adv, mask, dloss, T, beta, eps_low, eps_high, loss, logp,
@@ -391,10 +398,11 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  *   chunk_rows    rows per chunk, >= 1 (the last chunk may be shorter)
  *   workspace     device scratch of at least grpo_fused_linear_workspace_size() bytes,
  *                 256-byte aligned; its contents are not kept between calls.  The size is
- *                 one chunk's fp32 logits, bf16 dlogits and statistics (6 V8 + 32
- *                 ceil(V / 256) bytes a row, V8 = V rounded up to a multiple of 8) plus
- *                 128 MiB for the K splits of grad_hidden (as many splits of
- *                 chunk_rows * H * 4 bytes as fit, at most 32)
+ *                 one chunk's fp32 logits, bf16 dlogits, statistics, gathered hidden rows
+ *                 and row list (6 V8 + 32 ceil(V / 256) + 2 H + 4 bytes a row, V8 = V
+ *                 rounded up to a multiple of 8, each part rounded up to 256 bytes, plus
+ *                 256) and max(128 MiB, chunk_rows * H * 4) for the K splits of
+ *                 grad_hidden (as many splits of chunk_rows * H * 4 bytes as fit, at most 32)
  *   grad_hidden   [B*L, H] fp32 output (overwritten), or NULL
  *   grad_weight   [V, H] fp32, ACCUMULATED into (+=), or NULL; 16-byte aligned
  *
@@ -402,7 +410,7 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  * two backward GEMMs.  Calls on the same stream run in order.  A GEMM whose own copies or
  * MMAs stall for about 2 s gives up, sets GRPO_DEVERR_TIMEOUT in *dev_err and returns.
  */
-grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes);
+grpo_status grpo_fused_linear_workspace_size(int64_t H, int64_t V, int64_t chunk_rows, uint64_t* bytes);
 grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B, int64_t L, int64_t H, int64_t V,
                               const int64_t* idx, const float* old_logp, const float* ref_logp, const float* adv,
                               const uint8_t* mask, const float* dloss, float T, float beta, float eps_low,
@@ -417,13 +425,14 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
  * handed to a pool it does not control, or a step that must not stall on an allocation).
  * The pages have no counterpart; this is a convenience of this library.
  *
- * Its scratch (one chunk's fp32 logits, bf16 dlogits and per-128-column statistics, and the
- * K splits of grad_hidden) is a fixed 32 MiB device array inside the library, which every
- * device context that loads the library holds until the process exits.  Limit: the three
- * chunk buffers, chunk_rows * (4 V8 + 2 V8 + 32 ceil(V / 256)) bytes, each rounded up to
- * 256 bytes, plus one split of grad_hidden, chunk_rows * H * 4 bytes, must fit in 32 MiB
- * (V8 = V rounded up to a multiple of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before
- * any launch.  For V = 151936 and H = 1024 that is at most 35 rows per chunk.
+ * Its scratch (one chunk's fp32 logits, bf16 dlogits, per-128-column statistics, gathered
+ * hidden rows and row list, and the K splits of grad_hidden) is a fixed 32 MiB device array
+ * inside the library, which every device context that loads the library holds until the
+ * process exits.  Limit: the chunk buffers, chunk_rows * (4 V8 + 2 V8 + 32 ceil(V / 256) +
+ * 2 H + 4) bytes in five parts each rounded up to 256 bytes, plus 256 bytes, plus one split
+ * of grad_hidden, chunk_rows * H * 4 bytes, must fit in 32 MiB (V8 = V rounded up to a
+ * multiple of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before any launch.  For
+ * V = 151936 and H = 1024 that is at most 35 rows per chunk.
  *
  * The first call on a device (and the first after a cudaDeviceReset) does the set-up: it
  * looks up the array's device address in the current context.  Make that first call

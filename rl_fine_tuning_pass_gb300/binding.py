@@ -74,7 +74,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                       _P, _F, _F, _F, _F, rows_p, _P, _P],
         "selective_log_softmax_bwd_vocab_shard": [rows_p, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P, _F,
                                                   rows_p, _P, _P],
-        "grpo_fused_linear_workspace_size": [ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)],
+        "grpo_fused_linear_workspace_size": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.POINTER(ctypes.c_uint64)],
         "grpo_fused_linear": [_P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P,
                               _P, _P, _F, _F, _F, _F, ctypes.c_int64, _P, ctypes.c_uint64, _P, _P, _P, _P, _P, _P,
                               _P, _P, _P, _P],
@@ -389,10 +390,10 @@ def selective_log_softmax_bwd_vocab_shard(logits_shard, vocab_start, vocab_total
 # the GRPO loss on top of the LM head (hidden states and head weight)
 # ---------------------------------------------------------------------------
 
-def grpo_fused_linear_workspace_size(V, chunk_rows):
+def grpo_fused_linear_workspace_size(H, V, chunk_rows):
     out = ctypes.c_uint64(0)
     _check("grpo_fused_linear_workspace_size",
-           load_library().grpo_fused_linear_workspace_size(int(V), int(chunk_rows), ctypes.byref(out)))
+           load_library().grpo_fused_linear_workspace_size(int(H), int(V), int(chunk_rows), ctypes.byref(out)))
     return int(out.value)
 
 
@@ -422,7 +423,7 @@ def grpo_fused_linear(hidden, weight, idx, adv, dloss, *, B, L, T, beta, eps_low
         grad_weight = torch.zeros(V, H, **f32)
     out["grad_weight"] = grad_weight if with_grad_weight else None
     chunk = max(1, min(int(chunk_rows), R)) if R else 1
-    need = grpo_fused_linear_workspace_size(V, chunk)
+    need = grpo_fused_linear_workspace_size(H, V, chunk)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     st = load_library().grpo_fused_linear(

@@ -1,5 +1,6 @@
 // C-ABI entry points declared in include/grpo_rowpass.h.  Host-side validation runs
 // completely before any CUDA call, so a rejected call has no effect on the device.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -538,15 +539,19 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
 }  // extern "C"
 
 namespace {
-// Room for the K splits of grad_hidden's GEMM: 16 splits of a 2048-row chunk at H = 1024.
+// Room for the K splits of grad_hidden's GEMM: 16 splits of a 2048-row chunk at H = 1024,
+// and never less than one split.
 constexpr uint64_t kLinearSplitWs = uint64_t(128) << 20;
 }  // namespace
 
 extern "C" {
 
-grpo_status grpo_fused_linear_workspace_size(int64_t V, int64_t chunk_rows, uint64_t* bytes) {
-  if (bytes == nullptr || V < 1 || V > kMaxV || chunk_rows < 1 || chunk_rows > kMaxRows) return GRPO_ERR_INVALID_ARG;
-  *bytes = grpo::linear_chunk_bytes(V, chunk_rows) + kLinearSplitWs;
+grpo_status grpo_fused_linear_workspace_size(int64_t H, int64_t V, int64_t chunk_rows, uint64_t* bytes) {
+  if (bytes == nullptr || H < 8 || H % 8 != 0 || H > (int64_t(1) << 24) || V < 1 || V > kMaxV || chunk_rows < 1 ||
+      chunk_rows > kMaxRows)
+    return GRPO_ERR_INVALID_ARG;
+  const uint64_t one_split = grpo::linear_round256(static_cast<uint64_t>(chunk_rows) * H * 4);
+  *bytes = grpo::linear_chunk_bytes(H, V, chunk_rows) + std::max(kLinearSplitWs, one_split);
   return GRPO_OK;
 }
 
@@ -564,7 +569,7 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
   if (rows == 0) return GRPO_OK;
   uint64_t need = 0;
   const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
-  grpo_fused_linear_workspace_size(V, chunk, &need);
+  grpo_fused_linear_workspace_size(H, V, chunk, &need);
   if (hidden == nullptr || !aligned(hidden, 16) || weight == nullptr || !aligned(weight, 16) ||
       workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)
     return GRPO_ERR_INVALID_ARG;

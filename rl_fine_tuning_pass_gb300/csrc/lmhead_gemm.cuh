@@ -81,6 +81,14 @@ struct Params {
   float c;             // log2(e) / T
   int* err;            // device error word (nullable)
   int pair_limit;      // at most this many CTA pairs (0: as many as fit on the GPU)
+  // A extent known only on the device (the rows a chunk holds after the masked rows are
+  // left out), read when the kernel starts, after the grids before it have completed:
+  // null, or *dyn rows (dyn_k = 0: M = min(M, *dyn), m_tiles follows) or *dyn K elements
+  // (dyn_k = 1: k_blocks = ceil(*dyn / 64); splits must be 1).  M and m_tiles (k_blocks)
+  // above are then the upper bounds the launch is sized for.  Zero rows or zero K blocks:
+  // no tiles.
+  const int32_t* dyn;
+  int dyn_k;
 };
 
 // ---------------------------------------------------------------------------
@@ -197,24 +205,43 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float (&v)[32]) 
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The extents of this launch: Params' own, or with the device-side extent applied.
+struct Dims {
+  int M, m_tiles, k_blocks, total;
+};
+__device__ __forceinline__ Dims dims_of(const Params& p) {
+  Dims d{p.M, p.m_tiles, p.k_blocks, 0};
+  if (p.dyn != nullptr) {
+    const int n = max(*p.dyn, 0);
+    if (p.dyn_k) {
+      d.k_blocks = min(p.k_blocks, (n + BK - 1) / BK);
+    } else {
+      d.M = min(p.M, n);
+      d.m_tiles = (d.M + 2 * BM - 1) / (2 * BM);
+    }
+  }
+  d.total = (d.M > 0 && d.k_blocks > 0) ? d.m_tiles * p.n_tiles * p.splits : 0;
+  return d;
+}
+
 // The tile list: tile t -> (m, n, split) and the split's K blocks [kb0, kb1).
 struct Tile {
   int m, n, s, kb0, kb1;
 };
-__device__ __forceinline__ Tile tile_of(const Params& p, int t) {
+__device__ __forceinline__ Tile tile_of(const Params& p, const Dims& d, int t) {
   Tile u;
-  const int mn = p.m_tiles * p.n_tiles;
+  const int mn = d.m_tiles * p.n_tiles;
   u.s = t / mn;
   const int r = t - u.s * mn;
   if (p.m_fastest) {
-    u.m = r % p.m_tiles;
-    u.n = r / p.m_tiles;
+    u.m = r % d.m_tiles;
+    u.n = r / d.m_tiles;
   } else {
     u.n = r % p.n_tiles;
     u.m = r / p.n_tiles;
   }
-  u.kb0 = static_cast<int>(static_cast<int64_t>(p.k_blocks) * u.s / p.splits);
-  u.kb1 = static_cast<int>(static_cast<int64_t>(p.k_blocks) * (u.s + 1) / p.splits);
+  u.kb0 = static_cast<int>(static_cast<int64_t>(d.k_blocks) * u.s / p.splits);
+  u.kb1 = static_cast<int>(static_cast<int64_t>(d.k_blocks) * (u.s + 1) / p.splits);
   return u;
 }
 
@@ -344,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = p.m_tiles * p.n_tiles * p.splits;
+  const Dims dims = dims_of(p);
+  const int total = dims.total;
   const int first = static_cast<int>(cluster_id()), step = static_cast<int>(cluster_count());
 
   if (warp == 0) {
@@ -355,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;  // stages filled and not yet known to be consumed (for the abort path)
       bool ok = true;
       for (int t = first; t < total && ok; t += step) {
-        const Tile u = tile_of(p, t);
+        const Tile u = tile_of(p, dims, t);
         const int arow = u.m * 2 * BM + static_cast<int>(rank) * BM;  // this CTA's A rows
         const int bcol = u.n * BN + static_cast<int>(rank) * BNH;      // this CTA's B columns
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
@@ -409,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int local = 0;
       bool ok = true;
       for (int t = first; t < total && ok; t += step, ++local) {
-        const Tile u = tile_of(p, t);
+        const Tile u = tile_of(p, dims, t);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag)) break;
@@ -436,9 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) umma_commit_pair(tfull0 + 8 * acc);  // both CTAs' accumulator halves are ready
       }
-      // no MMA may still be writing either CTA's TMEM when it is freed
-      umma_commit_local(drain);
-      mbar_wait(drain, 0, abort_flag, false);
+      // no MMA may still be writing either CTA's TMEM when it is freed (a launch whose
+      // device-side extent left it no tiles issued none)
+      if (local > 0) {
+        umma_commit_local(drain);
+        mbar_wait(drain, 0, abort_flag, false);
+      }
     }
     __syncwarp();
   } else {
@@ -448,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t buf = smem_addr(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
     int local = 0;
     for (int t = first; t < total; t += step, ++local) {
-      const Tile u = tile_of(p, t);
+      const Tile u = tile_of(p, dims, t);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const bool ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag);
@@ -456,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row0 = u.m * 2 * BM + static_cast<int>(rank) * BM + quarter * 32;  // this warp's first row
       const int row = row0 + lane;
-      const bool row_ok = row < p.M;
+      const bool row_ok = row < dims.M;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN + half * (BN / 2));
       const int col_base = u.n * BN + half * (BN / 2);
@@ -482,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         stage_row(buf, lane, v[j]);
         __syncwarp();
-        write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, p.M - row0, valid);
+        write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0, valid);
         __syncwarp();  // every lane has read the box before the next one is staged
       }
       if constexpr (EPI == kEpiLogits) {

@@ -84,27 +84,30 @@ __device__ __forceinline__ void fill_bf16_row(uint16_t* out, int V, uint32_t pai
 }
 
 // One CTA per row of the chunk: merge the row's statistics, the forward epilogue and the row
-// factor, then one sweep over the fp32 row writing bf16 dlogits.
+// factor, then one sweep over the fp32 row writing bf16 dlogits.  Row i of the chunk is batch
+// row list[i]; the chunk holds state[0] rows, and the rows after them up to the next
+// multiple of 64 get zero dlogits, since grad_weight's GEMM reads its K (row) dimension in
+// blocks of 64.
 template <int THREADS, int UNROLL, bool kH>
 __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkParams q) {
   wait_for_previous_grids();
   constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
   const FwdParams& p = q.f;
   const int64_t rl = blockIdx.x;  // row within the chunk
-  const int64_t r = q.row0 + rl;  // row of the batch
-  const int64_t b = r / p.x.L;
+  const int n = q.state[0];
   const int tid = threadIdx.x;
   const int V = p.x.V;
-  const float c = p.c;
-  const float* row = q.logits + rl * q.ld;
   uint16_t* out = q.dlogits + rl * q.ld;
-
-  const int64_t id64 = p.idx[r];  // loaded with the mask, before either is waited on
-  if (p.mask != nullptr && p.mask[r] == 0) {  // masked token: zero outputs, zero gradient row
-    if (tid == 0) masked_row_outputs(p, r);
-    fill_bf16_row(out, V, 0u, THREADS);
+  if (rl >= n) {
+    if (rl < ((static_cast<int64_t>(n) + 63) & ~int64_t(63))) fill_bf16_row(out, V, 0u, THREADS);
     return;
   }
+  const int64_t r = q.list[rl];  // row of the batch (never a masked one)
+  const int64_t b = r / p.x.L;
+  const float c = p.c;
+  const float* row = q.logits + rl * q.ld;
+
+  const int64_t id64 = p.idx[r];
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
 
@@ -146,10 +149,14 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   if (owner) BF16::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
 
-// grad_hidden rows [row0, row0 + c) = the sum of the K splits, in split order.
+// grad_hidden row list[i] = the sum of the K splits of the chunk's row i, in split order,
+// for the chunk's state[0] rows.
 __global__ void __launch_bounds__(256) split_sum_kernel(const float4* __restrict__ part, float4* __restrict__ out,
-                                                        int64_t n4, int splits, int64_t split4) {
+                                                        const int32_t* __restrict__ list,
+                                                        const int32_t* __restrict__ state, int64_t h4, int splits,
+                                                        int64_t split4) {
   wait_for_previous_grids();
+  const int64_t n4 = static_cast<int64_t>(state[0]) * h4;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
     float4 a = part[i];
     for (int s = 1; s < splits; ++s) {
@@ -159,7 +166,100 @@ __global__ void __launch_bounds__(256) split_sum_kernel(const float4* __restrict
       a.z += v.z;
       a.w += v.w;
     }
-    out[i] = a;
+    const int64_t rl = i / h4;
+    out[static_cast<int64_t>(list[rl]) * h4 + (i - rl * h4)] = a;
+  }
+}
+
+// Masked rows: their forward outputs and their grad_hidden rows are zero, and nothing else of
+// the call touches them (one warp per row).
+__global__ void __launch_bounds__(256) linear_masked_kernel(const FwdParams p, float4* __restrict__ grad_hidden,
+                                                            int64_t rows, int64_t h4) {
+  wait_for_previous_grids();
+  const int64_t r = blockIdx.x * int64_t(8) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows || p.mask[r] != 0) return;
+  if (lane == 0) masked_row_outputs(p, r);
+  if (grad_hidden != nullptr)
+    for (int64_t i = lane; i < h4; i += 32) grad_hidden[r * h4 + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// The rows of the next chunk: up to `chunk` unmasked rows, in batch order, from the batch row
+// where the previous chunk stopped (state[1]; row 0 for the first chunk).  One CTA scans the
+// mask, 16 rows a thread per pass; state[0] = the rows found, state[1] = the row after the
+// last of them (or `rows` when the batch is used up).
+constexpr int kSelectThreads = 1024;
+__global__ void __launch_bounds__(kSelectThreads) linear_select_kernel(const uint8_t* __restrict__ mask,
+                                                                       int64_t rows, int chunk, int first,
+                                                                       int32_t* __restrict__ list,
+                                                                       int32_t* __restrict__ state) {
+  wait_for_previous_grids();
+  __shared__ int warp_sum[kSelectThreads / 32];
+  __shared__ int sh_total, sh_cursor;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t pos = first ? 0 : state[1];
+  int found = 0;
+  if (tid == 0) sh_cursor = -1;
+  while (pos < rows && found < chunk) {
+    const int64_t r0 = pos + 16 * static_cast<int64_t>(tid);
+    uint32_t bits = 0;  // bit j: row r0 + j is in the batch and unmasked
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int64_t r = r0 + j;
+      if (r < rows && (mask == nullptr || mask[r] != 0)) bits |= 1u << j;
+    }
+    const int cnt = __popc(bits);
+    int incl = cnt;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_sum[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      warp_sum[lane] = wi - w;  // exclusive
+      if (lane == 31) sh_total = wi;
+    }
+    __syncthreads();
+    int k = found + warp_sum[warp] + incl - cnt;  // this thread's first slot
+    for (uint32_t m = bits; m != 0u; m &= m - 1u) {
+      const int j = __ffs(m) - 1;
+      if (k < chunk) list[k] = static_cast<int32_t>(r0 + j);
+      if (k == chunk - 1) sh_cursor = static_cast<int>(r0 + j + 1);
+      ++k;
+    }
+    found += sh_total;
+    pos += 16 * static_cast<int64_t>(kSelectThreads);
+    __syncthreads();  // warp_sum and sh_total are rewritten by the next pass
+  }
+  if (tid == 0) {
+    state[0] = found < chunk ? found : chunk;
+    state[1] = found < chunk ? static_cast<int32_t>(rows) : sh_cursor;
+  }
+}
+
+// The chunk's hidden states in consecutive rows: row i = hidden row list[i] for the state[0]
+// rows of the chunk, zero after them up to the next multiple of 64 (within the chunk).
+__global__ void __launch_bounds__(256) linear_gather_kernel(const uint4* __restrict__ hidden,
+                                                            uint4* __restrict__ out,
+                                                            const int32_t* __restrict__ list,
+                                                            const int32_t* __restrict__ state, int64_t h8,
+                                                            int64_t chunk) {
+  wait_for_previous_grids();
+  const int64_t n = state[0];
+  const int64_t upto = std::min(chunk, (n + 63) & ~int64_t(63));
+  const int64_t total = upto * h8;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t rl = i / h8;
+    out[i] = rl < n ? hidden[static_cast<int64_t>(list[rl]) * h8 + (i - rl * h8)] : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -186,13 +286,17 @@ int grad_hidden_splits(int64_t tiles, int64_t k_blocks, uint64_t part_bytes, uin
 
 namespace {
 
-// The launches of one fused-linear call: the head weight's tensor maps, made once, and one
-// function per stage of a chunk.
+// The launches of one fused-linear call: the tensor maps of the head weight and of the chunk
+// buffers, made once, and one function per stage of a chunk.  Every chunk is sized for
+// q.chunk rows on the host; how many it holds is known only on the device (state[0]), where
+// the kernels read it.
 struct LinearLauncher {
   const FusedLinearParams& q;
   bool kH;
   int sms;
   CUtensorMap tW_k, tW_mn;  // the head weight K-major (logits) and MN-major (grad_hidden)
+  CUtensorMap tHc_k, tHc_mn;  // the chunk's gathered hidden rows: K-major (logits), MN-major (grad_weight)
+  CUtensorMap tD_k, tD_mn;  // the chunk's dlogits: K-major (grad_hidden), MN-major (grad_weight)
 
   explicit LinearLauncher(const FusedLinearParams& params) : q(params) {
     kH = q.chunk_params.f.entropy != nullptr;
@@ -201,20 +305,48 @@ struct LinearLauncher {
   bool init() {
     using namespace gemm;
     if (sms <= 0) return false;
+    const LinearChunkBufs& b = q.bufs;
     return make_operand_map(&tW_k, q.weight, false, q.V, q.H, q.H, BNH) &&
-           make_operand_map(&tW_mn, q.weight, true, q.H, q.V, q.H, BNH);
+           make_operand_map(&tW_mn, q.weight, true, q.H, q.V, q.H, BNH) &&
+           make_operand_map(&tHc_k, b.hidden, false, q.chunk, q.H, q.H, BM) &&
+           make_operand_map(&tHc_mn, b.hidden, true, q.H, q.chunk, q.H, BNH) &&
+           make_operand_map(&tD_k, b.dlogits, false, q.chunk, q.V, q.ld, BM) &&
+           make_operand_map(&tD_mn, b.dlogits, true, q.V, q.chunk, q.ld, BM);
   }
 
-  // logits [c, V] fp32 = h W^T, with the statistics of every 128 columns
-  cudaError_t logits(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
+  // masked rows: zero outputs and zero grad_hidden rows, once per call
+  cudaError_t masked(cudaStream_t s) const {
+    const FwdParams& f = q.chunk_params.f;
+    if (f.mask == nullptr) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>((q.rows + 7) / 8));
+    return launch_after_previous(linear_masked_kernel, grid, dim3(256), s, f,
+                                 reinterpret_cast<float4*>(q.grad_hidden), q.rows, q.H / 4);
+  }
+
+  // the chunk's rows (the next unmasked ones) and their hidden states, gathered
+  cudaError_t select(bool first, cudaStream_t s) const {
+    const LinearChunkBufs& b = q.bufs;
+    cudaError_t e = launch_after_previous(linear_select_kernel, dim3(1), dim3(kSelectThreads), s,
+                                          q.chunk_params.f.mask, q.rows, static_cast<int>(q.chunk),
+                                          first ? 1 : 0, b.list, b.state);
+    if (e != cudaSuccess) return e;
+    const int64_t h8 = q.H / 8, n = q.chunk * h8;
+    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, int64_t(sms) * 8));
+    return launch_after_previous(linear_gather_kernel, dim3(blocks), dim3(256), s,
+                                 reinterpret_cast<const uint4*>(q.hidden), reinterpret_cast<uint4*>(b.hidden),
+                                 static_cast<const int32_t*>(b.list), static_cast<const int32_t*>(b.state), h8,
+                                 q.chunk);
+  }
+
+  // logits [n, V] fp32 = h_chunk W^T, with the statistics of every 128 columns
+  cudaError_t logits(cudaStream_t s) const {
     using namespace gemm;
-    CUtensorMap tA;
-    if (!make_operand_map(&tA, q.hidden + r0 * q.H, false, c, q.H, q.H, BM)) return cudaErrorInvalidValue;
+    const LinearChunkBufs& b = q.bufs;
     Params pl{};
-    pl.M = static_cast<int>(c);
+    pl.M = static_cast<int>(q.chunk);
     pl.N = static_cast<int>(q.V);
     pl.k_blocks = static_cast<int>((q.H + BK - 1) / BK);
-    pl.m_tiles = static_cast<int>((c + 2 * BM - 1) / (2 * BM));
+    pl.m_tiles = static_cast<int>((q.chunk + 2 * BM - 1) / (2 * BM));
     pl.n_tiles = static_cast<int>((q.V + BN - 1) / BN);
     pl.splits = 1;
     pl.m_fastest = 1;
@@ -223,34 +355,39 @@ struct LinearLauncher {
     pl.stats = b.stats;
     pl.c = q.chunk_params.f.c;
     pl.err = q.chunk_params.f.dev_err;
-    return kH ? launch_gemm<kEpiLogits, false, false, true>(tA, tW_k, pl, s)
-              : launch_gemm<kEpiLogits, false, false, false>(tA, tW_k, pl, s);
+    pl.dyn = b.state;
+    return kH ? launch_gemm<kEpiLogits, false, false, true>(tHc_k, tW_k, pl, s)
+              : launch_gemm<kEpiLogits, false, false, false>(tHc_k, tW_k, pl, s);
   }
 
   // the row pass: forward outputs and bf16 dlogits of the chunk
-  cudaError_t rows(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
+  cudaError_t rows(cudaStream_t s) const {
+    const LinearChunkBufs& b = q.bufs;
     LinearChunkParams lp = q.chunk_params;
-    lp.row0 = r0;
     lp.logits = b.logits;
     lp.stats = b.stats;
     lp.dlogits = b.dlogits;
     lp.ld = q.ld;
     lp.n_stat = static_cast<int>(linear_n_stat(q.V));
-    const dim3 grid(static_cast<unsigned>(c));
+    lp.list = b.list;
+    lp.state = b.state;
+    lp.chunk = q.chunk;
+    const dim3 grid(static_cast<unsigned>(q.chunk));
     return kH ? launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, true>, grid,
                                       dim3(kLinearThreads), s, lp)
               : launch_after_previous(linear_rows_kernel<kLinearThreads, kUnroll, false>, grid,
                                       dim3(kLinearThreads), s, lp);
   }
 
-  // grad_h [c, H] = dlogits W (split along the vocabulary, the splits summed in order) and
-  // grad_W [V, H] += dlogits^T h (vector reduce-adds into the caller's fp32 gradient)
-  cudaError_t grads(const LinearChunkBufs& b, int64_t r0, int64_t c, cudaStream_t s) const {
+  // grad_h [n, H] = dlogits W (split along the vocabulary, the splits summed in order into
+  // the chunk's rows of grad_hidden) and grad_W [V, H] += dlogits^T h_chunk (vector
+  // reduce-adds into the caller's fp32 gradient)
+  cudaError_t grads(cudaStream_t s) const {
     using namespace gemm;
-    const int64_t H = q.H, V = q.V;
+    const LinearChunkBufs& b = q.bufs;
+    const int64_t H = q.H, V = q.V, c = q.chunk;
     cudaError_t e = cudaSuccess;
     if (q.grad_hidden != nullptr) {
-      CUtensorMap tDk;
       Params ph{};
       ph.M = static_cast<int>(c);
       ph.N = static_cast<int>(H);
@@ -261,28 +398,22 @@ struct LinearLauncher {
       ph.splits = grad_hidden_splits(int64_t(ph.m_tiles) * ph.n_tiles, ph.k_blocks, q.part_bytes, split_bytes,
                                      sms / 2);
       ph.m_fastest = 1;
-      float* gh = q.grad_hidden + r0 * H;
-      ph.C = ph.splits == 1 ? gh : q.part;
+      ph.C = q.part;
       ph.ldc = H;
       ph.split_stride = c * H;
       ph.err = q.chunk_params.f.dev_err;
-      if (!make_operand_map(&tDk, b.dlogits, false, c, V, q.ld, BM)) return cudaErrorInvalidValue;
-      e = launch_gemm<kEpiStore, false, true, false>(tDk, tW_mn, ph, s);
+      ph.dyn = b.state;
+      e = launch_gemm<kEpiStore, false, true, false>(tD_k, tW_mn, ph, s);
       if (e != cudaSuccess) return e;
-      if (ph.splits > 1) {
-        const int64_t n4 = c * H / 4;
-        const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, int64_t(sms) * 8));
-        e = launch_after_previous(split_sum_kernel, dim3(blocks), dim3(256), s,
-                                  reinterpret_cast<const float4*>(q.part), reinterpret_cast<float4*>(gh), n4,
-                                  ph.splits, n4);
-        if (e != cudaSuccess) return e;
-      }
+      const int64_t h4 = H / 4, n4 = c * h4;
+      const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n4 + 255) / 256, int64_t(sms) * 8));
+      e = launch_after_previous(split_sum_kernel, dim3(blocks), dim3(256), s,
+                                reinterpret_cast<const float4*>(q.part), reinterpret_cast<float4*>(q.grad_hidden),
+                                static_cast<const int32_t*>(b.list), static_cast<const int32_t*>(b.state), h4,
+                                ph.splits, n4);
+      if (e != cudaSuccess) return e;
     }
     if (q.grad_weight != nullptr) {
-      CUtensorMap tD, tHm;
-      if (!make_operand_map(&tD, b.dlogits, true, V, c, q.ld, BM) ||
-          !make_operand_map(&tHm, q.hidden + r0 * H, true, H, c, H, BNH))
-        return cudaErrorInvalidValue;
       Params pw{};
       pw.M = static_cast<int>(V);
       pw.N = static_cast<int>(H);
@@ -294,7 +425,9 @@ struct LinearLauncher {
       pw.C = q.grad_weight;
       pw.ldc = H;
       pw.err = q.chunk_params.f.dev_err;
-      e = launch_gemm<kEpiAccum, true, true, false>(tD, tHm, pw, s);
+      pw.dyn = b.state;
+      pw.dyn_k = 1;
+      e = launch_gemm<kEpiAccum, true, true, false>(tD_mn, tHc_mn, pw, s);
     }
     return e;
   }
@@ -305,17 +438,23 @@ struct LinearLauncher {
 cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream) {
   LinearLauncher run(q);
   if (!run.init()) return cudaErrorInvalidValue;
-  // logits, row pass and gradients of each chunk in turn.  (Running a chunk's row pass on a
-  // second stream next to its neighbours' GEMMs, with two sets of chunk buffers, measured no
-  // faster: the GEMMs and the row pass both lean on the L2 and DRAM bandwidth they share.)
-  for (int64_t r0 = 0; r0 < q.rows; r0 += q.chunk) {
-    const int64_t c = std::min(q.chunk, q.rows - r0);
-    cudaError_t e = run.logits(q.bufs, r0, c, stream);
-    if (e == cudaSuccess) e = run.rows(q.bufs, r0, c, stream);
-    if (e == cudaSuccess) e = run.grads(q.bufs, r0, c, stream);
-    if (e != cudaSuccess) return e;
+  // Masked rows are left out of every chunk: their outputs and gradients are zero by
+  // definition, so the GEMMs and the row pass see only the unmasked rows, packed into
+  // chunks in batch order (the zero-gradient early-out of "LinkedIn Liger-Kernel GRPO Loss
+  // Backward optimisation", applied to whole masked rows before their logits exist).  The
+  // host sizes the loop for an unmasked batch; chunks past the last unmasked row find no
+  // rows on the device and their kernels return at once.
+  // (Running a chunk's row pass on a second stream next to its neighbours' GEMMs, with two
+  // sets of chunk buffers, measured no faster: the GEMMs and the row pass both lean on the L2
+  // and DRAM bandwidth they share.)
+  cudaError_t e = run.masked(stream);
+  for (int64_t r0 = 0; e == cudaSuccess && r0 < q.rows; r0 += q.chunk) {
+    e = run.select(r0 == 0, stream);
+    if (e == cudaSuccess) e = run.logits(stream);
+    if (e == cudaSuccess) e = run.rows(stream);
+    if (e == cudaSuccess) e = run.grads(stream);
   }
-  return cudaSuccess;
+  return e;
 }
 
 }  // namespace grpo
@@ -405,8 +544,9 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
   if (rows == 0) return GRPO_OK;
   const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
   // the fixed array's limit: the chunk's buffers (fp32 logits, bf16 dlogits, statistics,
-  // each rounded up to 256 bytes) and one chunk of grad_hidden (chunk * H fp32) <= 32 MiB
-  const uint64_t chunk_bytes = grpo::linear_chunk_bytes(V, chunk);
+  // gathered bf16 hidden rows, row list and state, each rounded up to 256 bytes) and one
+  // split of grad_hidden (chunk * H fp32) <= 32 MiB
+  const uint64_t chunk_bytes = grpo::linear_chunk_bytes(H, V, chunk);
   if (chunk_bytes + static_cast<uint64_t>(chunk) * H * 4 > grpo::kNoallocScratchBytes) return GRPO_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
   if (!a16(hidden) || !a16(weight)) return GRPO_ERR_INVALID_ARG;

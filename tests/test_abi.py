@@ -200,10 +200,12 @@ def test_vocab_parallel_validation(lib):
 def test_fused_linear_validation(lib):
     """Shapes, alignment and the workspace size are checked on the host before any launch."""
     need = ctypes.c_uint64(0)
-    assert lib.grpo_fused_linear_workspace_size(1000, 16, ctypes.byref(need)) == binding.GRPO_OK
-    assert need.value >= 1000 * 16 * 6
-    assert lib.grpo_fused_linear_workspace_size(0, 16, ctypes.byref(need)) == INV
-    assert lib.grpo_fused_linear_workspace_size(1000, 0, ctypes.byref(need)) == INV
+    assert lib.grpo_fused_linear_workspace_size(64, 1000, 16, ctypes.byref(need)) == binding.GRPO_OK
+    assert need.value >= 1000 * 16 * 6 + 64 * 16 * 2
+    assert lib.grpo_fused_linear_workspace_size(64, 0, 16, ctypes.byref(need)) == INV
+    assert lib.grpo_fused_linear_workspace_size(64, 1000, 0, ctypes.byref(need)) == INV
+    assert lib.grpo_fused_linear_workspace_size(60, 1000, 16, ctypes.byref(need)) == INV   # H % 8 != 0
+    assert lib.grpo_fused_linear_workspace_size(64, 1000, 16, ctypes.byref(need)) == binding.GRPO_OK
     big = need.value
 
     def call(H=64, V=1000, hidden=FAKE, weight=FAKE, ws=FAKE, ws_bytes=big, chunk=16, T=1.0, beta=0.0, ref=None,

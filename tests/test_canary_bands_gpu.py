@@ -280,7 +280,7 @@ def test_fused_linear_writes_only_its_outputs(V):
     mask = (torch.rand(R, generator=g) > 0.3).to(torch.uint8).to(DEV)
     dloss = (mask.float() / R).contiguous()
     chunk = 5  # several chunks and a ragged last one
-    need = rp.grpo_fused_linear_workspace_size(V, chunk)
+    need = rp.grpo_fused_linear_workspace_size(H, V, chunk)
     ws = Banded(need, torch.uint8, band=256)  # the workspace must start 256-byte aligned
     o = {k: Banded(R, torch.float32) for k in ("loss", "logp", "lse", "kl", "entropy")}
     o["is_clipped"] = Banded(R, torch.uint8)

@@ -102,6 +102,53 @@ def test_fused_linear_every_row(V, chunk, beta):
     check_against_oracle(pb, out, f"fused linear V={V} chunk={chunk}")
 
 
+def test_fused_linear_without_a_mask():
+    """mask = NULL: every row counts, the chunks are the batch's rows in order."""
+    pb = problem(2, 21, 64, 1000, seed=11, beta=0.04, masked=False)
+    out, err = run_gpu(pb, 16)
+    assert err == 0
+    check_against_oracle(pb, out, "fused linear without a mask")
+
+
+@pytest.mark.parametrize("chunk", [5, 16, 64, 200])
+def test_fused_linear_packs_unmasked_rows_across_padding(chunk):
+    """Completions of different lengths with trailing padding (60 % of the rows masked, one
+    sequence fully masked): the chunks take only unmasked rows, so they cross sequence
+    boundaries, and the chunks after the last unmasked row find nothing to do.  Masked
+    rows get zero outputs and an exactly zero grad_hidden row."""
+    B, L, H, V = 4, 50, 64, 1003
+    pb = problem(B, L, H, V, seed=100 + chunk, beta=0.04)
+    lengths = [37, 0, 12, 31]
+    mask = torch.zeros(B * L, dtype=torch.uint8)
+    for b, n in enumerate(lengths):
+        mask[b * L:b * L + n] = 1
+    pb["mask"] = mask
+    pb["dloss"] = (pb["dloss"] + 0.1) * mask.float()
+    out, err = run_gpu(pb, chunk)
+    assert err == 0
+    check_against_oracle(pb, out, f"packed rows, chunk {chunk}")
+    m = mask.to(DEV).bool()
+    for k in ("loss", "logp", "lse", "kl", "entropy"):
+        assert torch.all(out[k][~m] == 0), k
+    assert torch.all(out["grad_hidden"][~m] == 0)
+
+
+def test_fused_linear_every_row_masked():
+    """No unmasked row: every output and grad_hidden row is zero and grad_weight keeps its
+    values bit for bit (no chunk holds a row, so no GEMM adds anything)."""
+    pb = problem(2, 21, 64, 517, seed=9, beta=0.04)
+    pb["mask"] = torch.zeros(42, dtype=torch.uint8)
+    pb["dloss"] = torch.zeros(42)
+    gW = torch.randn(517, 64, generator=torch.Generator().manual_seed(1)).to(DEV)
+    before = gW.clone()
+    out, err = run_gpu(pb, 16, grad_weight=gW)
+    assert err == 0
+    for k in ("loss", "logp", "lse", "kl", "entropy", "grad_hidden"):
+        assert torch.all(out[k] == 0), k
+    assert torch.all(out["is_clipped"] == 0)
+    assert torch.equal(gW, before)
+
+
 def test_fused_linear_accumulates_weight_gradient_and_chunking_is_invisible():
     """grad_weight is accumulated into the given tensor; the chunk size changes the row
     pass's outputs not at all, the GEMMs' outputs only by their fp32 summation order."""
