@@ -663,7 +663,7 @@ def run_linear(args):
     device = torch.device("cuda", local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    spec = W.get(LINEAR_WORKLOAD)
+    spec = W.get(LINEAR_WORKLOAD, **({"B": args.batch} if args.batch is not None else {}))
     step = LinearStep(spec, args.seed + rank, device, args.chunk_rows)
     flush_buf = L2Flush(device)
     step.call()

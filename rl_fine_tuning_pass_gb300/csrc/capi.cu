@@ -6,6 +6,7 @@
 
 #include "grpo_rowpass.h"
 #include "rowpass_internal.h"
+#include "rowpass_linear.h"
 
 namespace {
 

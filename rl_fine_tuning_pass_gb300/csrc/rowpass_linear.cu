@@ -21,6 +21,7 @@
 #include "grpo_rowpass.h"
 #include "lmhead_gemm.cuh"
 #include "rowpass_bwd.cuh"
+#include "rowpass_linear.h"
 
 namespace grpo {
 namespace {
