@@ -167,9 +167,14 @@ def kernel_source_hash(kernel: str = None) -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel: str, workload: str):
+def measured_traffic(kernel: str, spec):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current sources of that kernel (kernel_source_hash(kernel)); else None."""
+    current sources of that kernel (kernel_source_hash(kernel)) and the workload runs
+    with its own configuration (the records are for that one: another beta, batch or
+    layout moves other bytes); else None."""
+    if spec != W.get(spec.name):
+        return None
+    workload = spec.name
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -1145,7 +1150,7 @@ def entropy_run(step, K, Wm, flush_buf, peak):
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     nbytes = R * SLSM_ROW_BYTES["entropy_from_logits"](spec.V, spec.elem_size)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    traffic = measured_traffic("entropy_from_logits", spec.name)
+    traffic = measured_traffic("entropy_from_logits", spec)
     return {"kernel": "entropy_from_logits", "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 5),
             "bytes": int(nbytes), "rows_per_s": round(R / (ms * 1e-3), 1), "hbm_frac": round(gbs / peak, 4),
             "launches": K, "traffic": traffic,
@@ -1595,7 +1600,7 @@ def main(argv=None):
     peak, peak_src = load_peaks()
     dom = max(kern_ms, key=kern_ms.get)
     achieved = per_launch[dom] / (kern_ms[dom] * 1e-3) / 1e9
-    traffic = measured_traffic(dom, spec.name)
+    traffic = measured_traffic(dom, spec)
 
     e2e = None
     if not args.no_e2e:

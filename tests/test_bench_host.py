@@ -178,7 +178,12 @@ def test_kernel_source_hash_per_entry_point():
     hashes = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_UNITS}
     assert hashes["grpo_loss_fwd"] == hashes["entropy_from_logits"] != hashes["grpo_loss_bwd"]
     assert all(len(h) == 16 for h in hashes.values())
-    assert bench.measured_traffic("not_an_entry_point", "grpo_b4_l512_v32000") is None
+    spec = bench.W.get("grpo_b4_l512_v32000")
+    assert bench.measured_traffic("not_an_entry_point", spec) is None
+    # a record belongs to its workload's own configuration only
+    if bench.measured_traffic("grpo_loss_bwd", spec) is not None:
+        assert bench.measured_traffic("grpo_loss_bwd", spec.with_(beta=0.04)) is None
+        assert bench.measured_traffic("grpo_loss_bwd", spec.with_(B=2)) is None
 
 
 def test_e2e_parts_cover_every_row_once():
