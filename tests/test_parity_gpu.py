@@ -540,6 +540,71 @@ def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
                        bf16_or_f32_bits(select_rows(dl_same, np.arange(R))))
 
 
+@pytest.mark.parametrize("V", [65536, 100000, 151936, 158216])
+@pytest.mark.parametrize("beta", [0.0, 0.05])
+def test_fused_long_aligned_rows_every_row(V, beta):
+    """Long bf16 rows with 16-byte aligned starts (the 512-thread fused kernel, which keeps
+    the row in L2 between its two sweeps): every row against the oracle, including a row
+    with -inf logits, a peaked row (p_idx near 1), masked and zero-advantage rows; in place
+    equal bit for bit to out of place."""
+    B, L = 2, 5
+    R = B * L
+    seed = V + int(beta * 100)
+    x, idx, adv, mask, dloss = edge_inputs(B, L, V, torch.bfloat16, 0, 0, seed)
+    x[0, 1, 7::977] = float("-inf")
+    x[1, 2, int(idx[7])] += 30.0
+    mask[3] = 0
+    T, el, eh = f32(0.8), f32(0.2), f32(0.28)
+    beta = f32(beta)
+    xo = rows_f64(select_rows(x, np.arange(R)))
+    lp, _ = oracle.selective_log_softmax(xo, idx.cpu().numpy(), T)
+    g = torch.Generator().manual_seed(V)
+    old = oracle.round_to_fp32(lp + torch.randn(R, generator=g).double().numpy() * 0.3)
+    ref = oracle.round_to_fp32(lp + torch.randn(R, generator=g).double().numpy() * 0.1)
+    inp = W.Inputs(W.get("tiny_fp32", B=B, L=L, V=V), x, idx, adv, mask, dloss, None, None, None, None)
+    out = torch.empty(B, L, V, dtype=torch.bfloat16, device=DEV)
+    f, dl, err = run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=out)
+    assert err == 0
+    compare_grpo_rows(inp, f, dl, np.arange(R), old, ref, T, beta, el, eh, f"fused long rows V={V}")
+    x2 = x.clone()
+    inp2 = W.Inputs(inp.spec, x2, idx, adv, mask, dloss, None, None, None, None)
+    f2, dl2, err2 = run_gpu_fused(inp2, old, ref, T, beta, el, eh, dlogits=x2)   # in place
+    assert err2 == 0 and dl2.data_ptr() == x2.data_ptr()
+    assert torch.equal(dl2.view(torch.int16), dl.view(torch.int16))
+    for k in ("loss", "logp", "lse", "entropy"):
+        assert torch.equal(f2[k], f[k]), k
+
+
+def test_fused_long_rows_several_waves():
+    """Several waves of rows at V = 151936 (800 rows, about 300 resident at once, so rows
+    compete for L2 between their two sweeps): random masked rows and a run of 150 masked rows,
+    a zero-advantage sequence with beta = 0 (zero rows decided after the statistic); every row
+    against the oracle, in place equal bit for bit to out of place."""
+    B, L, V = 8, 100, 151936
+    R = B * L
+    x, idx, adv, mask, dloss = edge_inputs(B, L, V, torch.bfloat16, 0, 0, 4242)
+    mask[120:270] = 0
+    adv[2] = 0.0
+    T, beta, el, eh = f32(0.9), 0.0, f32(0.2), f32(0.28)
+    xo = rows_f64(select_rows(x, np.arange(R)))
+    lp, _ = oracle.selective_log_softmax(xo, idx.cpu().numpy(), T)
+    del xo
+    g = torch.Generator().manual_seed(17)
+    old = oracle.round_to_fp32(lp + torch.randn(R, generator=g).double().numpy() * 0.3)
+    inp = W.Inputs(W.get("tiny_fp32", B=B, L=L, V=V), x, idx, adv, mask, dloss, None, None, None, None)
+    out = torch.empty(B, L, V, dtype=torch.bfloat16, device=DEV)
+    f, dl, err = run_gpu_fused(inp, old, None, T, beta, el, eh, dlogits=out)
+    assert err == 0
+    for r0 in range(0, R, 50):
+        compare_grpo_rows(inp, f, dl, np.arange(r0, r0 + 50), old, None, T, beta, el, eh, f"many rows {r0}")
+    x2 = x.clone()
+    inp2 = W.Inputs(inp.spec, x2, idx, adv, mask, dloss, None, None, None, None)
+    f2, dl2, err2 = run_gpu_fused(inp2, old, None, T, beta, el, eh, dlogits=x2)
+    assert err2 == 0
+    assert torch.equal(dl2.view(torch.int16), dl.view(torch.int16))
+    assert torch.equal(f2["logp"], f["logp"]) and torch.equal(f2["entropy"], f["entropy"])
+
+
 # ---------------------------------------------------------------------------
 # entropy backward
 # ---------------------------------------------------------------------------
