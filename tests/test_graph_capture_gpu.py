@@ -61,3 +61,46 @@ def test_grpo_step_replays_in_a_cuda_graph(name):
     for k in eager:
         assert torch.equal(eager[k], graphed[k]), k
     assert torch.equal(dl_eager.view(torch.uint8), dl_graph.view(torch.uint8))
+
+
+def test_fused_linear_replays_in_a_cuda_graph_and_follows_the_mask():
+    """grpo_fused_linear in a CUDA graph: the rows of each chunk are picked on the device, so
+    the captured call needs no host synchronisation, and a replay after the mask has changed
+    (in place) packs the new unmasked rows.  Each replay equals an eager call on the same
+    inputs bit for bit (grad_weight accumulated from zero)."""
+    g = torch.Generator().manual_seed(7)
+    B, L, H, V, chunk = 3, 40, 64, 1003, 32
+    R = B * L
+    h = torch.randn(R, H, generator=g).to(torch.bfloat16).to(DEV)
+    Wt = (torch.randn(V, H, generator=g) * 0.25).to(torch.bfloat16).to(DEV)
+    idx = torch.randint(0, V, (R,), generator=g).to(DEV)
+    adv = torch.randn(B, generator=g).float().to(DEV)
+    mask = (torch.rand(R, generator=g) > 0.3).to(torch.uint8).to(DEV)
+    dloss = (torch.rand(R, generator=g) + 0.1).float().to(DEV)
+    ws = torch.empty(rp.grpo_fused_linear_workspace_size(H, V, chunk), dtype=torch.uint8, device=DEV)
+    kw = dict(B=B, L=L, T=0.9, beta=0.0, eps_low=0.2, eps_high=0.28, mask=mask, chunk_rows=chunk, workspace=ws)
+
+    def eager():
+        gw = torch.zeros(V, H, device=DEV)
+        out = rp.grpo_fused_linear(h, Wt, idx, adv, dloss, grad_weight=gw, **kw)
+        torch.cuda.synchronize()
+        return {k: v.clone() for k, v in out.items()}
+
+    gw = torch.zeros(V, H, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):                      # warm up (set-up of the GEMM launches) on the side stream
+        rp.grpo_fused_linear(h, Wt, idx, adv, dloss, grad_weight=gw, **kw)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = rp.grpo_fused_linear(h, Wt, idx, adv, dloss, grad_weight=gw, **kw)
+    for new_mask in (None, (torch.arange(R, device=DEV) % 7 != 3).to(torch.uint8)):
+        if new_mask is not None:
+            mask.copy_(new_mask)
+        want = eager()
+        gw.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in ("loss", "logp", "lse", "kl", "is_clipped", "entropy", "grad_hidden", "grad_weight"):
+            assert torch.equal(captured[k], want[k]), k
