@@ -13,6 +13,13 @@
 // element is g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
 // grad_hidden's contraction runs over the whole vocabulary, so it is split along K; the
 // splits are summed in a fixed order by a small kernel, so results do not depend on timing.
+//
+// The chunks hold unmasked rows only.  A masked row's outputs and gradients are zero by
+// definition, so it is given them once per call and never enters a chunk.  Before each chunk a
+// one-CTA kernel picks the next unmasked rows from the device-side mask, and a gather kernel
+// copies their hidden states into consecutive rows.  The GEMMs read the chunk's row count from
+// the device.  Nothing goes back to the host, so a call can be captured in a CUDA graph and
+// follows the mask a replay finds.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
