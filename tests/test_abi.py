@@ -249,3 +249,28 @@ def test_autograd_wrappers_have_no_cpu_path():
         ag.entropy(x)
     with pytest.raises(ValueError, match="CUDA"):
         ag.grpo_loss(x, idx, torch.zeros(2))
+
+
+def test_a_failed_launch_returns_grpo_err_cuda():
+    """A call whose arguments pass validation but whose launch fails returns
+    GRPO_ERR_CUDA and does not crash.  The failure is made on the host: the call runs in a
+    child process with no CUDA device visible, so the launch is refused before any kernel
+    exists and the fake device addresses are never dereferenced, on any machine."""
+    import subprocess
+    import sys
+    code = (
+        "import ctypes, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "from rl_fine_tuning_pass_gb300 import binding\n"
+        "lib = binding.load_library()\n"
+        f"F = {FAKE}\n"
+        "x = binding.GrpoRows(F, binding.GRPO_BF16, 0, 2, 3, 64, 192, 64)\n"
+        "st = lib.grpo_loss_fwd(ctypes.byref(x), F, None, None, F, None, 1.0, 0.0, 0.2, 0.2,\n"
+        "                       F, F + 64, F + 128, None, None, None, None, None)\n"
+        "print(st)\n"
+    )
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    build()
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip().splitlines()[-1] == str(binding.GRPO_ERR_CUDA)
