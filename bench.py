@@ -700,7 +700,7 @@ def run_linear(args):
                 "scaling": "weak", "vs_baseline": None, "data": "synthetic",
                 "config": {"workload": spec.name, "B": spec.B, "L": spec.L, "H": spec.H, "V": spec.V, "T": spec.T,
                            "beta": spec.beta, "eps_low": spec.eps_low, "eps_high": spec.eps_high,
-                           "chunk_rows": step.chunk, "operands": "bf16 hidden and head weight; fp32 logits per chunk",
+                           "chunk_rows": step.chunk, "operands": "bf16 hidden and head weight; fp32 accumulation; per chunk, fp16 exponentials of the logits relative to each 128-column maximum, turned into bf16 dlogits in place",
                            "l2": "flushed before every timed step (256 MB write + 256 MB read, not timed)",
                            "parallelism": f"{world} independent batch(es), one per GPU"},
                 "value": round(rows_per_s, 1), "steps": K, "warmup": Wm, "ms_per_step": round(step_ms, 4),

@@ -378,8 +378,13 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  *   (forward outputs, dlogits in bf16)  ->  grad_hidden_c = dlogits_c W,
  *   grad_weight += dlogits_c^T h_c  (tensor-core GEMMs, fp32 accumulation).
  * All of it runs in this library's kernels: the GEMMs are tcgen05 kernels with TMA-staged
- * bf16 operands and fp32 accumulators in tensor memory; the logits GEMM also forms each
- * row's softmax statistic per 128 columns, so the row pass reads the fp32 logits once.
+ * bf16 operands and fp32 accumulators in tensor memory.  The logits GEMM forms each row's
+ * softmax statistic per 128 columns from its fp32 results, and stores, instead of the logits,
+ * their exponentials relative to each 128-column maximum, e_j = exp((x_j - max) / T), in fp16
+ * (scaled by 2^15, so that every e_j above 2^-29 keeps 11 significant bits); the row pass
+ * scales them into bf16 dlogits in place.  dlogits thus carry an fp16 rounding of e_j before
+ * their bf16 rounding; x[idx] is formed apart in fp32 from the row's hidden state and row
+ * idx of the head weight.
  * grad_hidden's GEMM is split along the vocabulary and its splits are summed in a fixed
  * order, and each element of grad_weight receives one add per chunk, so the results do not
  * depend on timing.
@@ -398,16 +403,16 @@ grpo_status selective_log_softmax_bwd_vocab_shard(const grpo_rows* logits_shard,
  *   chunk_rows    rows per chunk, >= 1 (the last chunk may be shorter)
  *   workspace     device scratch of at least grpo_fused_linear_workspace_size() bytes,
  *                 256-byte aligned; its contents are not kept between calls.  The size is
- *                 one chunk's fp32 logits, bf16 dlogits, statistics, gathered hidden rows
- *                 and row list (6 V8 + 32 ceil(V / 256) + 2 H + 4 bytes a row, V8 = V
+ *                 one chunk's 16-bit exponentials / dlogits, statistics, gathered hidden rows
+ *                 and row list (2 V8 + 32 ceil(V / 256) + 2 H + 4 bytes a row, V8 = V
  *                 rounded up to a multiple of 8, each part rounded up to 256 bytes, plus
  *                 256) and max(128 MiB, chunk_rows * H * 4) for the K splits of
  *                 grad_hidden (as many splits of chunk_rows * H * 4 bytes as fit, at most 32)
  *   grad_hidden   [B*L, H] fp32 output (overwritten), or NULL
  *   grad_weight   [V, H] fp32, ACCUMULATED into (+=), or NULL; 16-byte aligned
  *
- * The logits are formed in fp32; dlogits are rounded to bf16 (the weight's type) for the
- * two backward GEMMs.  Calls on the same stream run in order.  A GEMM whose own copies or
+ * The logits are formed in fp32; the statistics (lse, entropy) and x[idx] come from fp32
+ * values; dlogits are bf16 (the weight's type) for the two backward GEMMs.  Calls on the same stream run in order.  A GEMM whose own copies or
  * MMAs stall for about 2 s gives up, sets GRPO_DEVERR_TIMEOUT in *dev_err and returns.
  */
 grpo_status grpo_fused_linear_workspace_size(int64_t H, int64_t V, int64_t chunk_rows, uint64_t* bytes);
@@ -425,14 +430,14 @@ grpo_status grpo_fused_linear(const void* hidden, const void* weight, int64_t B,
  * handed to a pool it does not control, or a step that must not stall on an allocation).
  * The pages have no counterpart; this is a convenience of this library.
  *
- * Its scratch (one chunk's fp32 logits, bf16 dlogits, per-128-column statistics, gathered
+ * Its scratch (one chunk's 16-bit exponentials / dlogits, per-128-column statistics, gathered
  * hidden rows and row list, and the K splits of grad_hidden) is a fixed 32 MiB device array
  * inside the library, which every device context that loads the library holds until the
- * process exits.  Limit: the chunk buffers, chunk_rows * (4 V8 + 2 V8 + 32 ceil(V / 256) +
- * 2 H + 4) bytes in five parts each rounded up to 256 bytes, plus 256 bytes, plus one split
- * of grad_hidden, chunk_rows * H * 4 bytes, must fit in 32 MiB (V8 = V rounded up to a
- * multiple of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before any launch.  For
- * V = 151936 and H = 1024 that is at most 35 rows per chunk.
+ * process exits.  Limit: the chunk buffers, chunk_rows * (2 V8 + 32 ceil(V / 256) + 2 H + 4)
+ * bytes in four parts each rounded up to 256 bytes, plus 256 bytes, plus one split of
+ * grad_hidden, chunk_rows * H * 4 bytes, must fit in 32 MiB (V8 = V rounded up to a multiple
+ * of 8); a larger chunk returns GRPO_ERR_UNSUPPORTED before any launch.  For V = 151936 and
+ * H = 1024 that is at most 101 rows per chunk.
  *
  * The first call on a device (and the first after a cudaDeviceReset) does the set-up: it
  * looks up the array's device address in the current context.  Make that first call

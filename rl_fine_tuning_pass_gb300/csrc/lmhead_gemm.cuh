@@ -6,10 +6,12 @@
 //   D[M, N] = A[M, K] B[K, N]    bf16 operands, fp32 accumulation in tensor memory
 //
 // with three epilogues:
-//   kEpiLogits  D is the chunk's fp32 logits (M = rows, N = V, K = H); besides storing
-//               them, each tile forms the online softmax statistic (a, s, u) of each half
-//               (128 columns) of every row, so the row pass that follows needs one sweep
-//               over the row instead of two;
+//   kEpiLogits  D is the chunk's logits (M = rows, N = V, K = H), kept in registers: each
+//               tile forms the softmax statistic (a, s, u) of each half (128 columns) of
+//               every row, a = c max x_j, and stores, in place of the logits, the
+//               exponentials e_j = 2^(x_j c - a) as fp16 scaled by 2^15 (C is then a 16-bit
+//               matrix), half the bytes of fp32 logits.  The row pass turns them into bf16
+//               dlogits in place: |g| p_j = e_j 2^(a - lse log2 e + log2 |g|);
 //   kEpiStore   D is stored (one K split of grad_hidden: M = rows, N = H, K = V);
 //   kEpiAccum   D is added to the fp32 output (grad_weight += dlogits^T h: M = V, N = H,
 //               K = rows).
@@ -25,11 +27,11 @@
 // MMAs and commits them to both CTAs' barriers.  Warps 2-9 of each CTA read its 128 rows
 // of the finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes of its
 // quarter; two warps share a quarter, one for each half of the columns) while the MMAs of
-// the next tile fill the other accumulator.  Each warp passes its 32 x 32 fp32 boxes through
-// a 128-byte-swizzled staging buffer (one row per lane in, four rows of 128 bytes per
-// instruction out), so that its global stores (kEpiLogits, kEpiStore) or vector reduce-adds
-// (kEpiAccum) write whole 128-byte lines; stores are fire-and-forget, so many lines per SM
-// are in flight.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
+// the next tile fill the other accumulator.  Each warp passes its 32 x 32 boxes through a
+// swizzled staging buffer (one row per lane in; out, four fp32 rows of 128 bytes or eight
+// bf16 rows of 64 bytes per instruction), so that its global stores (kEpiLogits, kEpiStore)
+// or vector reduce-adds (kEpiAccum) write whole row segments; stores are fire-and-forget, so
+// many lines per SM are in flight.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
 // grad_hidden) or MN-major (M or N contiguous: W in grad_hidden, dlogits^T and h in
 // grad_weight); the MN-major tiles are loaded as 64-wide boxes and described to the MMA
 // with the MN-major bit.
@@ -41,6 +43,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -75,6 +78,7 @@ struct Params {
   int m_tiles, n_tiles, splits;  // m_tiles counts the pair's 256-row tiles
   int m_fastest;       // 1: consecutive tiles share a B tile; 0: share an A tile
   float* C;            // fp32 output [M][ldc] (+ split * split_stride); ldc a multiple of 4
+                       // (kEpiLogits: 16-bit [M][ldc], ldc a multiple of 8)
   int64_t ldc, split_stride;
   // kEpiLogits only
   float4* stats;       // [M][2 n_tiles]: (a, s, u, 0) of each half tile's 128 columns
@@ -295,29 +299,87 @@ __device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, in
   }
 }
 
-// Fold 32 logits (the first `valid` of them) into the tile's running statistic, with the
-// numerics of the row kernels' stream (rowpass_fwd.cuh: one rescale per chunk, packed f32x2
-// sums).
-template <bool kH>
-__device__ __forceinline__ void stat_cols(Running& rs, float (&v)[32], int valid, float c) {
-  if (valid < 32) {
+// The logits epilogue's statistic over one row's 128 columns of the tile (the first `cols`
+// of them inside the matrix): the maximum m (tile_max), then, box by box, the exponentials
+// e_j = 2^(x_j c - a) with a = m c, written over the box, and s = sum e_j,
+// u = sum e_j (x_j c - a) (box_exp).  Columns at or past N get e = 0.  (The same (a, s, u) the
+// row kernels form, here in two passes over values already in registers, so no rescale.)
+__device__ __forceinline__ float tile_max(const float (&v)[BN / 64][32], int cols) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < BN / 64; ++j)
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (i >= valid) v[i] = -INFINITY;  // adds 2^-inf = 0; t * 0 is guarded below
-  }
-  float cm = v[0];
-#pragma unroll
-  for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
-  if (cm > rs.m) run_rescale<kH>(rs, cm, c);
-  const float2 c2 = make_float2(c, c), na2 = make_float2(-rs.a, -rs.a);
+      if (32 * j + i < cols) m = fmaxf(m, v[j][i]);
+  return m;
+}
+template <bool kH>
+__device__ __forceinline__ void box_exp(float (&v)[32], int cols, float2 c2, float2 na2, float2& s2, float2& u2) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float2 x = make_float2(v[2 * i], v[2 * i + 1]);
+    float2 x = make_float2(2 * i < cols ? v[2 * i] : -INFINITY, 2 * i + 1 < cols ? v[2 * i + 1] : -INFINITY);
     if (kH) {
-      x.x = fmaxf(x.x, kNegClamp);  // -inf (padding or input) adds 0 to u, not 0 * -inf
+      x.x = fmaxf(x.x, kNegClamp);  // -inf adds 0 to u, not 0 * -inf
       x.y = fmaxf(x.y, kNegClamp);
     }
-    run_pair<kH>(rs, x, c2, na2);
+    const float2 t = __ffma2_rn(x, c2, na2);
+    const float2 e = make_float2(ex2(t.x), ex2(t.y));
+    s2 = __fadd2_rn(s2, e);
+    if (kH) u2 = __ffma2_rn(e, t, u2);
+    v[2 * i] = e.x;
+    v[2 * i + 1] = e.y;
+  }
+}
+
+// The exponentials are stored as fp16 scaled by 2^15 (kExpScaleLog2): e <= 1 becomes at most
+// 32768, below fp16's 65504, and fp16's normal range then reaches down to e = 2^-29, so the
+// relative rounding is 2^-11 for every e that can matter.
+constexpr float kExpScale = 32768.f;
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a * kExpScale, b * kExpScale);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Row `lane` of a warp's 32 x 32 box of exponentials, as fp16, into its staging buffer (64
+// bytes a row): the 16-byte chunk q of row r sits at chunk q ^ ((r / 2) % 4), so the eight
+// rows a quarter-warp writes at once cover all 32 banks.
+__device__ __forceinline__ void stage_row_h16(uint32_t buf, int lane, const float (&v)[32]) {
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = make_uint4(pack_h2(v[8 * q], v[8 * q + 1]), pack_h2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_h2(v[8 * q + 4], v[8 * q + 5]), pack_h2(v[8 * q + 6], v[8 * q + 7]));
+    const uint32_t dst = row + static_cast<uint32_t>((q ^ ((lane >> 1) & 3)) * 16);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                 : "memory");
+  }
+}
+
+// Write a staged 32 x 32 box of 16-bit values to rows [0, rows) and columns [0, cols) of the
+// 16-bit matrix at `dst` (row stride ld elements, a multiple of 8): lane l takes 16-byte chunk l % 4 of rows
+// l / 4 + 8 i, so each instruction covers eight whole 64-byte row segments.
+__device__ __forceinline__ void write_box_h16(uint32_t buf, int lane, uint16_t* dst, int64_t ld, int rows,
+                                               int cols) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    uint4 w;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                 : "r"(buf + static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) * 16))));
+    if (r >= rows || 8 * q >= cols) continue;
+    uint16_t* d = dst + r * ld + 8 * q;
+    if (8 * q + 8 <= cols) {
+      *reinterpret_cast<uint4*>(d) = w;
+    } else {
+      const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (8 * q + k >= cols) break;
+        d[k] = static_cast<uint16_t>(e[k >> 1] >> (16 * (k & 1)));
+      }
+    }
   }
 }
 
@@ -492,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                              static_cast<uint32_t>(acc * BN + half * (BN / 2));
       const int col_base = u.n * BN + half * (BN / 2);
       float* cbase = p.C + static_cast<int64_t>(u.s) * p.split_stride;
-      Running rs{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       const int boxes = min(BN / 64, (p.N - col_base + 31) / 32);  // boxes with columns below N
       // all of this warp's 128 accumulator columns into registers with one wait, then the
       // accumulator goes back to the MMA while the statistic and the stores proceed
@@ -503,23 +564,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(map_to_rank(tempty0 + 8 * acc, 0));  // done with it
-#pragma unroll
-      for (int j = 0; j < BN / 64; ++j) {
-        if (j >= boxes) break;
-        const int col0 = col_base + 32 * j;
-        const int valid = p.N - col0;
-        if constexpr (EPI == kEpiLogits) {
-          if (row_ok) stat_cols<kH>(rs, v[j], valid, p.c);  // columns at or past N become -inf, not stored
-        }
-        stage_row(buf, lane, v[j]);
-        __syncwarp();
-        write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0, valid);
-        __syncwarp();  // every lane has read the box before the next one is staged
-      }
       if constexpr (EPI == kEpiLogits) {
+        // the statistic of the row's 128 columns, and the exponentials relative to their
+        // maximum stored (fp16, scaled by 2^15) in place of the logits
+        const float m = tile_max(v, p.N - col_base);
+        const float st_a = m * p.c;
+        // every logit -inf: e = 0 and nothing to add, with a finite shift (no -inf - -inf)
+        const float shift = m == -INFINITY ? 0.f : st_a;
+        const float2 c2 = make_float2(p.c, p.c), na2 = make_float2(-shift, -shift);
+        float2 s2 = make_float2(0.f, 0.f), u2 = make_float2(0.f, 0.f);
+        uint16_t* eb = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row0) * p.ldc;
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) {
+          if (j >= boxes) break;
+          const int col0 = col_base + 32 * j;
+          box_exp<kH>(v[j], p.N - col0, c2, na2, s2, u2);
+          stage_row_h16(buf, lane, v[j]);
+          __syncwarp();
+          write_box_h16(buf, lane, eb + col0, p.ldc, dims.M - row0, p.N - col0);
+          __syncwarp();  // every lane has read the box before the next one is staged
+        }
         if (row_ok && col_base < p.N)
           p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] =
-              make_float4(rs.a, rs.s.x + rs.s.y, rs.u.x + rs.u.y, 0.f);
+              make_float4(st_a, s2.x + s2.y, u2.x + u2.y, 0.f);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) {
+          if (j >= boxes) break;
+          const int col0 = col_base + 32 * j;
+          stage_row(buf, lane, v[j]);
+          __syncwarp();
+          write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0,
+                         p.N - col0);
+          __syncwarp();  // every lane has read the box before the next one is staged
+        }
       }
     }
   }

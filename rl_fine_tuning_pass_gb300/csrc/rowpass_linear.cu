@@ -5,12 +5,16 @@
 // before the next chunk, so the logits of the whole batch never exist at once.
 //
 // The three contractions are this library's tcgen05 GEMMs (lmhead_gemm.cuh: bf16 operands
-// staged by TMA, fp32 accumulation in tensor memory).  The logits GEMM also forms, in its
-// epilogue, the online softmax statistic of every 128 columns of every row.  The row pass
-// between the GEMMs is this file's kernel: one CTA per row of the chunk merges the row's
-// statistics, runs the forward epilogue, decides the row factor g, and sweeps the fp32 row
-// once to write dlogits in bf16, the operand type of the two backward GEMMs.  The idx
-// element is g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
+// staged by TMA, fp32 accumulation in tensor memory).  The logits GEMM forms, in its
+// epilogue, the softmax statistic of every 128 columns of every row from its fp32 results,
+// and stores, in place of the logits, their exponentials relative to each 128-column maximum
+// (fp16, scaled by 2^15): half the bytes of fp32 logits, and no exponential left for the row
+// pass.  The row
+// pass between the GEMMs is this file's kernel: one CTA per row of the chunk merges the row's
+// statistics, forms x[idx] in fp32 from the row's hidden state and the head weight, runs the
+// forward epilogue, decides the row factor g, and scales the row's exponentials into bf16
+// dlogits in place, the operand type of the two backward GEMMs.  The idx element is
+// g (1 - p_idx) formed as the complementary sum, as in the unsplit backward.
 // grad_hidden's contraction runs over the whole vocabulary, so it is split along K; the
 // splits are summed in a fixed order by a small kernel, so results do not depend on timing.
 //
@@ -25,6 +29,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "grpo_rowpass.h"
 #include "lmhead_gemm.cuh"
 #include "rowpass_bwd.cuh"
@@ -36,51 +42,75 @@ namespace {
 // Threads of the row-pass CTA (one row each).
 constexpr int kLinearThreads = 512;
 
-// Row pass over one chunk: fp32 logits [rows][ld] in, bf16 dlogits [rows][ld] out.
-template <int THREADS, int UNROLL, bool kH, bool NEG>
-__device__ __forceinline__ float linear_sweep2(const float* row, uint16_t* out, int V, int idx, float c, float nK,
-                                               bool& owner) {
+// The row pass's sweep over one row of the chunk, in place: the logits GEMM left the
+// exponentials e_j = 2^(x_j c - a_t) of each 128-column part t (a_t = c max x over the part, the
+// statistic's .x) as fp16 scaled by 2^15; with nK = log2|g| - lse log2 e,
+// |g| p_j = e_j 2^(a_t + nK), written back as bf16 dlogits d_j = -sign(g) |g| p_j.  Returns
+// this thread's share of sum_{j != idx} |g| p_j.
+__device__ __forceinline__ float2 unpack_h2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+template <int THREADS, bool NEG>
+__device__ __forceinline__ float linear_sweep_e(uint16_t* row, const float4* __restrict__ st_row, int V, int idx,
+                                                float nK, bool& owner) {
+  constexpr float kUnscale = -15.f;  // log2 of the exponentials' 2^-15 scale
   const int tid = threadIdx.x;
-  const uint4* vb = reinterpret_cast<const uint4*>(row);
-  uint4* ob = reinterpret_cast<uint4*>(out);
-  const float2 c2 = make_float2(c, c), nK2 = make_float2(nK, nK);
+  uint4* vb = reinterpret_cast<uint4*>(row);
   float q_acc = 0.f;
   float2 q2 = make_float2(0.f, 0.f);
-  const int groups = V / 8;  // 8 logits (two 16-byte fp32 vectors) -> one 16-byte bf16 vector
+  const int groups = V / 8;  // 8 exponentials (one 16-byte vector) -> 8 dlogits, in place
   for (int i = tid; i < groups; i += THREADS) {
-    const uint4 a = ld_v4_evict_first(vb + 2 * i), b = ld_v4_evict_first(vb + 2 * i + 1);
-    float2 e[4];
-    const float2 x[4] = {make_float2(__uint_as_float(a.x), __uint_as_float(a.y)),
-                         make_float2(__uint_as_float(a.z), __uint_as_float(a.w)),
-                         make_float2(__uint_as_float(b.x), __uint_as_float(b.y)),
-                         make_float2(__uint_as_float(b.z), __uint_as_float(b.w))};
+    const uint4 w = vb[i];
+    const float sc = ex2(st_row[i >> 4].x + (nK + kUnscale));  // 16 vectors per 128-column part
+    const float2 s2 = make_float2(sc, sc);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float2 e[BF16::kPairs];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 t = __ffma2_rn(x[q], c2, nK2);
-      e[q] = make_float2(ex2(t.x), ex2(t.y));
-    }
+    for (int q = 0; q < BF16::kPairs; ++q) e[q] = __fmul2_rn(unpack_h2(wv[q]), s2);
     const unsigned k = static_cast<unsigned>(idx - 8 * i);
-    if (k < 8u) {  // this group holds idx: leave it out of the sum
+    if (k < 8u) {  // this vector holds idx: leave it out of the sum
       owner = true;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < BF16::kPairs; ++q) {
         if (2 * q != static_cast<int>(k)) q_acc += e[q].x;
         if (2 * q + 1 != static_cast<int>(k)) q_acc += e[q].y;
       }
     } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) q2 = __fadd2_rn(q2, e[q]);
+      for (int q = 0; q < BF16::kPairs; ++q) q2 = __fadd2_rn(q2, e[q]);
     }
-    st_v4_evict_first(ob + i, BF16::pack_pairs<NEG>(e));
+    vb[i] = BF16::template pack_pairs<NEG>(e);
   }
   const int j = 8 * groups + tid;  // the last V % 8 elements
   if (j < V) {
-    const float e = ex2(fmaf(row[j], c, nK));
+    const __half hj = *reinterpret_cast<const __half*>(row + j);
+    const float d = __half2float(hj) * ex2(st_row[j >> 7].x + (nK + kUnscale));
     if (j == idx) owner = true;
-    else q_acc += e;
-    BF16::store_scalar(out + j, NEG ? -e : e);
+    else q_acc += d;
+    BF16::store_scalar(row + j, NEG ? -d : d);
   }
   return q_acc + (q2.x + q2.y);
+}
+
+// x[idx] of one row: its hidden state times row idx of the head weight, in fp32 (one warp).
+// The logits GEMM forms the same value (exact bf16 products, fp32 sums) in another order.
+__device__ __forceinline__ float linear_x_idx(const uint16_t* __restrict__ h, const uint16_t* __restrict__ w,
+                                              int64_t H, int lane) {
+  const uint4* hv = reinterpret_cast<const uint4*>(h);
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+  float acc = 0.f;
+  for (int64_t k = lane; k < H / 8; k += 32) {
+    const uint4 a = hv[k], b = wv[k];
+#pragma unroll
+    for (int q = 0; q < BF16::kPairs; ++q) {
+      const float2 x = BF16::pair(a, q), y = BF16::pair(b, q);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  return acc;
 }
 
 __device__ __forceinline__ void fill_bf16_row(uint16_t* out, int V, uint32_t pair, int nthreads) {
@@ -92,10 +122,10 @@ __device__ __forceinline__ void fill_bf16_row(uint16_t* out, int V, uint32_t pai
 }
 
 // One CTA per row of the chunk: merge the row's statistics, the forward epilogue and the row
-// factor, then one sweep over the fp32 row writing bf16 dlogits.  Row i of the chunk is batch
-// row list[i]; the chunk holds state[0] rows, and the rows after them up to the next
-// multiple of 64 get zero dlogits, since grad_weight's GEMM reads its K (row) dimension in
-// blocks of 64.
+// factor, then one sweep over the row's fp16 exponentials turning them into bf16 dlogits in
+// place.  Row i of the chunk is batch row list[i]; the chunk holds state[0] rows, and the rows
+// after them up to the next multiple of 64 get zero dlogits, since grad_weight's GEMM reads
+// its K (row) dimension in blocks of 64.
 template <int THREADS, int UNROLL, bool kH>
 __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkParams q) {
   wait_for_previous_grids();
@@ -113,11 +143,14 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   const int64_t r = q.list[rl];  // row of the batch (never a masked one)
   const int64_t b = r / p.x.L;
   const float c = p.c;
-  const float* row = q.logits + rl * q.ld;
 
   const int64_t id64 = p.idx[r];
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
+  // the selected logit, from the row's hidden state and the head weight (warp 0), while the
+  // other warps start on the statistics
+  float x_idx = 0.f;
+  if (tid < 32 && !bad_idx) x_idx = linear_x_idx(q.hidden_rows + rl * q.H, q.weight + idx * q.H, q.H, tid);
 
   // the row's statistic: its 128-column parts, merged in a fixed order
   const int n_valid = (V + 127) / 128;
@@ -127,7 +160,6 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
     const float4 e = st_row[k];
     mine = stat_combine(mine, Stat{e.x, e.y, e.z});
   }
-  const float x_idx = tid == 0 ? row[idx] : 0.f;
   const Stat st = stat_block_reduce<THREADS>(mine);
 
   __shared__ float sh_g, sh_nK;
@@ -151,8 +183,8 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   // the sweep: d_j = -sign(g) |g| p_j in bf16, and g (1 - p_idx) at idx
   bool owner = false;
   const float nK = sh_nK;
-  const float q_part = g > 0.f ? linear_sweep2<THREADS, UNROLL, kH, true>(row, out, V, idx, c, nK, owner)
-                               : linear_sweep2<THREADS, UNROLL, kH, false>(row, out, V, idx, c, nK, owner);
+  const float q_part = g > 0.f ? linear_sweep_e<THREADS, true>(out, st_row, V, idx, nK, owner)
+                               : linear_sweep_e<THREADS, false>(out, st_row, V, idx, nK, owner);
   const float q_total = block_sum_all<THREADS>(q_part);
   if (owner) BF16::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
@@ -358,7 +390,7 @@ struct LinearLauncher {
     pl.n_tiles = static_cast<int>((q.V + BN - 1) / BN);
     pl.splits = 1;
     pl.m_fastest = 1;
-    pl.C = b.logits;
+    pl.C = reinterpret_cast<float*>(b.dlogits);  // bf16 exponentials (kEpiLogits)
     pl.ldc = q.ld;
     pl.stats = b.stats;
     pl.c = q.chunk_params.f.c;
@@ -372,8 +404,10 @@ struct LinearLauncher {
   cudaError_t rows(cudaStream_t s) const {
     const LinearChunkBufs& b = q.bufs;
     LinearChunkParams lp = q.chunk_params;
-    lp.logits = b.logits;
     lp.stats = b.stats;
+    lp.hidden_rows = b.hidden;
+    lp.weight = q.weight;
+    lp.H = q.H;
     lp.dlogits = b.dlogits;
     lp.ld = q.ld;
     lp.n_stat = static_cast<int>(linear_n_stat(q.V));
@@ -474,8 +508,8 @@ cudaError_t launch_fused_linear(const FusedLinearParams& q, cudaStream_t stream)
 // For callers that must not allocate device memory at call time (an allocator-free
 // runtime, a host process that has handed all device memory to a pool it does not own, a
 // code path that must not synchronise on an allocation).  The scratch grpo_fused_linear
-// takes from the caller (one chunk's fp32 logits, bf16 dlogits and statistics, and the K
-// splits of grad_hidden) lives here in one array of kNoallocScratchBytes, reserved in every
+// takes from the caller (one chunk's 16-bit exponentials / dlogits, statistics, gathered hidden
+// rows and row list, and the K splits of grad_hidden) lives here in one array of kNoallocScratchBytes, reserved in every
 // device context that loads this library and held until the process exits.  Every call uses
 // the whole array: calls that run at the same time on the GPU (different streams, threads or
 // host processes sharing the context) race on it.  Nothing in it has to start at zero: each
@@ -551,7 +585,7 @@ extern "C" grpo_status grpo_fused_linear_noalloc(
   const int64_t rows = B * L;
   if (rows == 0) return GRPO_OK;
   const int64_t chunk = chunk_rows < rows ? chunk_rows : rows;
-  // the fixed array's limit: the chunk's buffers (fp32 logits, bf16 dlogits, statistics,
+  // the fixed array's limit: the chunk's buffers (16-bit exponentials / dlogits, statistics,
   // gathered bf16 hidden rows, row list and state, each rounded up to 256 bytes) and one
   // split of grad_hidden (chunk * H fp32) <= 32 MiB
   const uint64_t chunk_bytes = grpo::linear_chunk_bytes(H, V, chunk);

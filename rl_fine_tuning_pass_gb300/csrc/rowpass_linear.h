@@ -14,9 +14,11 @@ namespace grpo {
 struct LinearChunkParams {
   FwdParams f;            // per-row inputs and outputs of the whole batch; f.x.L = tokens per
                           // sequence, f.x.V = vocabulary
-  const float* logits;    // the chunk's logits [rows][ld] fp32
   const float4* stats;    // the chunk's per-128-column statistics [rows][n_stat]
-  uint16_t* dlogits;      // the chunk's dlogits [rows][ld] bf16 (written)
+  uint16_t* dlogits;      // [rows][ld]: the logits GEMM's fp16 exponentials in, bf16 dlogits out
+  const uint16_t* hidden_rows;  // the chunk's gathered hidden states [rows][H] bf16
+  const uint16_t* weight;       // the head weight [V][H] bf16
+  int64_t H;
   int64_t ld;             // elements between rows, a multiple of 8
   int n_stat;             // statistics slots per row (two per 256-column tile)
   const int32_t* list;    // the chunk's rows: row i of the chunk is batch row list[i]
@@ -25,12 +27,11 @@ struct LinearChunkParams {
   const float* dloss;     // [batch rows]
   float T;
 };
-// One chunk's buffers: its fp32 logits [chunk][ld], bf16 dlogits [chunk][ld], the
-// statistics of the logits GEMM [chunk][2 ceil(V / 256)], its hidden states gathered into
-// consecutive rows [chunk][H] bf16, the batch rows they come from [chunk] and the chunk's
-// state: [0] its number of rows, [1] the batch row after its last one.
+// One chunk's buffers: 16-bit [chunk][ld] (the logits GEMM's fp16 exponentials, then the row
+// pass's bf16 dlogits in their place), the statistics of the logits GEMM [chunk][2 ceil(V / 256)], its
+// hidden states gathered into consecutive rows [chunk][H] bf16, the batch rows they come from
+// [chunk] and the chunk's state: [0] its number of rows, [1] the batch row after its last one.
 struct LinearChunkBufs {
-  float* logits;
   uint16_t* dlogits;
   float4* stats;
   uint16_t* hidden;
@@ -55,13 +56,12 @@ inline uint64_t linear_round256(uint64_t v) { return (v + 255) & ~uint64_t(255);
 inline int64_t linear_ld(int64_t V) { return (V + 7) / 8 * 8; }
 inline int64_t linear_n_stat(int64_t V) { return 2 * ((V + 255) / 256); }
 struct LinearChunkLayout {
-  uint64_t logits, dlogits, stats, hidden, list, state;  // bytes of each part
-  uint64_t total() const { return logits + dlogits + stats + hidden + list + state; }
+  uint64_t dlogits, stats, hidden, list, state;  // bytes of each part
+  uint64_t total() const { return dlogits + stats + hidden + list + state; }
 };
 inline LinearChunkLayout linear_chunk_layout(int64_t H, int64_t V, int64_t chunk) {
   const uint64_t ld = static_cast<uint64_t>(linear_ld(V)), c = static_cast<uint64_t>(chunk);
-  return LinearChunkLayout{linear_round256(ld * c * 4),
-                           linear_round256(ld * c * 2),
+  return LinearChunkLayout{linear_round256(ld * c * 2),
                            linear_round256(static_cast<uint64_t>(linear_n_stat(V)) * c * 16),
                            linear_round256(static_cast<uint64_t>(H) * c * 2),
                            linear_round256(c * 4),
@@ -74,8 +74,6 @@ inline uint64_t linear_chunk_bytes(int64_t H, int64_t V, int64_t chunk) {
 inline void linear_carve(FusedLinearParams& q, char* base, uint64_t total_bytes) {
   const LinearChunkLayout l = linear_chunk_layout(q.H, q.V, q.chunk);
   char* p = base;
-  q.bufs.logits = reinterpret_cast<float*>(p);
-  p += l.logits;
   q.bufs.dlogits = reinterpret_cast<uint16_t*>(p);
   p += l.dlogits;
   q.bufs.stats = reinterpret_cast<float4*>(p);

@@ -113,10 +113,11 @@ def compare_to_workspace_entry_point(lib, x, chunk, what):
 
 @pytest.mark.parametrize("V", [151936, 151935])
 def test_noalloc_at_the_limit_of_its_array(lib, V):
-    """The largest chunk that fits the fixed array at the Qwen3 vocabulary (with H = 64: 36
-    rows; the chunk buffers then fill 33.5 of its 33.55 MB), with V a multiple of 8 and not:
-    rejected one row above it, and equal to grpo_fused_linear at it."""
-    x = inputs(3, V=V, H=64, B=1, L=40)
-    st, _ = call_noalloc(lib, x, 37)
+    """The largest chunk that fits the fixed array at the Qwen3 vocabulary (with H = 64: 103
+    rows; the chunk buffers and one split of grad_hidden then fill 33.30 of its 33.55 MB, and
+    104 rows would need 33.62), with V a multiple of 8 and not: rejected one row above it, and
+    equal to grpo_fused_linear at it."""
+    x = inputs(3, V=V, H=64, B=1, L=110)
+    st, _ = call_noalloc(lib, x, 104)
     assert st == rp.GRPO_ERR_UNSUPPORTED
-    compare_to_workspace_entry_point(lib, x, 36, f"V={V} chunk 36")
+    compare_to_workspace_entry_point(lib, x, 103, f"V={V} chunk 103")
