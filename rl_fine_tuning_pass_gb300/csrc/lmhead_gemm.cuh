@@ -300,29 +300,44 @@ __device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, in
 }
 
 // The logits epilogue's statistic over one row's 128 columns of the tile (the first `cols`
-// of them inside the matrix): the maximum m (tile_max), then, box by box, the exponentials
-// e_j = 2^(x_j c - a) with a = m c, written over the box, and s = sum e_j,
-// u = sum e_j (x_j c - a) (box_exp).  Columns at or past N get e = 0.  (The same (a, s, u) the
-// row kernels form, here in two passes over values already in registers, so no rescale.)
+// of them inside the matrix): the maximum m (tile_max), then, box by box, e_j = 2^(x_j c - a)
+// with a = m c, and s = sum e_j, u = sum e_j (x_j c - a) (box_exp).  Columns at or past N get
+// e = 0.  (The same (a, s, u) the row kernels form, here in two passes over values already in
+// registers, so no rescale.)  box_exp writes e_j 2^15 over the box, the scaled form that is
+// stored (fp16, below), by shifting the exponent: t' = x_j c - a + 15, so the scale costs no
+// multiply; s and u are taken back to the unscaled e at the end (tile_sums).
 __device__ __forceinline__ float tile_max(const float (&v)[BN / 64][32], int cols) {
   float m = -INFINITY;
+  if (cols >= BN / 2) {
 #pragma unroll
-  for (int j = 0; j < BN / 64; ++j)
+    for (int j = 0; j < BN / 64; ++j)
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (32 * j + i < cols) m = fmaxf(m, v[j][i]);
+      for (int i = 0; i < 32; ++i) m = fmaxf(m, v[j][i]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (32 * j + i < cols) m = fmaxf(m, v[j][i]);
+  }
   return m;
 }
+constexpr float kExpScaleLog2 = 15.f;  // the stored exponentials are e 2^15
 template <bool kH>
 __device__ __forceinline__ void box_exp(float (&v)[32], int cols, float2 c2, float2 na2, float2& s2, float2& u2) {
+  if (cols < 32) {  // the ragged end of the row: columns past N add nothing
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i >= cols) v[i] = -INFINITY;
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float2 x = make_float2(2 * i < cols ? v[2 * i] : -INFINITY, 2 * i + 1 < cols ? v[2 * i + 1] : -INFINITY);
+    float2 x = make_float2(v[2 * i], v[2 * i + 1]);
     if (kH) {
       x.x = fmaxf(x.x, kNegClamp);  // -inf adds 0 to u, not 0 * -inf
       x.y = fmaxf(x.y, kNegClamp);
     }
-    const float2 t = __ffma2_rn(x, c2, na2);
+    const float2 t = __ffma2_rn(x, c2, na2);  // x c - a + 15
     const float2 e = make_float2(ex2(t.x), ex2(t.y));
     s2 = __fadd2_rn(s2, e);
     if (kH) u2 = __ffma2_rn(e, t, u2);
@@ -330,13 +345,18 @@ __device__ __forceinline__ void box_exp(float (&v)[32], int cols, float2 c2, flo
     v[2 * i + 1] = e.y;
   }
 }
+// s = 2^-15 sum e', u = 2^-15 (sum e' t' - 15 sum e')  (e' = e 2^15, t' = t + 15)
+__device__ __forceinline__ float2 tile_sums(float2 s2, float2 u2) {
+  const float s = s2.x + s2.y, u = u2.x + u2.y;
+  constexpr float kInv = 1.f / 32768.f;
+  return make_float2(s * kInv, fmaf(-kExpScaleLog2, s, u) * kInv);
+}
 
-// The exponentials are stored as fp16 scaled by 2^15 (kExpScaleLog2): e <= 1 becomes at most
-// 32768, below fp16's 65504, and fp16's normal range then reaches down to e = 2^-29, so the
-// relative rounding is 2^-11 for every e that can matter.
-constexpr float kExpScale = 32768.f;
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a * kExpScale, b * kExpScale);
+// The exponentials are stored as fp16 scaled by 2^15: e <= 1 becomes at most 32768, below
+// fp16's 65504, and fp16's normal range then reaches down to e = 2^-29, so the relative
+// rounding is 2^-11 for every e that can matter.
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {  // a, b already scaled
+  const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
@@ -570,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m = tile_max(v, p.N - col_base);
         const float st_a = m * p.c;
         // every logit -inf: e = 0 and nothing to add, with a finite shift (no -inf - -inf)
-        const float shift = m == -INFINITY ? 0.f : st_a;
+        const float shift = (m == -INFINITY ? 0.f : st_a) - kExpScaleLog2;
         const float2 c2 = make_float2(p.c, p.c), na2 = make_float2(-shift, -shift);
         float2 s2 = make_float2(0.f, 0.f), u2 = make_float2(0.f, 0.f);
         uint16_t* eb = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row0) * p.ldc;
@@ -584,9 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           write_box_h16(buf, lane, eb + col0, p.ldc, dims.M - row0, p.N - col0);
           __syncwarp();  // every lane has read the box before the next one is staged
         }
-        if (row_ok && col_base < p.N)
-          p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] =
-              make_float4(st_a, s2.x + s2.y, u2.x + u2.y, 0.f);
+        if (row_ok && col_base < p.N) {
+          const float2 su = tile_sums(s2, u2);
+          p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] = make_float4(st_a, su.x, su.y, 0.f);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < BN / 64; ++j) {
