@@ -14,7 +14,7 @@
 //               dlogits in place: |g| p_j = e_j 2^(a - lse log2 e + log2 |g|);
 //   kEpiStore   D is stored (one K split of grad_hidden: M = rows, N = H, K = V);
 //   kEpiAccum   D is added to the fp32 output (grad_weight += dlogits^T h: M = V, N = H,
-//               K = rows).
+//               K = rows) by TMA reduce-adds.
 //
 // Layout and pipeline.  The kernel runs on pairs of CTAs (a cluster of two SMs); a pair
 // computes one 256 x 256 output tile at a time with tcgen05.mma.cta_group::2 (M = 256,
@@ -28,10 +28,13 @@
 // of the finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes of its
 // quarter; two warps share a quarter, one for each half of the columns) while the MMAs of
 // the next tile fill the other accumulator.  Each warp passes its 32 x 32 boxes through a
-// swizzled staging buffer (one row per lane in; out, four fp32 rows of 128 bytes or eight
-// bf16 rows of 64 bytes per instruction), so that its global stores (kEpiLogits, kEpiStore)
-// or vector reduce-adds (kEpiAccum) write whole row segments; stores are fire-and-forget, so
-// many lines per SM are in flight.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
+// swizzled staging buffer (one row per lane in).  kEpiLogits and kEpiStore read them back out
+// as whole row segments (eight 16-bit rows of 64 bytes or four fp32 rows of 128 bytes per
+// instruction) for coalesced global stores, which are fire-and-forget, so many lines per SM
+// are in flight.  kEpiAccum hands each box to a TMA reduce-add (the buffer's swizzle is the
+// tensor map's), one instruction where 16 vector reduce-adds per lane were; the fewer
+// instructions the epilogue warps issue, the less they slow the MMA thread that shares an SM
+// sub-partition with two of them.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
 // grad_hidden) or MN-major (M or N contiguous: W in grad_hidden, dlogits^T and h in
 // grad_weight); the MN-major tiles are loaded as 64-wide boxes and described to the MMA
 // with the MN-major bit.
@@ -141,6 +144,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "[%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+// Add the 32 x 32 fp32 box at shared address `src` to the tensor at box coordinates (x, y);
+// rows and columns outside the tensor are left out.  One bulk group per call.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// No bulk group of this thread still reading shared memory / none still in flight.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's shared-memory writes before the async proxy (TMA) reads them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -268,8 +287,7 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&
 
 // Write a staged 32 x 32 box to rows [0, rows) and columns [0, cols) of the fp32 matrix at
 // `dst` (row stride ld, a multiple of 4): lane l takes 16-byte chunk l % 8 of rows
-// l / 8 + 4 i, so each instruction covers four whole 128-byte rows.  kEpiAccum adds instead.
-template <int EPI>
+// l / 8 + 4 i, so each instruction covers four whole 128-byte rows.
 __device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, int64_t ld, int rows, int cols) {
   const int q = lane & 7;
 #pragma unroll
@@ -282,18 +300,13 @@ __device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, in
     if (r >= rows || 4 * q >= cols) continue;
     float* d = dst + r * ld + 4 * q;
     if (4 * q + 4 <= cols) {
-      if constexpr (EPI == kEpiAccum)
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(d), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
-                     : "memory");
-      else
-        *reinterpret_cast<float4*>(d) = x;
+      *reinterpret_cast<float4*>(d) = x;
     } else {
       const float e[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (4 * q + k >= cols) break;
-        if constexpr (EPI == kEpiAccum) atomicAdd(d + k, e[k]);
-        else d[k] = e[k];
+        d[k] = e[k];
       }
     }
   }
@@ -408,7 +421,8 @@ __device__ __forceinline__ void write_box_h16(uint32_t buf, int lane, uint16_t* 
 // ---------------------------------------------------------------------------
 template <int EPI, bool A_MN, bool B_MN, bool kH>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p,
+                const __grid_constant__ CUtensorMap tmC) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -441,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    if (EPI == kEpiAccum) prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -608,6 +623,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 su = tile_sums(s2, u2);
           p.stats[static_cast<int64_t>(row) * (2 * p.n_tiles) + 2 * u.n + half] = make_float4(st_a, su.x, su.y, 0.f);
         }
+      } else if constexpr (EPI == kEpiAccum) {
+        // each 32 x 32 box staged (128-byte swizzle, the tensor map's) and added to the output
+        // by a TMA reduce-add, so the adds cost one instruction a box; the box's buffer is
+        // restaged only once the previous reduce has read it
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) {
+          if (j >= boxes) break;
+          const int col0 = col_base + 32 * j;
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          stage_row(buf, lane, v[j]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_reduce_add_2d(&tmC, buf, col0, row0);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < BN / 64; ++j) {
@@ -615,13 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int col0 = col_base + 32 * j;
           stage_row(buf, lane, v[j]);
           __syncwarp();
-          write_box<EPI>(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0,
+          write_box(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0,
                          p.N - col0);
           __syncwarp();  // every lane has read the box before the next one is staged
         }
       }
     }
   }
+  if (EPI == kEpiAccum && warp >= 2 && lane == 0) bulk_wait_all();  // the reduce-adds are done
   __syncthreads();
   tc_fence_before();
   cluster_sync();  // neither CTA leaves while the other's copies, MMAs or arrivals may target it
@@ -728,7 +759,21 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params
   if (p.pair_limit > 0 && p.pair_limit < pairs) pairs = p.pair_limit;
   cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (total < pairs ? total : pairs)));
-  return cudaLaunchKernelEx(&cfg, kernel, a, b, p);
+  // kEpiAccum: the output's tensor map, 32 x 32 fp32 boxes with the staging buffer's swizzle
+  CUtensorMap c{};
+  if (EPI == kEpiAccum) {
+    const TensorMapEncodeFn enc = tensor_map_encoder();
+    if (enc == nullptr || p.ldc % 4 != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ldc) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    if (enc(&c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.C, dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, a, b, p, c);
 }
 
 }  // namespace gemm
