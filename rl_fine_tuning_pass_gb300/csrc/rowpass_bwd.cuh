@@ -100,10 +100,12 @@ __device__ __forceinline__ uint4 load_vec(const typename E::storage* in_body, in
 // sum_{j != idx} |g| p_j for the idx element.  Returns this thread's partial sum and
 // whether it wrote the idx element.  The gradient is stored with L2 priority evict_first;
 // LAST_READ loads the logits with evict_first too.
+// With kept_vecs > 0, body vectors [0, kept_vecs) come from `kept` (a copy the caller made in
+// shared memory) instead of global memory.
 template <class E, int THREADS, int UNROLL, bool SAME_PHASE, bool NEG, bool LAST_READ = false>
 __device__ __forceinline__ float stream_span(const typename E::storage* in, typename E::storage* out,
                                              const RowSplit& sp, const Span& sn, int idx, float c, float nK,
-                                             bool& owner) {
+                                             bool& owner, const uint4* kept = nullptr, int kept_vecs = 0) {
   constexpr int VEC = E::kVec;
   using S = typename E::storage;
   const int tid = threadIdx.x;
@@ -150,11 +152,14 @@ __device__ __forceinline__ float stream_span(const typename E::storage* in, type
   for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {
     uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = load_vec<E, SAME_PHASE, LAST_READ>(in_body, i + k * THREADS);
+    for (int k = 0; k < UNROLL; ++k) {
+      const int j = i + k * THREADS;
+      v[k] = j < kept_vecs ? kept[j] : load_vec<E, SAME_PHASE, LAST_READ>(in_body, j);
+    }
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
   }
-  for (; i < sn.v1; i += THREADS) process(load_vec<E, SAME_PHASE, LAST_READ>(in_body, i), i);
+  for (; i < sn.v1; i += THREADS) process(i < kept_vecs ? kept[i] : load_vec<E, SAME_PHASE, LAST_READ>(in_body, i), i);
   return q_acc + (q2.x + q2.y);
 }
 

@@ -14,8 +14,12 @@
 namespace grpo {
 namespace {
 
+// keep_vecs > 0 (rows whose logits and dlogits share their phase): the first keep_vecs 16-byte
+// vectors of the row's body are kept in (dynamic) shared memory by the first sweep and read
+// back from there by the second, so only the rest of the row has to stay in L2 between them.
 template <class E, int THREADS, int UNROLL, bool kH, bool SAME_PHASE>
-__global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
+__global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int keep_vecs) {
+  extern __shared__ uint4 fused_kept[];
   wait_for_previous_grids();
   constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
   constexpr int VEC = E::kVec;
@@ -54,17 +58,33 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   // any other row is kept (evict_last) for the second sweep, which lets it go.
   // Coherent loads: dlogits may alias the logits.
   const bool kept = A_pre != 0.f;
+  // the shared-memory copy: only for a row that is swept again (its first kv vectors are then
+  // loaded evict_first, as their last read from L2)
+  const int kv = (SAME_PHASE && kept) ? min(keep_vecs, sp.nvec) : 0;
   auto sweep1 = [&](auto load) {
     int i = tid;
     for (; i + (UNROLL - 1) * THREADS < sp.nvec; i += UNROLL * THREADS) {
       uint4 v[UNROLL];
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) v[k] = load(vb + i + k * THREADS);
+      for (int k = 0; k < UNROLL; ++k) {
+        const int j = i + k * THREADS;
+        if (j < kv) {
+          v[k] = ld_v4_evict_first(vb + j);
+          fused_kept[j] = v[k];
+        } else {
+          v[k] = load(vb + j);
+        }
+      }
       run_vectors<E, kH>(rs, v, c);
     }
     for (; i < sp.nvec; i += THREADS) {
       uint4 v[1];
-      v[0] = load(vb + i);
+      if (i < kv) {
+        v[0] = ld_v4_evict_first(vb + i);
+        fused_kept[i] = v[0];
+      } else {
+        v[0] = load(vb + i);
+      }
       run_vectors<E, kH>(rs, v, c);
     }
   };
@@ -107,17 +127,31 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q) {
   bool owner = false;
   const float nK = sh_nK;
   const float q_part =
-      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true, true>(row, out, osp, osn, gidx, c, nK, owner)
-              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false, true>(row, out, osp, osn, gidx, c, nK, owner);
+      g > 0.f ? stream_span<E, THREADS, UNROLL, SAME_PHASE, true, true>(row, out, osp, osn, gidx, c, nK, owner,
+                                                                         fused_kept, kv)
+              : stream_span<E, THREADS, UNROLL, SAME_PHASE, false, true>(row, out, osp, osn, gidx, c, nK, owner,
+                                                                          fused_kept, kv);
   const float q_total = block_sum_all<THREADS>(q_part);
   if (owner) E::store_scalar(out + gidx, g > 0.f ? q_total : -q_total);
 }
 
+// Shared memory a 512-thread CTA keeps of its row: two such CTAs fit on an SM, and the rest of
+// the ~300 rows in flight (at V = 151936, 193 KB each) then fits in L2.
+constexpr int kFusedKeepBytes = 104 * 1024;
+
 template <class E, int THREADS, int U, bool kH>
 cudaError_t launch_fused_h(const FusedParams& q, int64_t rows, bool same_phase, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(rows));
-  return same_phase ? launch_after_previous(fused_kernel<E, THREADS, U, kH, true>, grid, dim3(THREADS), s, q)
-                    : launch_after_previous(fused_kernel<E, THREADS, U, kH, false>, grid, dim3(THREADS), s, q);
+  if (!same_phase) return launch_after_previous(fused_kernel<E, THREADS, U, kH, false>, grid, dim3(THREADS), s, q, 0);
+  int keep = 0;
+  if (THREADS == 512) {  // rows of 128 KB and more
+    keep = kFusedKeepBytes / 16;
+    const cudaError_t e = cudaFuncSetAttribute(fused_kernel<E, THREADS, U, kH, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedKeepBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_after_previous_smem(fused_kernel<E, THREADS, U, kH, true>, grid, dim3(THREADS),
+                                    static_cast<size_t>(keep) * 16, s, q, keep);
 }
 
 template <class E, int THREADS, int U>
