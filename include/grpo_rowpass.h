@@ -76,8 +76,10 @@ typedef enum { GRPO_FP32 = 0, GRPO_BF16 = 1 } grpo_dtype;
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define GRPO_DEVERR_IDX_OUT_OF_RANGE 1
-/* A tensor-core GEMM of grpo_fused_linear(_noalloc) gave up waiting for its own copies or
- * MMAs (about 2 s): its outputs are not valid.  It returns without trapping, TMEM freed. */
+/* A kernel gave up waiting for its own asynchronous copies (about 2 s): a tensor-core GEMM of
+ * grpo_fused_linear(_noalloc) (copies or MMAs), or a row of grpo_loss_fused (the bulk copy of
+ * the part of the row kept in shared memory).  Those outputs are not valid.  The kernel
+ * returns without trapping (the GEMM with its TMEM freed). */
 #define GRPO_DEVERR_TIMEOUT 2
 
 /* A [B, L, V] logits (or dlogits) tensor: ptr + b*stride_b + l*stride_l + j. */

@@ -148,18 +148,21 @@ __device__ __forceinline__ float stream_span(const typename E::storage* in, type
     st_v4_evict_first(ob + i, E::template pack_pairs<NEG>(e));
   };
 
-  int i = sn.v0 + tid;
-  for (; i + (UNROLL - 1) * THREADS < sn.v1; i += UNROLL * THREADS) {
-    uint4 v[UNROLL];
+  // the part read from global memory first (L2, while it is still there), then the part kept in
+  // shared memory
+  auto sweep = [&](auto load, int i, int n) {
+    for (; i + (UNROLL - 1) * THREADS < n; i += UNROLL * THREADS) {
+      uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const int j = i + k * THREADS;
-      v[k] = j < kept_vecs ? kept[j] : load_vec<E, SAME_PHASE, LAST_READ>(in_body, j);
+      for (int k = 0; k < UNROLL; ++k) v[k] = load(i + k * THREADS);
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
     }
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) process(v[k], i + k * THREADS);
-  }
-  for (; i < sn.v1; i += THREADS) process(i < kept_vecs ? kept[i] : load_vec<E, SAME_PHASE, LAST_READ>(in_body, i), i);
+    for (; i < n; i += THREADS) process(load(i), i);
+  };
+  const int g0 = sn.v0 > kept_vecs ? sn.v0 : kept_vecs;
+  sweep([&](int j) { return load_vec<E, SAME_PHASE, LAST_READ>(in_body, j); }, g0 + tid, sn.v1);
+  if (kept_vecs > sn.v0) sweep([&](int j) { return kept[j]; }, sn.v0 + tid, kept_vecs < sn.v1 ? kept_vecs : sn.v1);
   return q_acc + (q2.x + q2.y);
 }
 

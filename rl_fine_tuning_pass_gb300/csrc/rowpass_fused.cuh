@@ -14,21 +14,64 @@
 namespace grpo {
 namespace {
 
+// The kept part of a row comes into shared memory by 1-D bulk copies (TMA) that thread 0
+// issues: `bytes` (a multiple of 16) from the 16-byte aligned `src`, in pieces of 16 KB, each
+// counted on the CTA's mbarrier `bar` (initialised here for one arrival with the byte count).
+// These bytes are not needed in L2 again, so the copies read them with priority evict_first.
+__device__ __forceinline__ void kept_copy_issue(uint32_t bar, uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  const char* s = static_cast<const char*>(src);
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  for (uint32_t off = 0; off < bytes; off += 16384u) {
+    const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst + off),
+        "l"(s + off), "r"(n), "r"(bar), "l"(pol)
+        : "memory");
+  }
+}
+// Wait for the kept part to land: false after about two seconds (4e9 cycles) without it.
+__device__ __forceinline__ bool kept_copy_wait(uint32_t bar) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(bar)
+        : "memory");
+    if (done != 0) return true;
+    if (clock64() - t0 > 4000000000LL) return false;
+  }
+}
+
 // keep_vecs > 0 (rows whose logits and dlogits share their phase): the first keep_vecs 16-byte
-// vectors of the row's body are kept in (dynamic) shared memory by the first sweep and read
-// back from there by the second, so only the rest of the row has to stay in L2 between them.
+// vectors of the row's body are copied into (dynamic) shared memory by bulk copies issued
+// before the first sweep, which streams the rest of the row meanwhile and then takes the kept
+// part from shared memory; the second sweep reads it back from there too (after the rest, which
+// it takes from L2 first, while it is still there), so only the rest of the row has to stay in
+// L2 between the sweeps.
 template <class E, int THREADS, int UNROLL, bool kH, bool SAME_PHASE>
 __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int keep_vecs) {
   extern __shared__ uint4 fused_kept[];
+  __shared__ __align__(8) uint64_t kept_bar;
   wait_for_previous_grids();
   constexpr int MODE = kH ? kFwdGrpoH : kFwdGrpo;
   constexpr int VEC = E::kVec;
   using S = typename E::storage;
   const FwdParams& p = q.f;
 
-  const int64_t r = blockIdx.x;
-  const int64_t b = r / p.x.L;
-  const int64_t l = r - b * p.x.L;
+  // CTAs in launch order take token l of every sequence in turn (the grid has one CTA per row),
+  // so the rows in flight at any time come from all the sequences, masked and unmasked mixed
+  const int64_t nseq = gridDim.x / p.x.L;
+  const int64_t b = blockIdx.x % nseq;
+  const int64_t l = blockIdx.x / nseq;
+  const int64_t r = b * p.x.L + l;
   const int tid = threadIdx.x;
   const int V = p.x.V;
   const float c = p.c;
@@ -58,38 +101,45 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   // any other row is kept (evict_last) for the second sweep, which lets it go.
   // Coherent loads: dlogits may alias the logits.
   const bool kept = A_pre != 0.f;
-  // the shared-memory copy: only for a row that is swept again (its first kv vectors are then
-  // loaded evict_first, as their last read from L2)
+  // the shared-memory copy: only for a row that is swept again
   const int kv = (SAME_PHASE && kept) ? min(keep_vecs, sp.nvec) : 0;
-  auto sweep1 = [&](auto load) {
-    int i = tid;
-    for (; i + (UNROLL - 1) * THREADS < sp.nvec; i += UNROLL * THREADS) {
+  const uint32_t bar = smem_addr(&kept_bar);
+  if (kv > 0) {
+    if (tid == 0) kept_copy_issue(bar, smem_addr(fused_kept), vb, static_cast<uint32_t>(kv) * 16u);
+    __syncthreads();  // the mbarrier is initialised before anyone waits on it
+  }
+  // a row swept again: while the CTA loads one step of UNROLL x THREADS vectors, thread 0 asks
+  // L2 for the next step (a bulk prefetch, evict_last), one step ahead and no more
+  uint64_t pf_pol = 0;
+  if (tid == 0) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pf_pol));
+  auto sweep1 = [&](auto load, const uint4* src, int i, int n, bool prefetch) {
+    constexpr int kStep = UNROLL * THREADS;
+    for (; i + (UNROLL - 1) * THREADS < n; i += kStep) {
+      if (prefetch && tid == 0 && i + kStep < n) {
+        const int e = i + 2 * kStep < n ? i + 2 * kStep : n;
+        asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src + i + kStep),
+                     "r"(static_cast<uint32_t>(e - i - kStep) * 16u), "l"(pf_pol)
+                     : "memory");
+      }
       uint4 v[UNROLL];
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const int j = i + k * THREADS;
-        if (j < kv) {
-          v[k] = ld_v4_evict_first(vb + j);
-          fused_kept[j] = v[k];
-        } else {
-          v[k] = load(vb + j);
-        }
-      }
+      for (int k = 0; k < UNROLL; ++k) v[k] = load(src + i + k * THREADS);
       run_vectors<E, kH>(rs, v, c);
     }
-    for (; i < sp.nvec; i += THREADS) {
-      uint4 v[1];
-      if (i < kv) {
-        v[0] = ld_v4_evict_first(vb + i);
-        fused_kept[i] = v[0];
-      } else {
-        v[0] = load(vb + i);
-      }
+    for (; i < n; i += THREADS) {
+      uint4 v[1] = {load(src + i)};
       run_vectors<E, kH>(rs, v, c);
     }
   };
-  if (kept) sweep1([](const uint4* q) { return ld_v4_evict_last(q); });
-  else sweep1([](const uint4* q) { return ld_v4_evict_first(q); });
+  if (kept) sweep1([](const uint4* a) { return ld_v4_evict_last(a); }, vb, kv + tid, sp.nvec, true);
+  else sweep1([](const uint4* a) { return ld_v4_evict_first(a); }, vb, tid, sp.nvec, false);
+  if (kv > 0) {
+    if (!kept_copy_wait(bar)) {  // the row's outputs are not valid; wait once more for the copies in flight
+      if (tid == 0 && p.dev_err != nullptr) atomicOr(p.dev_err, GRPO_DEVERR_TIMEOUT_BIT);
+      kept_copy_wait(bar);
+    }
+    sweep1([](const uint4* a) { return *a; }, fused_kept, tid, kv, false);
+  }
   // the selected logit, loaded after the stream so that no dependent load delays it
   const float x_idx = tid == 0 ? E::load_scalar_coherent(row + idx) : 0.f;
   Stat mine;

@@ -47,7 +47,7 @@ inline cudaError_t launch_after_previous_smem(void (*kernel)(KArgs...), dim3 gri
 
 // Error bit OR-ed into the caller's device error word (GRPO_DEVERR_IDX_OUT_OF_RANGE).
 constexpr int GRPO_DEVERR_IDX_OUT_OF_RANGE_BIT = 1;
-// A tensor-core GEMM's bounded wait ran out (GRPO_DEVERR_TIMEOUT).
+// A bounded wait on the kernel's own asynchronous copies ran out (GRPO_DEVERR_TIMEOUT).
 constexpr int GRPO_DEVERR_TIMEOUT_BIT = 2;
 
 // 16-byte loads in flight per thread: single-warp CTAs keep more of them so that a
