@@ -50,6 +50,34 @@ __device__ __forceinline__ bool kept_copy_wait(uint32_t bar) {
   }
 }
 
+// A row of +0.0 written by bulk copies (TMA) from a zeroed 16 KB block `buf` of shared memory
+// (evict_first); the scalar head and tail by plain stores.  Thread 0 waits until the copies
+// have read the block, so the CTA may exit or reuse it afterwards.
+template <class E, int THREADS>
+__device__ __forceinline__ void zero_row_bulk(typename E::storage* out, const RowSplit& sp, uint4* buf) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 1024; i += THREADS) buf[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid < sp.head) E::store_bits(out + tid, 0u);
+  if (tid < sp.tail) E::store_bits(out + sp.head + sp.nvec * E::kVec + tid, 0u);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (tid == 0) {
+    char* dst = reinterpret_cast<char*>(out + sp.head);
+    const uint32_t src = smem_addr(buf);
+    const uint32_t bytes = static_cast<uint32_t>(sp.nvec) * 16u;
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    for (uint32_t off = 0; off < bytes; off += 16384u) {
+      const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst + off),
+                   "r"(src), "r"(n), "l"(pol)
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+}
+
 // keep_vecs > 0 (rows whose logits and dlogits share their phase): the first keep_vecs 16-byte
 // vectors of the row's body are copied into (dynamic) shared memory by bulk copies issued
 // before the first sweep, which streams the rest of the row meanwhile and then takes the kept
@@ -83,7 +111,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   const float A_pre = p.beta == 0.f ? p.adv[b] : 1.f;
   if (p.mask != nullptr && p.mask[r] == 0) {  // masked token: zero outputs, zero gradient row
     if (tid == 0) masked_row_outputs(p, r);
-    fill_span<E, THREADS>(out, osp, osn, 0u);
+    if (SAME_PHASE && keep_vecs >= 1024) zero_row_bulk<E, THREADS>(out, osp, fused_kept);
+    else fill_span<E, THREADS>(out, osp, osn, 0u);
     return;
   }
 
@@ -162,7 +191,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   __syncthreads();
   const float g = sh_g;
   if (g == 0.f) {  // early-out: +0.0 over the row
-    fill_span<E, THREADS>(out, osp, osn, 0u);
+    if (SAME_PHASE && keep_vecs >= 1024) zero_row_bulk<E, THREADS>(out, osp, fused_kept);
+    else fill_span<E, THREADS>(out, osp, osn, 0u);
     if (kept) l2_demote<THREADS>(row, static_cast<int64_t>(V) * sizeof(S));
     return;
   }
