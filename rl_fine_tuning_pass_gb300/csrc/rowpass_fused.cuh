@@ -116,6 +116,16 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
     return;
   }
 
+  // the row's scalars for thread 0's epilogue, loaded now so that their latency is hidden
+  // behind the stream
+  RowScalars pre{0.f, 0.f, 0.f};
+  float pre_dloss = 0.f;
+  if (tid == 0) {
+    if (p.old_logp) pre.old = p.old_logp[r];
+    if (p.beta != 0.f) pre.ref = p.ref_logp[r];
+    pre.A = p.adv[b];
+    pre_dloss = q.dloss[r];
+  }
   const S* row = static_cast<const S*>(p.x.ptr) + b * p.x.sb + l * p.x.sl;
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
@@ -162,6 +172,9 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   };
   if (kept) sweep1([](const uint4* a) { return ld_v4_evict_last(a); }, vb, kv + tid, sp.nvec, true);
   else sweep1([](const uint4* a) { return ld_v4_evict_first(a); }, vb, tid, sp.nvec, false);
+  // the selected logit, loaded after the stream from global memory so that no dependent load
+  // delays it, and before the kept part is processed, which hides its latency
+  const float x_idx = tid == 0 ? E::load_scalar_coherent(row + idx) : 0.f;
   if (kv > 0) {
     if (!kept_copy_wait(bar)) {  // the row's outputs are not valid; wait once more for the copies in flight
       if (tid == 0 && p.dev_err != nullptr) atomicOr(p.dev_err, GRPO_DEVERR_TIMEOUT_BIT);
@@ -169,8 +182,6 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
     }
     sweep1([](const uint4* a) { return *a; }, fused_kept, tid, kv, false);
   }
-  // the selected logit, loaded after the stream so that no dependent load delays it
-  const float x_idx = tid == 0 ? E::load_scalar_coherent(row + idx) : 0.f;
   Stat mine;
   mine.a = rs.a;
   mine.s = rs.s.x + rs.s.y;
@@ -182,8 +193,9 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   __shared__ int sh_idx;
   if (tid == 0) {
     float logp = 0.f, lse = 0.f;
-    row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx, &logp, &lse);
-    const float g = grpo_factor(logp, p.old_logp, p.ref_logp, p.adv[b], q.dloss[r], p.beta, p.lo, p.hi, q.T, r);
+    row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx, &logp, &lse, &pre);
+    const float g = grpo_factor_of(logp, p.old_logp ? pre.old : logp, p.old_logp != nullptr, pre.ref, pre.A,
+                                   pre_dloss, p.beta, p.lo, p.hi, q.T);
     sh_g = g;
     sh_nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
     sh_idx = bad_idx ? -1 : idx;

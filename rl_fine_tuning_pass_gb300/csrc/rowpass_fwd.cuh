@@ -99,12 +99,17 @@ __device__ __forceinline__ void stream_vectors(Running& rs, const uint4* vb, int
   }
 }
 
+// A row's old_logp, ref_logp (0 when beta == 0) and advantage, loaded in advance.
+struct RowScalars {
+  float old, ref, A;
+};
+
 // Outputs of one row from its merged statistic (thread 0); returns logp and lse through
-// the optional pointers.
+// the optional pointers.  `pre` (optional): the row's scalars, already loaded.
 template <int MODE>
 __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int64_t b, const Stat& st, float c,
                                              float x_idx, bool bad_idx, float* logp_out = nullptr,
-                                             float* lse_out = nullptr) {
+                                             float* lse_out = nullptr, const RowScalars* pre = nullptr) {
   constexpr bool kH = MODE == kFwdEntropy || MODE == kFwdGrpoH;
   constexpr bool kGrpo = MODE == kFwdGrpo || MODE == kFwdGrpoH;
   const float ln_s = logf(st.s);
@@ -125,8 +130,8 @@ __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int6
   if (lse_out) *lse_out = lse;
   if (!kGrpo) return;
 
-  const float ratio = p.old_logp ? expf(logp - p.old_logp[r]) : 1.f;
-  const float A = p.adv[b];
+  const float ratio = p.old_logp ? expf(logp - (pre ? pre->old : p.old_logp[r])) : 1.f;
+  const float A = pre ? pre->A : p.adv[b];
   // clip(ratio, lo, hi) written with comparisons so that a NaN ratio stays NaN
   const float clipped = ratio < p.lo ? p.lo : (ratio > p.hi ? p.hi : ratio);
   const float obj = ratio * A, obj_clipped = clipped * A;
@@ -134,7 +139,7 @@ __device__ __forceinline__ void row_epilogue(const FwdParams& p, int64_t r, int6
   const float pg = is_clipped ? -obj_clipped : -obj;
   float kl = 0.f;
   if (p.beta != 0.f) {
-    const float d = p.ref_logp[r] - logp;
+    const float d = (pre ? pre->ref : p.ref_logp[r]) - logp;
     kl = p.beta * (expm1f(d) - d);  // beta (e^d - d - 1), no cancellation for small d
   }
   if (bad_idx) kl = __int_as_float(0x7FC00000);
