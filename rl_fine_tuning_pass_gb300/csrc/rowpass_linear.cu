@@ -50,7 +50,7 @@ constexpr int kLinearThreads = 512;
 __device__ __forceinline__ float2 unpack_h2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
-template <int THREADS, bool NEG>
+template <int THREADS, int UNROLL, bool NEG>
 __device__ __forceinline__ float linear_sweep_e(uint16_t* row, const float4* __restrict__ st_row, int V, int idx,
                                                 float nK, bool& owner) {
   constexpr float kUnscale = -15.f;  // log2 of the exponentials' 2^-15 scale
@@ -59,9 +59,8 @@ __device__ __forceinline__ float linear_sweep_e(uint16_t* row, const float4* __r
   float q_acc = 0.f;
   float2 q2 = make_float2(0.f, 0.f);
   const int groups = V / 8;  // 8 exponentials (one 16-byte vector) -> 8 dlogits, in place
-  for (int i = tid; i < groups; i += THREADS) {
-    const uint4 w = vb[i];
-    const float sc = ex2(st_row[i >> 4].x + (nK + kUnscale));  // 16 vectors per 128-column part
+  auto process = [&](const uint4& w, float a, int i) {
+    const float sc = ex2(a + (nK + kUnscale));
     const float2 s2 = make_float2(sc, sc);
     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
     float2 e[BF16::kPairs];
@@ -80,7 +79,28 @@ __device__ __forceinline__ float linear_sweep_e(uint16_t* row, const float4* __r
       for (int q = 0; q < BF16::kPairs; ++q) q2 = __fadd2_rn(q2, e[q]);
     }
     vb[i] = BF16::template pack_pairs<NEG>(e);
+  };
+  // UNROLL vectors a thread (and their parts' offsets) loaded before any is written back;
+  // meanwhile thread 0 asks L2 for the CTA's next step (a bulk prefetch), one step ahead
+  constexpr int kStep = UNROLL * THREADS;
+  int i = tid;
+  for (; i + (UNROLL - 1) * THREADS < groups; i += kStep) {
+    if (tid == 0 && i + kStep < groups) {
+      const int e = i + 2 * kStep < groups ? i + 2 * kStep : groups;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vb + i + kStep),
+                   "r"(static_cast<uint32_t>(e - i - kStep) * 16u)
+                   : "memory");
+    }
+    uint4 w[UNROLL];
+    float a[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) w[k] = vb[i + k * THREADS];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) a[k] = st_row[(i + k * THREADS) >> 4].x;  // 16 vectors a 128-column part
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) process(w[k], a[k], i + k * THREADS);
   }
+  for (; i < groups; i += THREADS) process(vb[i], st_row[i >> 4].x, i);
   const int j = 8 * groups + tid;  // the last V % 8 elements
   if (j < V) {
     const __half hj = *reinterpret_cast<const __half*>(row + j);
@@ -145,6 +165,15 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   const float c = p.c;
 
   const int64_t id64 = p.idx[r];
+  // the row's scalars for thread 0's epilogue, loaded now so that their latency is hidden
+  RowScalars pre{0.f, 0.f, 0.f};
+  float pre_dloss = 0.f;
+  if (tid == 0) {
+    if (p.old_logp) pre.old = p.old_logp[r];
+    if (p.beta != 0.f) pre.ref = p.ref_logp[r];
+    pre.A = p.adv[b];
+    pre_dloss = q.dloss[r];
+  }
   const bool bad_idx = id64 < 0 || id64 >= V;
   const int idx = bad_idx ? 0 : static_cast<int>(id64);
   // the selected logit, from the row's hidden state and the head weight (warp 0), while the
@@ -165,8 +194,9 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   __shared__ float sh_g, sh_nK;
   if (tid == 0) {
     float logp = 0.f, lse = 0.f;
-    row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx, &logp, &lse);
-    const float g = grpo_factor(logp, p.old_logp, p.ref_logp, p.adv[b], q.dloss[r], p.beta, p.lo, p.hi, q.T, r);
+    row_epilogue<MODE>(p, r, b, st, c, x_idx, bad_idx, &logp, &lse, &pre);
+    const float g = grpo_factor_of(logp, p.old_logp ? pre.old : logp, p.old_logp != nullptr, pre.ref, pre.A,
+                                   pre_dloss, p.beta, p.lo, p.hi, q.T);
     sh_g = g;
     sh_nK = fmaf(-lse, kLog2e, log2f(fabsf(g)));  // -(lse*log2e - log2|g|)
   }
@@ -183,8 +213,8 @@ __global__ void __launch_bounds__(THREADS) linear_rows_kernel(const LinearChunkP
   // the sweep: d_j = -sign(g) |g| p_j in bf16, and g (1 - p_idx) at idx
   bool owner = false;
   const float nK = sh_nK;
-  const float q_part = g > 0.f ? linear_sweep_e<THREADS, true>(out, st_row, V, idx, nK, owner)
-                               : linear_sweep_e<THREADS, false>(out, st_row, V, idx, nK, owner);
+  const float q_part = g > 0.f ? linear_sweep_e<THREADS, UNROLL, true>(out, st_row, V, idx, nK, owner)
+                               : linear_sweep_e<THREADS, UNROLL, false>(out, st_row, V, idx, nK, owner);
   const float q_total = block_sum_all<THREADS>(q_part);
   if (owner) BF16::store_scalar(out + idx, g > 0.f ? q_total : -q_total);
 }
