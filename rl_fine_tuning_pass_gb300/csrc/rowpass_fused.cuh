@@ -94,11 +94,12 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   using S = typename E::storage;
   const FwdParams& p = q.f;
 
-  // CTAs in launch order take token l of every sequence in turn (the grid has one CTA per row),
-  // so the rows in flight at any time come from all the sequences, masked and unmasked mixed
+  // Long rows (512-thread CTAs, several waves of them): CTAs in launch order take token l of
+  // every sequence in turn (the grid has one CTA per row), so the rows in flight at any time come
+  // from all the sequences, masked and unmasked mixed.  Shorter rows go in row order.
   const int64_t nseq = gridDim.x / p.x.L;
-  const int64_t b = blockIdx.x % nseq;
-  const int64_t l = blockIdx.x / nseq;
+  const int64_t b = THREADS == 512 ? blockIdx.x % nseq : blockIdx.x / p.x.L;
+  const int64_t l = THREADS == 512 ? blockIdx.x / nseq : blockIdx.x % p.x.L;
   const int64_t r = b * p.x.L + l;
   const int tid = threadIdx.x;
   const int V = p.x.V;
@@ -147,8 +148,8 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
     if (tid == 0) kept_copy_issue(bar, smem_addr(fused_kept), vb, static_cast<uint32_t>(kv) * 16u);
     __syncthreads();  // the mbarrier is initialised before anyone waits on it
   }
-  // a row swept again: while the CTA loads one step of UNROLL x THREADS vectors, thread 0 asks
-  // L2 for the next step (a bulk prefetch, evict_last), one step ahead and no more
+  // a long row swept again: while the CTA loads one step of UNROLL x THREADS vectors, thread 0
+  // asks L2 for the next step (a bulk prefetch, evict_last), one step ahead and no more
   uint64_t pf_pol = 0;
   if (tid == 0) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pf_pol));
   auto sweep1 = [&](auto load, const uint4* src, int i, int n, bool prefetch) {
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
       run_vectors<E, kH>(rs, v, c);
     }
   };
-  if (kept) sweep1([](const uint4* a) { return ld_v4_evict_last(a); }, vb, kv + tid, sp.nvec, true);
+  if (kept) sweep1([](const uint4* a) { return ld_v4_evict_last(a); }, vb, kv + tid, sp.nvec, THREADS == 512);
   else sweep1([](const uint4* a) { return ld_v4_evict_first(a); }, vb, tid, sp.nvec, false);
   // the selected logit, loaded after the stream from global memory so that no dependent load
   // delays it, and before the kept part is processed, which hides its latency
