@@ -196,6 +196,41 @@ def test_row_pass_entry_points_write_only_their_outputs(dtype, V, head):
     sdl.check(f"slsm bwd V={V}")
 
 
+@pytest.mark.parametrize("V", [65541, 151936])
+@pytest.mark.parametrize("head", HEADS)
+@pytest.mark.parametrize("beta", [0.0, 0.05])
+def test_fused_same_phase_rows_write_only_their_rows(V, head, beta):
+    """grpo_loss_fused with the dlogits rows in the logits' own layout (row stride V + 3, so
+    the rows start at varying 16-byte phases): the long-row launch, which holds the first
+    104 KB of each row in shared memory, prefetches the rest into L2 and writes masked and
+    zero rows (beta = 0, zero advantage) by bulk stores from shared memory.  Out of place,
+    then in place."""
+    lib = rp.load_library()
+    B, L = 2, 5
+    R = B * L
+    s = torch.cuda.current_stream().cuda_stream
+    x, idx, adv, mask, dloss, noise = _inputs(B, L, V, torch.bfloat16, head, V * 17 + head)
+    xd = rp.rows_of(x.t)
+    T, el, eh = 0.9, 0.2, 0.28
+    logp, lse = Banded(R, torch.float32), Banded(R, torch.float32)
+    _ok(lib.selective_log_softmax_fwd(ctypes.byref(xd), _p(idx), T, logp.ptr, lse.ptr, None, s), "slsm fwd")
+    old = (logp.t + 0.2 * noise).contiguous()
+    ref = (logp.t - 0.1 * noise).contiguous()
+    for in_place in (False, True):
+        fo = {k: Banded(R, torch.float32) for k in ("loss", "logp", "lse", "kl", "entropy")}
+        fo["is_clipped"] = Banded(R, torch.uint8)
+        fdl = x if in_place else BandedRows(B, L, V, torch.bfloat16, head, gap=3)
+        fdld = rp.rows_of(fdl.t)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        _ok(lib.grpo_loss_fused(ctypes.byref(xd), _p(idx), _p(old), _p(ref), _p(adv), _p(mask), _p(dloss), T,
+                                beta, el, eh, fo["loss"].ptr, fo["logp"].ptr, fo["lse"].ptr, fo["kl"].ptr,
+                                fo["is_clipped"].ptr, fo["entropy"].ptr, ctypes.byref(fdld), _p(err), s), "fused")
+        for k, b in fo.items():
+            b.check(f"fused {k} in_place={in_place}")
+        fdl.check(f"fused dlogits V={V} in_place={in_place}")
+        assert int(err.item()) == 0
+
+
 @pytest.mark.parametrize("V", VS)
 @pytest.mark.parametrize("head", HEADS)
 def test_vocab_shard_entry_points_write_only_their_outputs(V, head):

@@ -511,14 +511,21 @@ def test_fused_pages_workload_every_row_and_matches_separate():
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
-@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000, 151936])
+@pytest.mark.parametrize("V", [1, 9, 513, 4097, 40000, 65541, 151936])
 @pytest.mark.parametrize("offset,extra", [(0, 0), (3, 1)])
-def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
+@pytest.mark.parametrize("beta", [0.0, 0.05])
+def test_fused_edge_shapes_every_row(dtype, V, offset, extra, beta):
+    """Every row against the oracle twice: with dlogits rows out of phase with the logits
+    (scalar-load variant), and with dlogits rows in the logits' own layout, where a long
+    row's first 104 KB are held in shared memory between the sweeps and masked or zero rows
+    are written by bulk stores; rows start at varying 16-byte phases when extra is odd.
+    In place equals the same layout bit for bit."""
     B, L = 2, 5
     R = B * L
-    seed = V * 7 + offset
+    seed = V * 7 + offset + int(beta * 100)
     x, idx, adv, mask, dloss = edge_inputs(B, L, V, dtype, offset, extra, seed)
-    T, beta, el, eh = f32(0.8), f32(0.05), f32(0.2), f32(0.28)
+    T, el, eh = f32(0.8), f32(0.2), f32(0.28)
+    beta = f32(beta)
     xo = rows_f64(select_rows(x, np.arange(R)))
     lp, _ = oracle.selective_log_softmax(xo, idx.cpu().numpy(), T)
     g = torch.Generator().manual_seed(V)
@@ -532,7 +539,9 @@ def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
     compare_grpo_rows(inp, f, dl, np.arange(R), old, ref, T, beta, el, eh, f"fused edge V={V}")
     x2, _ = strided_logits(B, L, V, dtype, offset, extra, seed)
     same_layout, _ = strided_logits(B, L, V, dtype, offset, extra, seed + 99)
-    _, dl_same, _ = run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=same_layout)
+    f_same, dl_same, err_same = run_gpu_fused(inp, old, ref, T, beta, el, eh, dlogits=same_layout)
+    assert err_same == 0
+    compare_grpo_rows(inp, f_same, dl_same, np.arange(R), old, ref, T, beta, el, eh, f"fused edge V={V} same phase")
     inp2 = W.Inputs(inp.spec, x2, idx, adv, mask, dloss, None, None, None, None)
     _, dl2, err2 = run_gpu_fused(inp2, old, ref, T, beta, el, eh, dlogits=x2)   # in place
     assert err2 == 0 and dl2.data_ptr() == x2.data_ptr()
@@ -543,8 +552,9 @@ def test_fused_edge_shapes_every_row(dtype, V, offset, extra):
 @pytest.mark.parametrize("V", [65536, 100000, 151936, 158216])
 @pytest.mark.parametrize("beta", [0.0, 0.05])
 def test_fused_long_aligned_rows_every_row(V, beta):
-    """Long bf16 rows with 16-byte aligned starts (the 512-thread fused kernel, which keeps
-    the row in L2 between its two sweeps): every row against the oracle, including a row
+    """Long bf16 rows with 16-byte aligned starts (the 512-thread fused kernel, which holds
+    the first 104 KB of each row in shared memory and the rest in L2 between its two sweeps):
+    every row against the oracle, including a row
     with -inf logits, a peaked row (p_idx near 1), masked and zero-advantage rows; in place
     equal bit for bit to out of place."""
     B, L = 2, 5
