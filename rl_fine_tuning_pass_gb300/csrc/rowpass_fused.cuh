@@ -94,12 +94,19 @@ __global__ void __launch_bounds__(THREADS) fused_kernel(const FusedParams q, int
   using S = typename E::storage;
   const FwdParams& p = q.f;
 
-  // Long rows (512-thread CTAs, several waves of them): CTAs in launch order take token l of
-  // every sequence in turn (the grid has one CTA per row), so the rows in flight at any time come
-  // from all the sequences, masked and unmasked mixed.  Shorter rows go in row order.
+  // Long rows (512-thread CTAs, several waves of them): CTAs in launch order take the j-th token
+  // position of every sequence in turn (the grid has one CTA per row), so the rows in flight at
+  // any time come from all the sequences.  With a mask, whose masked rows sit at the ends of the
+  // sequences, the positions are taken alternately from the start and the end (l = j / 2, then
+  // L - 1 - j / 2), so that masked (write-only) and unmasked rows stay mixed over the launch.
+  // Shorter rows go in row order.
   const int64_t nseq = gridDim.x / p.x.L;
+  const int64_t j = blockIdx.x / nseq;
   const int64_t b = THREADS == 512 ? blockIdx.x % nseq : blockIdx.x / p.x.L;
-  const int64_t l = THREADS == 512 ? blockIdx.x / nseq : blockIdx.x % p.x.L;
+  const int64_t l = THREADS != 512      ? blockIdx.x % p.x.L
+                    : p.mask == nullptr ? j
+                    : (j & 1)           ? p.x.L - 1 - (j >> 1)
+                                        : (j >> 1);
   const int64_t r = b * p.x.L + l;
   const int tid = threadIdx.x;
   const int V = p.x.V;
