@@ -12,7 +12,9 @@ One step = one pass of the whole hot path over one batch of synthetic logits:
   ``--seq-level``, the sequence-level form (``selective_log_softmax_fwd``,
   ``grpo_seq_terms``, ``selective_log_softmax_bwd``); with ``--vocab-shards S``, the
   vocabulary-parallel form with its S shards run one after another.  The same line
-  carries ``entropy``: ``entropy_from_logits`` timed alone over the same logits.
+  carries ``entropy``: ``entropy_from_logits`` timed alone over the same logits, and (for
+  the fwd + bwd step) ``fused``: ``grpo_loss_fused`` timed alone over the same batch, with
+  its rows/s over the step's.
 * ``entropy_slsm_b16_l4096_v32000``: ``entropy_from_logits``, ``selective_log_softmax_fwd``
   and ``selective_log_softmax_bwd``; with ``--entropy-bwd``, ``entropy_from_logits`` (with
   lse) and ``entropy_from_logits_bwd``.
@@ -1157,6 +1159,47 @@ def entropy_run(step, K, Wm, flush_buf, peak):
             "dram_frac": None if traffic is None else round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}
 
 
+def fused_run(step, K, Wm, flush_buf, peak, step_ms):
+    """grpo_loss_fused over the same batch as the fwd + bwd step (the same inputs, dloss
+    known in advance, outputs and dlogits into the step's own buffers): Wm untimed
+    launches, then K launches with L2 flushed before each and CUDA events around each, on
+    the launching stream.  `vs_fwd_bwd_rows` is the step's time over this kernel's, i.e.
+    its rows/s over the fwd + bwd step's."""
+    lib = rp.load_library()
+    spec, inp, o = step.spec, step.inp, step.out
+    R = spec.rows
+    args = (ctypes.byref(step.x_desc), _p(inp.idx), _p(step.old), _p(step.ref), _p(inp.adv), _p(inp.mask),
+            _p(inp.dloss), spec.T, spec.beta, spec.eps_low, spec.eps_high, _p(o["loss"]), _p(o["logp"]),
+            _p(o["lse"]), _p(o["kl"]), _p(o["is_clipped"]), _p(o["entropy"]), ctypes.byref(step.dx_desc), None,
+            step.stream)
+
+    def call():
+        st = lib.grpo_loss_fused(*args)
+        if st:
+            raise rp.GrpoError("grpo_loss_fused", st)
+
+    for i in range(Wm):
+        flush_buf(i)
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush_buf(i + 1)
+        ev[i][0].record()
+        call()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    live = np.ones(R, bool) if inp.mask is None else inp.mask.bool().cpu().numpy()
+    nbytes = int(fused_row_bytes(spec, live, inp.mask is not None, step.old is not None, step.ref is not None).sum())
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    traffic = measured_traffic("grpo_loss_fused", spec)
+    return {"kernel": "grpo_loss_fused", "value": round(gbs, 2), "unit": "GB/s", "ms": round(ms, 5),
+            "bytes": nbytes, "rows_per_s": round(R / (ms * 1e-3), 1), "hbm_frac": round(gbs / peak, 4),
+            "vs_fwd_bwd_rows": round(step_ms / ms, 4), "launches": K, "traffic": traffic,
+            "dram_frac": None if traffic is None else round(traffic / (ms * 1e-3) / 1e9 / peak, 4)}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -1618,9 +1661,11 @@ def main(argv=None):
                        "ranges of one sequence for the token-level passes), the logits copied in, the kernels and "
                        "the outputs copied out per part on three streams"}
 
-    ent = None
+    ent = fus = None
     if step_kind(args, spec) == "grpo" and not args.vocab_shards:
         ent = entropy_run(step, K, Wm, flush_buf, peak)
+        if not args.fused:  # the same batch through the single-read kernel, beside the fwd + bwd step
+            fus = fused_run(step, K, Wm, flush_buf, peak, step_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1643,7 +1688,7 @@ def main(argv=None):
                          "source_hash": kernel_source_hash(dom) if dom in KERNEL_UNITS else None,
                          "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": int(per_launch[dom])},
-            "cpu_baseline": cpu, "e2e": e2e, "entropy": ent,
+            "cpu_baseline": cpu, "e2e": e2e, "entropy": ent, "fused": fus,
             "gpu_launches": getattr(step, "launches_per_step", len(step.kernels)) * K,
             "gpu_launches_note": "in the headline pass (the per-kernel pass launches as many again)",
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
