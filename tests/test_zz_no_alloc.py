@@ -26,7 +26,9 @@ def lib():
     return rp.load_library()
 
 
-def inputs(seed, B=2, L=21, H=64, V=1003):
+def inputs(seed, B=2, L=21, H=64, V=1003, T=0.9):
+    """Seeded inputs; old / ref sit near the oracle's logp of h W^T (old within about 0.3,
+    ref 0.1), so that rows fall on both sides of the clip range and the KL term is live."""
     g = torch.Generator().manual_seed(seed)
     R = B * L
     h = torch.randn(R, H, generator=g).to(torch.bfloat16)
@@ -35,11 +37,12 @@ def inputs(seed, B=2, L=21, H=64, V=1003):
     adv = torch.randn(B, generator=g).float()
     mask = (torch.rand(R, generator=g) > 0.2).to(torch.uint8)
     dloss = (torch.rand(R, generator=g) + 0.1).float() * mask.float()
-    old = -6.0 + 0.3 * torch.randn(R, generator=g).float()
-    ref = -6.0 + 0.3 * torch.randn(R, generator=g).float()
+    lp, _ = oracle.selective_log_softmax(rows_f64(h) @ rows_f64(W).T, idx.numpy(), T)
+    old = torch.from_numpy(oracle.round_to_fp32(lp + 0.3 * torch.randn(R, generator=g).double().numpy())).float()
+    ref = torch.from_numpy(oracle.round_to_fp32(lp + 0.1 * torch.randn(R, generator=g).double().numpy())).float()
     d = lambda t: t.to(DEV)
     return dict(h=d(h), W=d(W), idx=d(idx), adv=d(adv), mask=d(mask), dloss=d(dloss), old=d(old), ref=d(ref),
-                B=B, L=L, H=H, V=V, T=0.9, beta=0.04, el=0.2, eh=0.28)
+                B=B, L=L, H=H, V=V, T=T, beta=0.04, el=0.2, eh=0.28)
 
 
 def call_noalloc(lib, x, chunk):
