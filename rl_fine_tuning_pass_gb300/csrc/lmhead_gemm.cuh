@@ -28,13 +28,13 @@
 // of the finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes of its
 // quarter; two warps share a quarter, one for each half of the columns) while the MMAs of
 // the next tile fill the other accumulator.  Each warp passes its 32 x 32 boxes through a
-// swizzled staging buffer (one row per lane in).  kEpiLogits and kEpiStore read them back out
-// as whole row segments (eight 16-bit rows of 64 bytes or four fp32 rows of 128 bytes per
-// instruction) for coalesced global stores, which are fire-and-forget, so many lines per SM
-// are in flight.  kEpiAccum hands each box to a TMA reduce-add (the buffer's swizzle is the
-// tensor map's), one instruction where 16 vector reduce-adds per lane were; the fewer
-// instructions the epilogue warps issue, the less they slow the MMA thread that shares an SM
-// sub-partition with two of them.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
+// swizzled staging buffer (one row per lane in).  kEpiStore reads them back out as whole row
+// segments (four fp32 rows of 128 bytes per instruction) for coalesced global stores, which are
+// fire-and-forget, so many lines per SM are in flight.  kEpiLogits hands each 16-bit box to a
+// TMA store and kEpiAccum each fp32 box to a TMA reduce-add (the buffer's swizzle is the
+// tensor map's), one instruction where a lane's shared loads and global stores (or 16 vector
+// reduce-adds) were; the fewer instructions the epilogue warps issue, the less they slow the
+// MMA thread that shares an SM sub-partition with two of them.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
 // grad_hidden) or MN-major (M or N contiguous: W in grad_hidden, dlogits^T and h in
 // grad_weight); the MN-major tiles are loaded as 64-wide boxes and described to the MMA
 // with the MN-major bit.
@@ -154,6 +154,18 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// Store the 32 x 32 16-bit box at shared address `src` (64-byte rows, the map's 64-byte swizzle)
+// to the tensor at box coordinates (x, y); rows and columns outside the tensor are left out.
+// One bulk group per call.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most one bulk group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // No bulk group of this thread still reading shared memory / none still in flight.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -375,7 +387,8 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {  // a, b already
 
 // Row `lane` of a warp's 32 x 32 box of exponentials, as fp16, into its staging buffer (64
 // bytes a row): the 16-byte chunk q of row r sits at chunk q ^ ((r / 2) % 4), so the eight
-// rows a quarter-warp writes at once cover all 32 banks.
+// rows a quarter-warp writes at once cover all 32 banks.  This is the TMA's 64-byte swizzle
+// (address bits 4-5 XOR bits 7-8), so the buffer goes out as one tensor store.
 __device__ __forceinline__ void stage_row_h16(uint32_t buf, int lane, const float (&v)[32]) {
   const uint32_t row = buf + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
@@ -385,34 +398,6 @@ __device__ __forceinline__ void stage_row_h16(uint32_t buf, int lane, const floa
     const uint32_t dst = row + static_cast<uint32_t>((q ^ ((lane >> 1) & 3)) * 16);
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
                  : "memory");
-  }
-}
-
-// Write a staged 32 x 32 box of 16-bit values to rows [0, rows) and columns [0, cols) of the
-// 16-bit matrix at `dst` (row stride ld elements, a multiple of 8): lane l takes 16-byte chunk l % 4 of rows
-// l / 4 + 8 i, so each instruction covers eight whole 64-byte row segments.
-__device__ __forceinline__ void write_box_h16(uint32_t buf, int lane, uint16_t* dst, int64_t ld, int rows,
-                                               int cols) {
-  const int q = lane & 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 8 * i + (lane >> 2);
-    uint4 w;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                 : "r"(buf + static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) * 16))));
-    if (r >= rows || 8 * q >= cols) continue;
-    uint16_t* d = dst + r * ld + 8 * q;
-    if (8 * q + 8 <= cols) {
-      *reinterpret_cast<uint4*>(d) = w;
-    } else {
-      const uint32_t e[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (8 * q + k >= cols) break;
-        d[k] = static_cast<uint16_t>(e[k >> 1] >> (16 * (k & 1)));
-      }
-    }
   }
 }
 
@@ -455,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
-    if (EPI == kEpiAccum) prefetch_tensormap(&tmC);
+    if (EPI == kEpiAccum || EPI == kEpiLogits) prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -574,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t buf = smem_addr(sC) + static_cast<uint32_t>(warp - 2) * kStageC;
+    uint32_t nbox = 0;  // kEpiLogits: boxes this warp has stored (they alternate between two 2 KB halves)
     int local = 0;
     for (int t = first; t < total; t += step, ++local) {
       const Tile u = tile_of(p, dims, t);
@@ -608,16 +594,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float shift = (m == -INFINITY ? 0.f : st_a) - kExpScaleLog2;
         const float2 c2 = make_float2(p.c, p.c), na2 = make_float2(-shift, -shift);
         float2 s2 = make_float2(0.f, 0.f), u2 = make_float2(0.f, 0.f);
-        uint16_t* eb = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row0) * p.ldc;
 #pragma unroll
         for (int j = 0; j < BN / 64; ++j) {
           if (j >= boxes) break;
           const int col0 = col_base + 32 * j;
           box_exp<kH>(v[j], p.N - col0, c2, na2, s2, u2);
-          stage_row_h16(buf, lane, v[j]);
+          const uint32_t hb = buf + (nbox & 1u) * 2048u;
+          if (lane == 0) bulk_wait_read1();  // the store before the last one has read this half
           __syncwarp();
-          write_box_h16(buf, lane, eb + col0, p.ldc, dims.M - row0, p.N - col0);
-          __syncwarp();  // every lane has read the box before the next one is staged
+          stage_row_h16(hb, lane, v[j]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) tma_store_2d(&tmC, hb, col0, row0);
+          ++nbox;
         }
         if (row_ok && col_base < p.N) {
           const float2 su = tile_sums(s2, u2);
@@ -652,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (EPI == kEpiAccum && warp >= 2 && lane == 0) bulk_wait_all();  // the reduce-adds are done
+  if ((EPI == kEpiAccum || EPI == kEpiLogits) && warp >= 2 && lane == 0) bulk_wait_all();  // stores / adds done
   __syncthreads();
   tc_fence_before();
   cluster_sync();  // neither CTA leaves while the other's copies, MMAs or arrivals may target it
@@ -761,6 +750,18 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params
   cfg.gridDim = dim3(static_cast<unsigned>(2 * (total < pairs ? total : pairs)));
   // kEpiAccum: the output's tensor map, 32 x 32 fp32 boxes with the staging buffer's swizzle
   CUtensorMap c{};
+  if (EPI == kEpiLogits) {  // 32 x 32 boxes of the 16-bit exponentials, 64-byte swizzle (the staging's)
+    const TensorMapEncodeFn enc = tensor_map_encoder();
+    if (enc == nullptr || p.ldc % 8 != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ldc) * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    if (enc(&c, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.C, dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   if (EPI == kEpiAccum) {
     const TensorMapEncodeFn enc = tensor_map_encoder();
     if (enc == nullptr || p.ldc % 4 != 0) return cudaErrorInvalidValue;
