@@ -28,11 +28,10 @@
 // of the finished accumulator back with tcgen05.ld (a warp reaches the 32 TMEM lanes of its
 // quarter; two warps share a quarter, one for each half of the columns) while the MMAs of
 // the next tile fill the other accumulator.  Each warp passes its 32 x 32 boxes through a
-// swizzled staging buffer (one row per lane in).  kEpiStore reads them back out as whole row
-// segments (four fp32 rows of 128 bytes per instruction) for coalesced global stores, which are
-// fire-and-forget, so many lines per SM are in flight.  kEpiLogits hands each 16-bit box to a
-// TMA store and kEpiAccum each fp32 box to a TMA reduce-add (the buffer's swizzle is the
-// tensor map's), one instruction where a lane's shared loads and global stores (or 16 vector
+// swizzled staging buffer (one row per lane in) and hands it to the TMA: kEpiLogits (16-bit
+// boxes, 64-byte swizzle) and kEpiStore (fp32 boxes, 128-byte swizzle, one split per z) by a
+// tensor store, kEpiAccum by a tensor reduce-add (the buffer's swizzle is the tensor map's).
+// That is one instruction where a lane's shared loads and global stores (or 16 vector
 // reduce-adds) were; the fewer instructions the epilogue warps issue, the less they slow the
 // MMA thread that shares an SM sub-partition with two of them.  Operands may be K-major (K contiguous: h, W in the logits GEMM, dlogits in
 // grad_hidden) or MN-major (M or N contiguous: W in grad_hidden, dlogits^T and h in
@@ -161,6 +160,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Store the 32 x 32 fp32 box at shared address `src` (128-byte rows, the map's 128-byte swizzle)
+// to split z of the tensor at box coordinates (x, y); rows and columns outside are left out.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -297,33 +305,6 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int lane, const float (&
   }
 }
 
-// Write a staged 32 x 32 box to rows [0, rows) and columns [0, cols) of the fp32 matrix at
-// `dst` (row stride ld, a multiple of 4): lane l takes 16-byte chunk l % 8 of rows
-// l / 8 + 4 i, so each instruction covers four whole 128-byte rows.
-__device__ __forceinline__ void write_box(uint32_t buf, int lane, float* dst, int64_t ld, int rows, int cols) {
-  const int q = lane & 7;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + (lane >> 3);
-    float4 x;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                 : "r"(buf + static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) * 16))));
-    if (r >= rows || 4 * q >= cols) continue;
-    float* d = dst + r * ld + 4 * q;
-    if (4 * q + 4 <= cols) {
-      *reinterpret_cast<float4*>(d) = x;
-    } else {
-      const float e[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (4 * q + k >= cols) break;
-        d[k] = e[k];
-      }
-    }
-  }
-}
-
 // The logits epilogue's statistic over one row's 128 columns of the tile (the first `cols`
 // of them inside the matrix): the maximum m (tile_max), then, box by box, e_j = 2^(x_j c - a)
 // with a = m c, and s = sum e_j, u = sum e_j (x_j c - a) (box_exp).  Columns at or past N get
@@ -440,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
-    if (EPI == kEpiAccum || EPI == kEpiLogits) prefetch_tensormap(&tmC);
+    prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -574,7 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * BN + half * (BN / 2));
       const int col_base = u.n * BN + half * (BN / 2);
-      float* cbase = p.C + static_cast<int64_t>(u.s) * p.split_stride;
       const int boxes = min(BN / 64, (p.N - col_base + 31) / 32);  // boxes with columns below N
       // all of this warp's 128 accumulator columns into registers with one wait, then the
       // accumulator goes back to the MMA while the statistic and the stores proceed
@@ -628,20 +608,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) tma_reduce_add_2d(&tmC, buf, col0, row0);
         }
       } else {
+        // each 32 x 32 box staged (128-byte swizzle, the tensor map's) and stored to split u.s
+        // by one TMA store; the buffer is restaged only once the previous store has read it
 #pragma unroll
         for (int j = 0; j < BN / 64; ++j) {
           if (j >= boxes) break;
           const int col0 = col_base + 32 * j;
-          stage_row(buf, lane, v[j]);
+          if (lane == 0) bulk_wait_read0();
           __syncwarp();
-          write_box(buf, lane, cbase + static_cast<int64_t>(row0) * p.ldc + col0, p.ldc, dims.M - row0,
-                         p.N - col0);
-          __syncwarp();  // every lane has read the box before the next one is staged
+          stage_row(buf, lane, v[j]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.M) tma_store_3d(&tmC, buf, col0, row0, u.s);
         }
       }
     }
   }
-  if ((EPI == kEpiAccum || EPI == kEpiLogits) && warp >= 2 && lane == 0) bulk_wait_all();  // stores / adds done
+  if (warp >= 2 && lane == 0) bulk_wait_all();  // the epilogue's stores / adds are done
   __syncthreads();
   tc_fence_before();
   cluster_sync();  // neither CTA leaves while the other's copies, MMAs or arrivals may target it
@@ -759,6 +742,21 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params
     const cuuint32_t elem_strides[2] = {1, 1};
     if (enc(&c, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.C, dims, strides, box, elem_strides,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (EPI == kEpiStore) {  // [splits][M][ldc] fp32, 32 x 32 boxes with the staging buffer's swizzle
+    const TensorMapEncodeFn enc = tensor_map_encoder();
+    if (enc == nullptr || p.ldc % 4 != 0) return cudaErrorInvalidValue;
+    const int64_t zs = p.splits > 1 ? p.split_stride : p.ldc * p.M;
+    if (zs % 4 != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M),
+                                static_cast<cuuint64_t>(p.splits)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.ldc) * 4, static_cast<cuuint64_t>(zs) * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    if (enc(&c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.C, dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
